@@ -1,0 +1,180 @@
+"""FP64 CPU oracle for the forward 2D convolution -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  The CUDA
+library never calls it and shares no code with it.
+
+The arithmetic lives in ``conv_oracle.c`` (plain seven-loop FP64 nest, OpenMP
+over (n, co)); this module compiles it with gcc on first use and marshals
+numpy arrays into it through ctypes.  What it computes, with the passages it
+follows, is stated at the top of ``conv_oracle.c``:
+
+* dot-product definition and index map: "GPU lesson 9: how a GPU executes
+  neural-network convolution" (lincklin.cn), section 2;
+* zero padding by address predicate: lesson 9, section 26;
+* dilation, effective kernel, output size, groups: "Convolution variants and
+  their matrix operations" (lpnh.cn/news/2674933), sections 2.2, 2.3, 4.2,
+  4.3, 6.2;
+* bias after the sum, then ReLU: lesson 9, section 31.
+
+Every function here is pinned by ``tests/test_oracle.py`` against values the
+pages print, closed forms, and two independent restatements.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "conv_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("N", "C_in", "H", "W", "C_out", "Kh", "Kw", "S", "P", "D", "G", "relu")] + \
+               [(n, ctypes.c_int64) for n in
+                ("xs_n", "xs_c", "xs_h", "xs_w", "ws_o", "ws_i", "ws_h", "ws_w",
+                 "ys_n", "ys_c", "ys_h", "ys_w")]
+
+
+def build(force: bool = False) -> str:
+    """Compile ``conv_oracle.c`` into ``liboracle.so`` beside it (gcc, -O2, OpenMP)."""
+    with _lock:
+        if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+            return _LIB
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        cmd = ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c99", "-o", tmp, _SRC]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+        return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P = ctypes.POINTER
+        lib.oracle_out_size.argtypes = [ctypes.c_int] * 5
+        lib.oracle_out_size.restype = ctypes.c_int
+        lib.oracle_conv2d_f64.argtypes = [P(_Desc), ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        lib.oracle_conv2d_f64.restype = ctypes.c_int
+        lib.oracle_conv2d_points_f64.argtypes = [P(_Desc), ctypes.c_void_p, ctypes.c_void_p,
+                                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                                 ctypes.c_void_p, ctypes.c_int]
+        lib.oracle_conv2d_points_f64.restype = ctypes.c_int
+        lib.oracle_conv2d_macs_at.argtypes = [P(_Desc), ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        lib.oracle_conv2d_macs_at.restype = ctypes.c_long
+        lib.oracle_max_threads.argtypes = []
+        lib.oracle_max_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def out_size(size: int, k: int, s: int, p: int, d: int) -> int:
+    """Output extent floor((size + 2p - d(k-1) - 1)/s) + 1, or 0 if the window never fits."""
+    return int(_load().oracle_out_size(size, k, s, p, d))
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+# Logical axis order: x/y (n, c, h, w); w (o, i, h, w).
+_ACT_LAYOUTS = {"NCHW": "nchw", "NHWC": "nhwc"}
+_W_LAYOUTS = {"OIHW": "oihw", "OHWI": "ohwi"}
+
+
+def _strides(arr: np.ndarray, layout: str, logical: str):
+    """Element strides of ``arr`` (C-contiguous in ``layout`` order) per logical axis."""
+    st = [s // arr.itemsize for s in arr.strides]
+    return [st[layout.index(a)] for a in logical]
+
+
+def _logical_shape(arr: np.ndarray, layout: str, logical: str):
+    return [arr.shape[layout.index(a)] for a in logical]
+
+
+def _desc(x, w, x_layout, w_layout, y_layout, stride, padding, dilation, groups, relu, y=None):
+    xl, wl = _ACT_LAYOUTS[x_layout], _W_LAYOUTS[w_layout]
+    N, C_in, H, W = _logical_shape(x, xl, "nchw")
+    C_out, Cin_g, Kh, Kw = _logical_shape(w, wl, "oihw")
+    if Cin_g * groups != C_in:
+        raise ValueError("weight input-channel extent %d x groups %d != C_in %d" % (Cin_g, groups, C_in))
+    d = _Desc()
+    d.N, d.C_in, d.H, d.W, d.C_out = N, C_in, H, W, C_out
+    d.Kh, d.Kw, d.S, d.P, d.D, d.G = Kh, Kw, stride, padding, dilation, groups
+    d.relu = 1 if relu else 0
+    d.xs_n, d.xs_c, d.xs_h, d.xs_w = _strides(x, xl, "nchw")
+    d.ws_o, d.ws_i, d.ws_h, d.ws_w = _strides(w, wl, "oihw")
+    if y is not None:
+        d.ys_n, d.ys_c, d.ys_h, d.ys_w = _strides(y, _ACT_LAYOUTS[y_layout], "nchw")
+    return d
+
+
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def conv2d(x, w, bias=None, stride=1, padding=0, dilation=1, groups=1, relu=False,
+           x_layout="NCHW", w_layout="OIHW", y_layout="NCHW", nthreads=0):
+    """Full FP64 output of the convolution (see module docstring).
+
+    ``x`` is given in ``x_layout`` ("NCHW" or "NHWC"), ``w`` in ``w_layout``
+    ("OIHW" = [C_out][C_in/G][Kh][Kw], or "OHWI" = [C_out][Kh][Kw][C_in/G]),
+    ``bias`` is [C_out] or None.  The result is returned in ``y_layout``.
+    """
+    lib = _load()
+    x, w = _f64(x), _f64(w)
+    b = None if bias is None else _f64(bias)
+    xl = _ACT_LAYOUTS[x_layout]
+    N, C_in, H, W = _logical_shape(x, xl, "nchw")
+    C_out, _, Kh, Kw = _logical_shape(w, _W_LAYOUTS[w_layout], "oihw")
+    Ho = out_size(H, Kh, stride, padding, dilation)
+    Wo = out_size(W, Kw, stride, padding, dilation)
+    if Ho <= 0 or Wo <= 0:
+        raise ValueError("empty output (H_out=%d, W_out=%d)" % (Ho, Wo))
+    shape = {"NCHW": (N, C_out, Ho, Wo), "NHWC": (N, Ho, Wo, C_out)}[y_layout]
+    y = np.empty(shape, dtype=np.float64)
+    d = _desc(x, w, x_layout, w_layout, y_layout, stride, padding, dilation, groups, relu, y)
+    rc = lib.oracle_conv2d_f64(ctypes.byref(d), x.ctypes.data, w.ctypes.data,
+                               None if b is None else b.ctypes.data, y.ctypes.data, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected the convolution descriptor")
+    return y
+
+
+def conv2d_points(x, w, bias, pts, stride=1, padding=0, dilation=1, groups=1, relu=False,
+                  x_layout="NCHW", w_layout="OIHW", nthreads=0):
+    """FP64 values at selected outputs; ``pts`` is an int array [npts, 4] of (n, co, ho, wo)."""
+    lib = _load()
+    x, w = _f64(x), _f64(w)
+    b = None if bias is None else _f64(bias)
+    pts = np.ascontiguousarray(pts, dtype=np.int64).reshape(-1, 4)
+    out = np.empty(pts.shape[0], dtype=np.float64)
+    d = _desc(x, w, x_layout, w_layout, "NCHW", stride, padding, dilation, groups, relu)
+    rc = lib.oracle_conv2d_points_f64(ctypes.byref(d), x.ctypes.data, w.ctypes.data,
+                                      None if b is None else b.ctypes.data, pts.ctypes.data,
+                                      pts.shape[0], out.ctypes.data, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected the descriptor or a point")
+    return out
+
+
+def macs_at(x, w, n, co, ho, wo, stride=1, padding=0, dilation=1, groups=1,
+            x_layout="NCHW", w_layout="OIHW"):
+    """Number of multiply terms the oracle takes for output (n, co, ho, wo)."""
+    lib = _load()
+    x, w = _f64(x), _f64(w)
+    d = _desc(x, w, x_layout, w_layout, "NCHW", stride, padding, dilation, groups, False)
+    return int(lib.oracle_conv2d_macs_at(ctypes.byref(d), x.ctypes.data, w.ctypes.data,
+                                         n, co, ho, wo))

@@ -1,0 +1,317 @@
+"""Pins for the FP64 oracle (CPU only).
+
+Each test ties the oracle to something other than itself: numbers the pages
+print (tests/golden/), closed forms, identities the pages state (1x1 conv is a
+GEMM, grouped conv is G independent convs, dilation is a zero-inserted dense
+kernel), and two independent restatements on small random shapes (torch's
+float64 CPU conv2d and a numpy explicit-im2col GEMM).
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from workloads import ConvShape, random_shape
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def conv(x, w, b=None, s=1, p=0, d=1, g=1, relu=False):
+    return oracle.conv2d(x, w, b, stride=s, padding=p, dilation=d, groups=g, relu=relu)
+
+
+# ----------------------------------------------------------------- im2col restatement
+def im2col_gemm(x, w, b, s, p, d, g, relu):
+    """Explicit im2col + matmul per group (lesson 9 sections 7-8; variants page 3.1),
+    written independently of the oracle: pad with zeros, gather each window
+    column by slicing, multiply by the flattened kernel."""
+    N, C, H, W = x.shape
+    Co, Cg, Kh, Kw = w.shape
+    Ho = (H + 2 * p - d * (Kh - 1) - 1) // s + 1
+    Wo = (W + 2 * p - d * (Kw - 1) - 1) // s + 1
+    xp = np.zeros((N, C, H + 2 * p, W + 2 * p))
+    xp[:, :, p:p + H, p:p + W] = x
+    out = np.zeros((N, Co, Ho, Wo))
+    cog = Co // g
+    for n in range(N):
+        for gi in range(g):
+            cols = np.zeros((Cg * Kh * Kw, Ho * Wo))
+            r = 0
+            for c in range(Cg):
+                for kh in range(Kh):
+                    for kw in range(Kw):
+                        patch = xp[n, gi * Cg + c,
+                                   kh * d: kh * d + s * (Ho - 1) + 1: s,
+                                   kw * d: kw * d + s * (Wo - 1) + 1: s]
+                        cols[r] = patch.reshape(-1)
+                        r += 1
+            wm = w[gi * cog:(gi + 1) * cog].reshape(cog, -1)
+            out[n, gi * cog:(gi + 1) * cog] = (wm @ cols).reshape(cog, Ho, Wo)
+    if b is not None:
+        out += b[None, :, None, None]
+    if relu:
+        out = np.maximum(out, 0.0)
+    return out
+
+
+# ----------------------------------------------------------------- 1. lesson 9 worked example
+def test_lesson9_im2col_worked_example():
+    """3x3 input a..i, 2x2 kernel, stride 1 (lesson 9, section 8).  With a one-hot
+    kernel at tap t the oracle's four outputs are column t of the printed X_col."""
+    lines = [l.split() for l in open(os.path.join(GOLDEN, "lesson9_im2col_2x2.txt"))
+             if l.strip() and not l.startswith("#")]
+    letters = lines[0][1:]
+    val = {ch: float(i + 1) for i, ch in enumerate(letters)}
+    xcol = np.array([[val[ch] for ch in l[2:]] for l in lines[1:]])
+    assert xcol.shape == (4, 4)
+    assert np.array_equal(xcol, xcol.T)  # the printed matrix is symmetric
+    x = np.array([val[ch] for ch in letters]).reshape(1, 1, 3, 3)
+    for t in range(4):
+        w = np.zeros((1, 1, 2, 2))
+        w[0, 0, t // 2, t % 2] = 1.0
+        y = conv(x, w)
+        assert y.shape == (1, 1, 2, 2)
+        assert np.array_equal(y.reshape(-1), xcol[:, t])
+    # the full X_col also comes out of the independent restatement
+    w = np.arange(1, 5, dtype=float).reshape(1, 1, 2, 2)
+    assert np.array_equal(conv(x, w).reshape(-1), xcol @ w.reshape(-1))
+
+
+# ----------------------------------------------------------------- 2. variants page 4x4 example
+def test_variants_4x4_example(facts):
+    """1x4x4 input, 3x3 kernel, S1 P0 -> 2x2 output; X_col is 9x4 (variants page 3.1)."""
+    rng = np.random.default_rng(1)
+    n_in, n_out = facts["small_in"], facts["small_out"]
+    x = rng.standard_normal((1, 1, n_in, n_in))
+    assert oracle.out_size(n_in, 3, 1, 0, 1) == n_out
+    xcol = np.zeros((facts["small_xcol_rows"], facts["small_xcol_cols"]))
+    for t in range(9):
+        w = np.zeros((1, 1, 3, 3))
+        w[0, 0, t // 3, t % 3] = 1.0
+        xcol[t] = conv(x, w).reshape(-1)
+    # each column is one window, flattened row-major
+    for j in range(4):
+        ho, wo = divmod(j, 2)
+        assert np.array_equal(xcol[:, j], x[0, 0, ho:ho + 3, wo:wo + 3].reshape(-1))
+
+
+# ----------------------------------------------------------------- 3. MAC counts
+@pytest.mark.parametrize("cin,key", [(3, "macs_3x3_cin3"), (64, "macs_3x3_cin64"),
+                                     (256, "macs_3x3_cin256")])
+def test_mac_counts_interior(cin, key, facts):
+    x = np.ones((1, cin, 6, 6))
+    w = np.ones((2, cin, 3, 3))
+    assert oracle.macs_at(x, w, 0, 1, 2, 3, padding=1) == facts[key]
+
+
+def test_mac_counts_groups_depthwise_borders():
+    x = np.ones((1, 8, 7, 7))
+    # grouped: (C_in/G) * K^2 per output
+    w = np.ones((4, 2, 3, 3))
+    assert oracle.macs_at(x, w, 0, 3, 3, 3, padding=1, groups=4) == 2 * 9
+    # depthwise: one channel per output, 9 taps
+    w = np.ones((8, 1, 3, 3))
+    assert oracle.macs_at(x, w, 0, 5, 3, 3, padding=1, groups=8) == 9
+    # zero padding skips taps: corner 4, edge 6
+    w = np.ones((1, 8, 3, 3))
+    assert oracle.macs_at(x, w, 0, 0, 0, 0, padding=1) == 4 * 8
+    assert oracle.macs_at(x, w, 0, 0, 0, 3, padding=1) == 6 * 8
+    # dilation: still 9 live taps, never the 25 of the 5x5 window
+    assert oracle.macs_at(x, w, 0, 0, 3, 3, padding=2, dilation=2) == 9 * 8
+
+
+# ----------------------------------------------------------------- 4. shapes
+def test_stem_shape(facts):
+    n = facts["stem_in"]
+    assert oracle.out_size(n, 3, 2, 1, 1) == facts["stem_out"]
+    x = np.zeros((1, 3, n, n))
+    w = np.zeros((facts["stem_cout"], 3, 3, 3))
+    assert conv(x, w, s=2, p=1).shape == (1, facts["stem_cout"], facts["stem_out"], facts["stem_out"])
+
+
+def test_output_size_sweep_against_torch():
+    for H in range(1, 12):
+        for K in (1, 2, 3, 5):
+            for S in (1, 2, 3):
+                for P in range(0, 4):
+                    for D in (1, 2, 3):
+                        ho = oracle.out_size(H, K, S, P, D)
+                        keff = K + (K - 1) * (D - 1)
+                        # dilation only widens the window: same size as the dense K_eff kernel
+                        assert ho == oracle.out_size(H, keff, S, P, 1)
+                        if H + 2 * P < keff:
+                            assert ho == 0
+                            continue
+                        t = F.conv2d(torch.zeros(1, 1, H, H), torch.zeros(1, 1, K, K),
+                                     stride=S, padding=P, dilation=D)
+                        assert ho == t.shape[-1]
+
+
+def test_dilated_effective_kernel(facts):
+    k, d = facts["dilated_k"], facts["dilated_d"]
+    assert k + (k - 1) * (d - 1) == facts["dilated_k_eff"]
+    assert oracle.out_size(64, k, 1, 2, d) == 64
+    x = np.ones((1, 1, 9, 9))
+    w = np.ones((1, 1, k, k))
+    assert oracle.macs_at(x, w, 0, 0, 4, 4, padding=2, dilation=d) == facts["dilated_live_taps"]
+
+
+# ----------------------------------------------------------------- 5. 1x1 == GEMM
+def test_1x1_is_gemm():
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((2, 16, 5, 7))
+    w = rng.standard_normal((12, 16, 1, 1))
+    y = conv(x, w)
+    ref = np.einsum("oc,nchw->nohw", w[:, :, 0, 0], x)
+    gemm = (w[:, :, 0, 0] @ x.transpose(1, 0, 2, 3).reshape(16, -1)).reshape(12, 2, 5, 7).transpose(1, 0, 2, 3)
+    assert np.allclose(y, gemm, rtol=1e-12, atol=1e-12)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------- 6. dilation == zero-inserted dense kernel
+def test_dilation_bit_equals_dense_kernel_with_zero_taps():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((2, 3, 11, 10))
+    w = rng.standard_normal((4, 3, 3, 3))
+    b = rng.standard_normal(4)
+    dense = np.zeros((4, 3, 5, 5))
+    dense[:, :, ::2, ::2] = w
+    y_d = conv(x, w, b, p=2, d=2)
+    y_dense = conv(x, dense, b, p=2, d=1)
+    assert y_d.shape == y_dense.shape == (2, 4, 11, 10)
+    assert np.array_equal(y_d, y_dense)
+
+
+# ----------------------------------------------------------------- 7. groups == independent convs
+@pytest.mark.parametrize("g", [2, 4, 8])
+def test_groups_bit_equal_independent_convs(g):
+    rng = np.random.default_rng(4 + g)
+    cin, cout = 8, 16
+    x = rng.standard_normal((2, cin, 7, 6))
+    w = rng.standard_normal((cout, cin // g, 3, 3))
+    b = rng.standard_normal(cout)
+    y = conv(x, w, b, s=2, p=1, g=g)
+    cg, og = cin // g, cout // g
+    for gi in range(g):
+        part = conv(x[:, gi * cg:(gi + 1) * cg], w[gi * og:(gi + 1) * og], b[gi * og:(gi + 1) * og], s=2, p=1)
+        assert np.array_equal(y[:, gi * og:(gi + 1) * og], part)
+
+
+def test_depthwise_is_per_channel():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((1, 6, 8, 8))
+    w = rng.standard_normal((6, 1, 3, 3))
+    y = conv(x, w, p=1, g=6)
+    for c in range(6):
+        assert np.array_equal(y[:, c:c + 1], conv(x[:, c:c + 1], w[c:c + 1], p=1))
+
+
+# ----------------------------------------------------------------- 8. closed forms
+def test_all_ones_input_closed_form():
+    """All-ones input with fixed weights (variants page 6.4): interior = sum(w) + b,
+    border = sum of the in-bounds taps + b."""
+    w = np.arange(1, 10, dtype=float).reshape(1, 1, 3, 3)
+    b = np.array([0.5])
+    y = conv(np.ones((1, 1, 5, 5)), w, b, p=1)[0, 0]
+    assert y[2, 2] == w.sum() + 0.5
+    assert y[0, 0] == w[0, 0, 1:, 1:].sum() + 0.5
+    assert y[0, 2] == w[0, 0, 1:, :].sum() + 0.5
+    assert y[4, 4] == w[0, 0, :2, :2].sum() + 0.5
+
+
+def test_zero_input_gives_relu_of_bias():
+    b = np.array([-1.5, 0.0, 2.25])
+    w = np.ones((3, 2, 3, 3))
+    y = conv(np.zeros((1, 2, 4, 4)), w, b, p=1)
+    assert np.all(y == b[None, :, None, None])
+    yr = conv(np.zeros((1, 2, 4, 4)), w, b, p=1, relu=True)
+    assert np.all(yr == np.maximum(b, 0)[None, :, None, None])
+
+
+def test_bias_before_relu():
+    # acc = -1, bias = +2: bias-then-ReLU gives 1; ReLU-then-bias would also give 1,
+    # so use acc = -3, bias = +2: bias-then-ReLU gives 0, ReLU-then-bias gives 2.
+    x = np.full((1, 1, 1, 1), -3.0)
+    w = np.ones((1, 1, 1, 1))
+    assert conv(x, w, np.array([2.0]), relu=True)[0, 0, 0, 0] == 0.0
+
+
+def test_translation_equivariance_interior():
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((1, 2, 12, 12))
+    w = rng.standard_normal((3, 2, 3, 3))
+    y = conv(x, w)
+    xs = np.roll(x, shift=(2, 1), axis=(2, 3))
+    ys = conv(xs, w)
+    assert np.allclose(ys[:, :, 2:, 1:], y[:, :, :-2, :-1], rtol=0, atol=0)
+
+
+# ----------------------------------------------------------------- 9. brute force vs two restatements
+def test_random_sweep_against_torch_and_im2col():
+    rng = np.random.default_rng(7)
+    for _ in range(150):
+        s = random_shape(rng, "f32")
+        x = rng.standard_normal((s.N, s.C_in, s.H, s.W))
+        w = rng.standard_normal((s.C_out, s.C_in // s.G, s.Kh, s.Kw))
+        b = rng.standard_normal(s.C_out) if s.bias else None
+        y = conv(x, w, b, s.S, s.P, s.D, s.G, s.relu)
+        t = F.conv2d(torch.from_numpy(x), torch.from_numpy(w),
+                     None if b is None else torch.from_numpy(b),
+                     stride=s.S, padding=s.P, dilation=s.D, groups=s.G)
+        if s.relu:
+            t = torch.relu(t)
+        r = im2col_gemm(x, w, b, s.S, s.P, s.D, s.G, s.relu)
+        assert y.shape == tuple(t.shape) == r.shape, s
+        scale = 1.0 + np.abs(y)
+        assert np.max(np.abs(y - t.numpy()) / scale) < 1e-12, s
+        assert np.max(np.abs(y - r) / scale) < 1e-12, s
+
+
+# ----------------------------------------------------------------- 10. im2col size arithmetic
+def test_body_layer_im2col_arithmetic(facts):
+    """112x112x128 -> 256 at 3x3 (variants page 3.3): X_col is (C_in*K*K) x (H_out*W_out)."""
+    s = ConvShape(1, 128, 112, 112, 256, 3, 3, 1, 1, 1, 1)
+    rows = s.C_in * s.Kh * s.Kw
+    cols = oracle.out_size(112, 3, 1, 1, 1) ** 2
+    assert rows == facts["body_xcol_rows"] and cols == facts["body_xcol_cols"]
+    # the page's "about 1447 x 10^4" is loose: 1152*12544 = 14,450,688
+    assert rows * cols / 1e4 == pytest.approx(facts["body_xcol_entries_wan"], rel=5e-3)
+    assert round(rows * cols * 4 / 2**20) == facts["body_xcol_mb"]
+    assert round(112 * 112 * 128 * 4 / 2**20, 1) == pytest.approx(facts["body_input_mb"], abs=0.3)
+    assert rows * cols // (112 * 112 * 128) == facts["body_inflation"]
+
+
+# ----------------------------------------------------------------- layout / points plumbing
+def test_nhwc_and_ohwi_layouts_bit_equal():
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((2, 6, 7, 5))
+    w = rng.standard_normal((4, 3, 3, 2))
+    b = rng.standard_normal(4)
+    y = oracle.conv2d(x, w, b, 2, 1, 2, 2, True)
+    y2 = oracle.conv2d(x.transpose(0, 2, 3, 1), w.transpose(0, 2, 3, 1), b, 2, 1, 2, 2, True,
+                       x_layout="NHWC", w_layout="OHWI", y_layout="NHWC")
+    assert np.array_equal(y, y2.transpose(0, 3, 1, 2))
+
+
+def test_points_bit_equal_full():
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((2, 4, 9, 9))
+    w = rng.standard_normal((6, 2, 3, 3))
+    b = rng.standard_normal(6)
+    y = oracle.conv2d(x, w, b, 1, 1, 1, 2, True)
+    pts = np.stack([rng.integers(0, 2, 50), rng.integers(0, 6, 50),
+                    rng.integers(0, 9, 50), rng.integers(0, 9, 50)], 1)
+    v = oracle.conv2d_points(x, w, b, pts, 1, 1, 1, 2, True)
+    assert np.array_equal(v, y[pts[:, 0], pts[:, 1], pts[:, 2], pts[:, 3]])
+    with pytest.raises(ValueError):
+        oracle.conv2d_points(x, w, b, np.array([[0, 6, 0, 0]]), 1, 1, 1, 2, True)
+
+
+def test_rejects_bad_descriptors():
+    with pytest.raises(ValueError):
+        oracle.conv2d(np.zeros((1, 3, 4, 4)), np.zeros((2, 2, 3, 3)), groups=1)
+    with pytest.raises(ValueError):
+        oracle.conv2d(np.zeros((1, 2, 2, 2)), np.zeros((2, 2, 5, 5)))  # empty output
