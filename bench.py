@@ -1,0 +1,355 @@
+"""Benchmark: forward conv2d on one GB300 through the library's C ABI.
+
+Headline workload: the body layer N=32, 128 -> 256 channels, 112x112, 3x3,
+stride 1, pad 1, BF16 in / FP32 accumulate / BF16 out, bias + ReLU fused
+(236.76 GFLOP per step).  One step = one conv_forward over the batch.  The
+depthwise half of the metric (FP32 depthwise 3x3, N=64, C=256, 56x56; GB/s) and
+the other layers are measured in the same run and reported beside it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (the
+forward pass needs no exchange between ranks); rank 0 prints the line with the
+max time over ranks and the aggregate throughput.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import WORKLOADS, b_device, inputs, w_device, x_device  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20   # twice the 129 MB L2
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def load_traffic():
+    """dram bytes per launch from the committed ncu summaries (profiles/*.md lines
+    'traffic_bytes_per_launch <workload> <bytes> <kernel-source-hash>')."""
+    out = {}
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return out
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith(".md"):
+            continue
+        for line in open(os.path.join(pdir, name)):
+            parts = line.strip().strip("`").split()
+            if len(parts) == 4 and parts[0] == "traffic_bytes_per_launch":
+                out[parts[1]] = (float(parts[2]), parts[3])
+    return out
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    cdir = os.path.join(ROOT, "cnn_convolution_implicit_gb300", "csrc")
+    for name in sorted(os.listdir(cdir)):
+        with open(os.path.join(cdir, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:12]
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- timing
+def time_steps(fn, steps, warmup, flush):
+    """Per-step CUDA-event time of fn() on the current stream, L2 flushed
+    between steps outside the events.  Returns (list of ms, launches per call)."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def gpu_layer(name):
+    """Device tensors + plan for a named workload."""
+    from cnn_convolution_implicit_gb300 import ConvPlan
+    s, x, w, b = inputs(name)
+    plan = ConvPlan.for_shape(s)
+    xd, wd = x_device(x, s.dtype), w_device(w, s.dtype)
+    bd = b_device(b) if s.bias else None
+    y = plan.empty_output()
+    return s, plan, (x, w, b), (xd, wd, bd, y)
+
+
+def measure_layer(name, steps, warmup, flush, peaks):
+    s, plan, host, (xd, wd, bd, y) = gpu_layer(name)
+
+    def step():
+        plan.forward(xd, wd, bd, y)
+
+    ms = time_steps(step, steps, warmup, flush)
+    t = float(np.mean(ms)) * 1e-3
+    tflops = s.flops / t / 1e12
+    gbs = s.algorithmic_bytes / t / 1e9
+    bound = "hbm" if s.flops / s.algorithmic_bytes < peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9) \
+        or s.dtype == "f32" else "tensor"
+    res = {"workload": name, "kernel": plan.path, "ms": t * 1e3, "tflops": tflops, "gbs": gbs,
+           "bound": bound, "flops": s.flops, "bytes": s.algorithmic_bytes, "launches": steps}
+    if bound == "tensor":
+        res["frac"] = tflops / peaks["bf16_tflops"]
+    else:
+        res["frac"] = gbs / peaks["hbm_gbs"]
+    return res, (s, plan, host, (xd, wd, bd, y))
+
+
+def oracle_sample(name, seconds_target=12.0):
+    """Time the FP64 oracle (as it stands) on a bounded sample of a workload's
+    outputs, on this host's cores.  Returns (TFLOP/s, GB/s-equivalent, threads, sample text)."""
+    import oracle
+    s, x, w, b = inputs(name)
+    rng = np.random.default_rng(77)
+    per_pt_flops = 2 * (s.C_in // s.G) * s.Kh * s.Kw
+
+    def pts(n):
+        return np.stack([rng.integers(0, s.N, n), rng.integers(0, s.C_out, n),
+                         rng.integers(0, s.H_out, n), rng.integers(0, s.W_out, n)], 1)
+
+    xf = np.ascontiguousarray(x, dtype=np.float64)
+    wf = np.ascontiguousarray(w, dtype=np.float64)
+    bf = None if b is None else np.ascontiguousarray(b, dtype=np.float64)
+    n = 2048
+    while True:
+        p = pts(n)
+        t0 = time.perf_counter()
+        oracle.conv2d_points(xf, wf, bf, p, s.S, s.P, s.D, s.G, s.relu)
+        dt = time.perf_counter() - t0
+        if dt > 1.0 or n >= 1 << 26:
+            break
+        n *= 4
+    n_final = max(n, int(n * seconds_target / max(dt, 1e-6)))
+    p = pts(n_final)
+    t0 = time.perf_counter()
+    oracle.conv2d_points(xf, wf, bf, p, s.S, s.P, s.D, s.G, s.relu)
+    dt = time.perf_counter() - t0
+    flops = per_pt_flops * n_final
+    frac_outputs = n_final / (s.pixels * s.C_out)
+    bytes_equiv = s.algorithmic_bytes * frac_outputs
+    sample = "%d seeded output points of %s (%.4f%% of the layer's outputs), FP64, %.1f s" % (
+        n_final, name, 100 * frac_outputs, dt)
+    return flops / dt / 1e12, bytes_equiv / dt / 1e9, oracle.max_threads(), sample, dt
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    peaks = load_peaks()
+    head = WORKLOADS["body"]
+    config = {"workload": "body conv N=32 128->256 112x112 3x3 s1 p1 bf16 bias+relu (NHWC)",
+              "global_batch": head.shape.N * world, "parallelism": "replicas x%d" % world,
+              "l2": "flushed between steps (256 MiB memset outside the timed events)",
+              "layout": "NHWC activations, [C_out][Kh][Kw][C_in] weights (conversion untimed)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        tf, _, cores, sample, _ = oracle_sample("body")
+        per_step = []
+        for _ in range(max(1, min(args.steps, 3))):
+            per_step.append(tf)
+        v = float(np.mean(per_step))
+        line = {"impl": "reference", "metric": "conv2d TFLOP/s (body 3x3 layer)", "value": v,
+                "unit": "TFLOP/s", "n_gpus": 0, "steps": len(per_step), "warmup": 0,
+                "higher_is_better": True, "dtype": "f64", "data": "synthetic (seeded)",
+                "config": config,
+                "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    # ---- headline: body layer, device-resident inputs
+    head_res, (s, plan, host, (xd, wd, bd, y)) = measure_layer("body", 3, 2, flush, peaks)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    try:
+        gpu_id = "GPU-%s" % torch.cuda.get_device_properties(local).uuid
+    except Exception:
+        gpu_id = str(local)
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    ms = time_steps(lambda: plan.forward(xd, wd, bd, y), args.steps, args.warmup, flush)
+    clk = clocks.stop()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t_step = float(np.mean(ms)) * 1e-3
+    t_total = float(np.sum(ms)) * 1e-3
+    if dist:
+        tt = torch.tensor([t_total], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_total = float(tt.item())
+        t_step = t_total / args.steps
+    value = s.flops * world / t_step / 1e12
+    kern_tflops = s.flops / t_step / 1e12
+
+    # ---- e2e through the public API with pinned host buffers
+    x_h = xd.cpu().pin_memory()
+    w_h = wd.cpu().pin_memory()
+    b_h = bd.cpu().pin_memory()
+    y_h = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    x_e, w_e, b_e, y_e = torch.empty_like(xd), torch.empty_like(wd), torch.empty_like(bd), torch.empty_like(y)
+
+    def e2e_step():
+        x_e.copy_(x_h, non_blocking=True)
+        w_e.copy_(w_h, non_blocking=True)
+        b_e.copy_(b_h, non_blocking=True)
+        plan.forward(x_e, w_e, b_e, y_e)
+        y_h.copy_(y_e, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    ms_e2e = time_steps(e2e_step, e2e_steps, 3, flush)
+    h2d = x_h.numel() * 2 + w_h.numel() * 2 + b_h.numel() * 4
+    d2h = y_h.numel() * 2
+    e2e = {"value": s.flops * world / (float(np.mean(ms_e2e)) * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": float(np.mean(ms_e2e))}
+
+    # ---- the other layers of the metric (depthwise GB/s first)
+    others = {}
+    for name in ("dw", "stem", "pw", "dilated"):
+        r, _ = measure_layer(name, max(10, args.steps // 2), args.warmup, flush, peaks)
+        others[name] = r
+
+    traffic = load_traffic()
+    src_hash = kernel_source_hash()
+    tr = traffic.get("body")
+    roofline = {"bound": "tensor", "achieved": kern_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": kern_tflops / peaks["bf16_tflops"],
+                "peak_source": "%s bf16_tflops (burst, kernel timed alone)" % peaks["source"],
+                "traffic": (tr[0] if tr and tr[1] == src_hash else None),
+                "kernel": "tc_conv_kernel (implicit GEMM, TMA im2col, tcgen05)",
+                "algorithmic_flops_per_launch": s.flops}
+    dwr = others["dw"]
+    trd = traffic.get("dw")
+    dw_roof = {"bound": "hbm", "achieved": dwr["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+               "frac": dwr["gbs"] / peaks["hbm_gbs"], "traffic": (trd[0] if trd and trd[1] == src_hash else None),
+               "kernel": "depthwise_kernel (TMA halo tile)", "algorithmic_bytes_per_launch": dwr["bytes"]}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        tf, _, cores, sample, _ = oracle_sample("body")
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {"metric": "conv2d TFLOP/s (body 3x3 layer, % of BF16 tensor peak); depthwise GB/s (% of HBM peak)",
+                "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs, Kaiming weights)",
+                "config": config, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": args.steps, "clocks": clk,
+                "depthwise": {"value": dwr["gbs"], "unit": "GB/s", "ms": dwr["ms"], "roofline": dw_roof,
+                              "workload": WORKLOADS["dw"].description},
+                "layers": others, "peaks": peaks, "kernel_source_hash": src_hash}
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,193 @@
+"""Thin ctypes binding over libconv.so (include/conv.h).
+
+Argument marshalling only: shapes, dtypes, device pointers and the CUDA
+stream are checked and passed through; every step of the convolution runs in
+the library's CUDA kernels.  PyTorch supplies device memory and streams.  There
+is no CPU path: if the library is missing or no GPU is present, calls fail.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libconv.so")
+
+CONV_F32, CONV_BF16 = 0, 1
+CONV_FLAG_BIAS, CONV_FLAG_RELU, CONV_FLAG_OUT_BF16 = 1, 2, 4
+STATUS = {0: "CONV_OK", 1: "CONV_ERR_INVALID_ARG", 2: "CONV_ERR_UNSUPPORTED", 3: "CONV_ERR_MISALIGNED",
+          4: "CONV_ERR_CUDA", 5: "CONV_ERR_NO_MEMORY", 6: "CONV_ERR_TIMEOUT"}
+PATHS = {0: "direct", 1: "depthwise", 2: "gemm_1x1", 3: "implicit_gemm", 4: "small_k_gemm"}
+
+# Every symbol include/conv.h declares.
+EXPORTS = ("conv_plan_create", "conv_plan_output_shape", "conv_plan_info", "conv_forward",
+           "conv_plan_destroy", "conv_status_string", "conv_device_status", "conv_plan_num_sms")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class ConvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s: %s (%s)" % (what, STATUS.get(status, str(status)), _status_text(status)))
+
+
+def _status_text(status: int) -> str:
+    try:
+        return lib().conv_status_string(status).decode()
+    except Exception:  # pragma: no cover - only while the library itself is broken
+        return "?"
+
+
+def lib():
+    """Load libconv.so (building it in-tree first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            from . import build as _build
+            if not _build.up_to_date():
+                _build.build()
+            L = ctypes.CDLL(LIB_PATH)
+            c_int, c_ll, vp = ctypes.c_int, ctypes.c_longlong, ctypes.c_void_p
+            L.conv_plan_create.argtypes = [ctypes.POINTER(vp)] + [c_int] * 11 + [c_int, ctypes.c_uint]
+            L.conv_plan_create.restype = c_int
+            L.conv_plan_output_shape.argtypes = [vp, ctypes.POINTER(c_int), ctypes.POINTER(c_int)]
+            L.conv_plan_output_shape.restype = c_int
+            L.conv_plan_info.argtypes = [vp, ctypes.POINTER(c_int), ctypes.POINTER(c_ll),
+                                         ctypes.POINTER(c_ll), ctypes.POINTER(c_ll)]
+            L.conv_plan_info.restype = c_int
+            L.conv_forward.argtypes = [vp, vp, vp, vp, vp, vp]
+            L.conv_forward.restype = c_int
+            L.conv_plan_destroy.argtypes = [vp]
+            L.conv_plan_destroy.restype = c_int
+            L.conv_status_string.argtypes = [c_int]
+            L.conv_status_string.restype = ctypes.c_char_p
+            L.conv_device_status.argtypes = [ctypes.POINTER(c_int)]
+            L.conv_device_status.restype = c_int
+            L.conv_plan_num_sms.argtypes = [vp]
+            L.conv_plan_num_sms.restype = c_int
+            _lib = L
+        return _lib
+
+
+def device_status() -> int:
+    """Synchronise the device and read/clear the library's timeout word (0 = clean)."""
+    code = ctypes.c_int(0)
+    st = lib().conv_device_status(ctypes.byref(code))
+    if st not in (0, 6):
+        raise ConvError(st, "conv_device_status")
+    return code.value
+
+
+class ConvPlan:
+    """A planned convolution: shapes fixed, pointers supplied per call.
+
+    Tensors are NHWC activations [N][H][W][C], weights [C_out][Kh][Kw][C_in/G]
+    and an FP32 bias [C_out].  dtype "bf16": BF16 x, w, y.  dtype "f32": FP32
+    x, w and FP32 y (BF16 y with out_bf16=True).
+    """
+
+    def __init__(self, N, C_in, H, W, C_out, Kh, Kw, S=1, P=0, D=1, G=1, dtype="bf16",
+                 bias=True, relu=False, out_bf16=False):
+        L = lib()
+        self._plan = None
+        flags = (CONV_FLAG_BIAS if bias else 0) | (CONV_FLAG_RELU if relu else 0) | \
+                (CONV_FLAG_OUT_BF16 if out_bf16 else 0)
+        dt = {"bf16": CONV_BF16, "f32": CONV_F32}[dtype]
+        h = ctypes.c_void_p()
+        st = L.conv_plan_create(ctypes.byref(h), N, C_in, H, W, C_out, Kh, Kw, S, P, D, G, dt, flags)
+        if st != 0:
+            raise ConvError(st, "conv_plan_create")
+        self._plan = h
+        self.shape = (N, C_in, H, W, C_out, Kh, Kw, S, P, D, G)
+        self.dtype, self.bias, self.relu, self.out_bf16 = dtype, bias, relu, out_bf16
+        ho, wo = ctypes.c_int(), ctypes.c_int()
+        L.conv_plan_output_shape(h, ctypes.byref(ho), ctypes.byref(wo))
+        self.H_out, self.W_out = ho.value, wo.value
+        path, m, n, k = ctypes.c_int(), ctypes.c_longlong(), ctypes.c_longlong(), ctypes.c_longlong()
+        L.conv_plan_info(h, ctypes.byref(path), ctypes.byref(m), ctypes.byref(n), ctypes.byref(k))
+        self.path = PATHS[path.value]
+        self.gemm_mnk = (m.value, n.value, k.value)
+        self.num_sms = L.conv_plan_num_sms(h)
+
+    @classmethod
+    def for_shape(cls, s):
+        """Plan from a workloads.ConvShape-like object."""
+        return cls(s.N, s.C_in, s.H, s.W, s.C_out, s.Kh, s.Kw, s.S, s.P, s.D, s.G, s.dtype,
+                   s.bias, s.relu, s.out_bf16)
+
+    def close(self):
+        if self._plan is not None and _lib is not None:
+            _lib.conv_plan_destroy(self._plan)
+        self._plan = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ------------------------------------------------------------------ torch side
+    def out_dtype(self):
+        import torch
+        return torch.bfloat16 if (self.dtype == "bf16" or self.out_bf16) else torch.float32
+
+    def empty_output(self, device="cuda"):
+        import torch
+        N, _, _, _, C_out = self.shape[:5]
+        return torch.empty((N, self.H_out, self.W_out, C_out), dtype=self.out_dtype(), device=device)
+
+    def forward(self, x, w, bias=None, y=None, stream=None):
+        """Launch on ``stream`` (default: torch's current stream); returns y."""
+        import torch
+        N, C_in, H, W, C_out, Kh, Kw, S, P, D, G = self.shape
+        dt = torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        if not (x.is_cuda and w.is_cuda):
+            raise ValueError("x and w must be CUDA tensors")
+        if x.dtype != dt or w.dtype != dt:
+            raise ValueError("x and w must be %s" % dt)
+        if tuple(x.shape) != (N, H, W, C_in) or not x.is_contiguous():
+            raise ValueError("x must be a contiguous NHWC tensor of shape %s" % ((N, H, W, C_in),))
+        if tuple(w.shape) != (C_out, Kh, Kw, C_in // G) or not w.is_contiguous():
+            raise ValueError("w must be a contiguous tensor of shape %s" % ((C_out, Kh, Kw, C_in // G),))
+        if self.bias:
+            if bias is None or bias.dtype != torch.float32 or tuple(bias.shape) != (C_out,) or \
+                    not bias.is_contiguous() or not bias.is_cuda:
+                raise ValueError("bias must be a contiguous CUDA float32 tensor of shape (%d,)" % C_out)
+        if y is None:
+            y = self.empty_output(x.device)
+        elif tuple(y.shape) != (N, self.H_out, self.W_out, C_out) or y.dtype != self.out_dtype() or \
+                not y.is_contiguous():
+            raise ValueError("y has the wrong shape, dtype or layout")
+        if stream is None:
+            stream = torch.cuda.current_stream(x.device)
+        st = lib().conv_forward(self._plan, x.data_ptr(), w.data_ptr(),
+                                bias.data_ptr() if (self.bias and bias is not None) else None,
+                                y.data_ptr(), stream.cuda_stream)
+        if st != 0:
+            raise ConvError(st, "conv_forward")
+        return y
+
+    __call__ = forward
+
+
+_plan_cache = {}
+
+
+def conv2d(x, w, bias=None, stride=1, padding=0, dilation=1, groups=1, relu=False, out_bf16=False,
+           y=None, stream=None):
+    """Functional form: x NHWC [N][H][W][C_in], w [C_out][Kh][Kw][C_in/G], bias FP32 or None."""
+    import torch
+    N, H, W, C_in = x.shape
+    C_out, Kh, Kw, _ = w.shape
+    dtype = "bf16" if x.dtype == torch.bfloat16 else "f32"
+    key = (x.device.index, N, C_in, H, W, C_out, Kh, Kw, stride, padding, dilation, groups, dtype,
+           bias is not None, relu, out_bf16)
+    plan = _plan_cache.get(key)
+    if plan is None:
+        plan = ConvPlan(N, C_in, H, W, C_out, Kh, Kw, stride, padding, dilation, groups, dtype,
+                        bias is not None, relu, out_bf16)
+        _plan_cache[key] = plan
+    return plan.forward(x, w, bias, y=y, stream=stream)

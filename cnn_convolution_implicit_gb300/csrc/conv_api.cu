@@ -1,0 +1,439 @@
+// conv_api.cu -- the C ABI (include/conv.h): plan creation, shape checks,
+// kernel choice, TMA descriptor encoding and launch.
+//
+// Shape math: H_out = floor((H + 2P - D(Kh-1) - 1)/S) + 1 ("Convolution
+// variants and their matrix operations", lpnh.cn/news/2674933, section 6.2;
+// the printed formula is garbled, this is its reading), with the effective
+// dilated kernel K + (K-1)(D-1) (same page, section 2.3).  GEMM extents
+// M = C_out, N = N*H_out*W_out, K = (C_in/G)*Kh*Kw ("GPU lesson 9: how a GPU
+// executes neural-network convolution", lincklin.cn, section 19).
+//
+// Kernel choice by shape (the channel-alignment concerns of lesson 9 sections
+// 20 and 33 decide it):
+//   FP32, G = C_in = C_out, C % 32 == 0   -> depthwise halo-tile kernel
+//   BF16, 1x1, S=1, P=0, G=1, aligned      -> tcgen05 GEMM with tiled TMA
+//   BF16, (C_in/G) % 64 == 0, aligned      -> tcgen05 implicit GEMM, TMA im2col
+//   BF16, G=1, C_in*Kh*Kw <= 64            -> tcgen05 small-K kernel (stem)
+//   anything else                          -> direct CUDA-core kernel
+#include <mutex>
+#include <new>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/conv.h"
+#include "conv_internal.h"
+
+using namespace convgb;
+
+// Device status word: bits latched by kernels whose bounded waits gave up.
+__device__ unsigned int g_conv_status_word;
+
+struct conv_plan {
+    ConvGeom g;
+    conv_dtype dtype;
+    unsigned flags;
+    int path;
+    int device;
+    int num_sms;
+    int smem_optin;
+    unsigned* status;
+    // per-path configuration
+    TcGemmParams tc;
+    SmallKParams sk;
+    DepthwiseParams dw;
+    // descriptor cache, keyed by the pointers it was encoded for
+    const void* cache_x;
+    const void* cache_w;
+    bool cache_valid;
+    CUtensorMap map_a;  // the type carries its own 64-byte alignment
+    CUtensorMap map_b;
+};
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+PFN_cuTensorMapEncodeIm2col_v12000 g_encode_im2col = nullptr;
+std::once_flag g_entry_once;
+bool g_entry_ok = false;
+
+bool load_entry_points() {
+    std::call_once(g_entry_once, [] {
+        cudaDriverEntryPointQueryResult q1, q2;
+        void* f1 = nullptr;
+        void* f2 = nullptr;
+        const cudaError_t e1 = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f1, 12000,
+                                                                cudaEnableDefault, &q1);
+        const cudaError_t e2 = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &f2, 12000,
+                                                                cudaEnableDefault, &q2);
+        if (e1 == cudaSuccess && e2 == cudaSuccess && q1 == cudaDriverEntryPointSuccess &&
+            q2 == cudaDriverEntryPointSuccess && f1 && f2) {
+            g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f1);
+            g_encode_im2col = reinterpret_cast<PFN_cuTensorMapEncodeIm2col_v12000>(f2);
+            g_entry_ok = true;
+        }
+    });
+    return g_entry_ok;
+}
+
+int out_extent(int in, int k, int s, int p, int d) {
+    const long long num = static_cast<long long>(in) + 2LL * p - static_cast<long long>(d) * (k - 1) - 1;
+    if (num < 0) return 0;
+    return static_cast<int>(num / s + 1);
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+int pow2_at_least(int v) {
+    int r = 32;
+    while (r < v) r <<= 1;
+    return r;
+}
+
+// tcgen05 GEMM configuration; false when the shape does not fit it.
+bool configure_tc(conv_plan* pl, bool one_by_one) {
+    const ConvGeom& g = pl->g;
+    TcGemmParams& t = pl->tc;
+    if (g.cin_g % kTcBlockK != 0) return false;
+    if (g.cout_g % 16 != 0) return false;
+    const long long ktot = static_cast<long long>(g.cin_g) * g.Kh * g.Kw;
+    if ((ktot * 2) % 16 != 0) return false;
+    int n_tile, mma_n, gpc;
+    if (g.cout_g >= 256) {
+        if (g.cout_g % 256 != 0) return false;
+        n_tile = mma_n = 256;
+        gpc = 1;
+    } else {
+        mma_n = g.cout_g;
+        gpc = 0;
+        for (int c = g.G; c >= 1; --c)
+            if (g.G % c == 0 && c * g.cout_g <= 256 && (c * g.cout_g) % 32 == 0) {
+                gpc = c;
+                break;
+            }
+        if (gpc == 0) return false;
+        n_tile = gpc * g.cout_g;
+    }
+    if (!one_by_one) {
+        // im2col bounding box corners must fit the 4-D map's signed 8-bit range
+        const int lo = -g.P;
+        const int up_w = g.P - (g.Kw - 1) * g.D, up_h = g.P - (g.Kh - 1) * g.D;
+        if (lo < -128 || up_w < -128 || up_h < -128 || g.P > 127) return false;
+        if (g.S > 8) return false;
+        if ((g.Kw - 1) * g.D > 65535 || (g.Kh - 1) * g.D > 65535) return false;
+    }
+    if (g.pixels > 0x7fffffffLL) return false;
+    t.g = g;
+    t.mode = one_by_one ? kTcMode1x1 : kTcModeIm2col;
+    t.n_tile = n_tile;
+    t.mma_n = mma_n;
+    t.gpc = gpc;
+    t.kblk = g.cin_g / kTcBlockK;
+    t.ksteps = g.Kh * g.Kw * t.kblk;
+    t.num_m_tiles = static_cast<int>((g.pixels + kTcBlockM - 1) / kTcBlockM);
+    t.num_n_tiles = g.C_out / n_tile;
+    t.num_tiles = t.num_m_tiles * t.num_n_tiles;
+    const int stage_bytes = kTcBlockM * kTcBlockK * 2 + mma_n * 128;
+    const int fixed = 1024 + 256;
+    int stages = (pl->smem_optin - fixed) / stage_bytes;
+    if (stages > 8) stages = 8;
+    if (stages < 2) return false;
+    t.stages = stages;
+    t.smem_bytes = fixed + stages * stage_bytes;
+    t.tmem_cols = pow2_at_least(2 * n_tile);
+    t.relu = (pl->flags & CONV_FLAG_RELU) ? 1 : 0;
+    t.status = pl->status;
+    return true;
+}
+
+bool configure_smallk(conv_plan* pl) {
+    const ConvGeom& g = pl->g;
+    SmallKParams& s = pl->sk;
+    if (g.G != 1) return false;
+    const int ktot = g.C_in * g.Kh * g.Kw;
+    if (ktot > 64) return false;
+    if (g.C_out % 32 != 0 || g.C_out > 256) return false;
+    const long long row_bytes = static_cast<long long>(g.W) * g.C_in * 2;
+    if (row_bytes % 16 != 0) return false;
+    const long long raw = (static_cast<long long>(g.Kh) * row_bytes + 1023) / 1024 * 1024;
+    if (raw > 32 * 1024) return false;
+    const long long segs = (g.W_out + 127) / 128;
+    const long long tiles = static_cast<long long>(g.N) * g.H_out * segs;
+    if (tiles > 0x7fffffffLL) return false;
+    s.g = g;
+    s.ktot = ktot;
+    s.kmma = (ktot + 15) / 16;
+    s.segs = static_cast<int>(segs);
+    s.num_tiles = static_cast<int>(tiles);
+    s.row_bytes = static_cast<int>(row_bytes);
+    s.raw_bytes = static_cast<int>(raw);
+    const int fixed = 1024 + g.C_out * 128 + 512;
+    const int stage_bytes = 128 * 128 + s.raw_bytes;
+    int stages = (pl->smem_optin - fixed) / stage_bytes;
+    if (stages > 8) stages = 8;
+    if (stages < 2) return false;
+    s.stages = stages;
+    s.smem_bytes = fixed + stages * stage_bytes;
+    s.tmem_cols = pow2_at_least(2 * g.C_out);
+    s.relu = (pl->flags & CONV_FLAG_RELU) ? 1 : 0;
+    s.status = pl->status;
+    return true;
+}
+
+bool configure_depthwise(conv_plan* pl) {
+    const ConvGeom& g = pl->g;
+    DepthwiseParams& d = pl->dw;
+    if (!(g.G == g.C_in && g.C_out == g.C_in)) return false;
+    if (g.C_in % 32 != 0) return false;
+    const int t = depthwise_tile_for(g);
+    if (t == 0) return false;
+    d.g = g;
+    d.tile = t;
+    d.tiles_h = (g.H_out + t - 1) / t;
+    d.tiles_w = (g.W_out + t - 1) / t;
+    d.cblocks = g.C_in / 32;
+    d.in_h = (t - 1) * g.S + (g.Kh - 1) * g.D + 1;
+    d.in_w = (t - 1) * g.S + (g.Kw - 1) * g.D + 1;
+    const long long blocks = static_cast<long long>(g.N) * d.tiles_h * d.tiles_w * d.cblocks;
+    if (blocks > 0x7fffffffLL) return false;
+    d.relu = (pl->flags & CONV_FLAG_RELU) ? 1 : 0;
+    d.out_bf16 = (pl->flags & CONV_FLAG_OUT_BF16) ? 1 : 0;
+    d.status = pl->status;
+    return true;
+}
+
+conv_status encode_maps(conv_plan* pl, const void* x, const void* w) {
+    if (pl->cache_valid && pl->cache_x == x && pl->cache_w == w) return CONV_OK;
+    if (!load_entry_points()) return CONV_ERR_CUDA;
+    const ConvGeom& g = pl->g;
+    CUresult r = CUDA_SUCCESS;
+    if (pl->path == CONV_PATH_GEMM_1X1 || pl->path == CONV_PATH_IMPLICIT_GEMM) {
+        if (pl->path == CONV_PATH_GEMM_1X1) {
+            const cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.C_in), static_cast<cuuint64_t>(g.pixels)};
+            const cuuint64_t strides[1] = {static_cast<cuuint64_t>(g.C_in) * 2};
+            const cuuint32_t box[2] = {kTcBlockK, kTcBlockM};
+            const cuuint32_t estr[2] = {1, 1};
+            r = g_encode_tiled(&pl->map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides,
+                               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        } else {
+            const cuuint64_t dims[4] = {static_cast<cuuint64_t>(g.C_in), static_cast<cuuint64_t>(g.W),
+                                        static_cast<cuuint64_t>(g.H), static_cast<cuuint64_t>(g.N)};
+            const cuuint64_t strides[3] = {static_cast<cuuint64_t>(g.C_in) * 2,
+                                           static_cast<cuuint64_t>(g.W) * g.C_in * 2,
+                                           static_cast<cuuint64_t>(g.H) * g.W * g.C_in * 2};
+            const int lower[2] = {-g.P, -g.P};
+            const int upper[2] = {g.P - (g.Kw - 1) * g.D, g.P - (g.Kh - 1) * g.D};
+            const cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(g.S), static_cast<cuuint32_t>(g.S), 1};
+            r = g_encode_im2col(&pl->map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides,
+                                lower, upper, kTcBlockK, kTcBlockM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        }
+        if (r != CUDA_SUCCESS) return CONV_ERR_CUDA;
+        const long long ktot = static_cast<long long>(g.cin_g) * g.Kh * g.Kw;
+        const cuuint64_t bdims[2] = {static_cast<cuuint64_t>(ktot), static_cast<cuuint64_t>(g.C_out)};
+        const cuuint64_t bstrides[1] = {static_cast<cuuint64_t>(ktot) * 2};
+        const cuuint32_t bbox[2] = {kTcBlockK, static_cast<cuuint32_t>(pl->tc.mma_n)};
+        const cuuint32_t bestr[2] = {1, 1};
+        r = g_encode_tiled(&pl->map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), bdims, bstrides,
+                           bbox, bestr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return CONV_ERR_CUDA;
+    } else if (pl->path == CONV_PATH_DEPTHWISE) {
+        const cuuint64_t dims[4] = {static_cast<cuuint64_t>(g.C_in), static_cast<cuuint64_t>(g.W),
+                                    static_cast<cuuint64_t>(g.H), static_cast<cuuint64_t>(g.N)};
+        const cuuint64_t strides[3] = {static_cast<cuuint64_t>(g.C_in) * 4, static_cast<cuuint64_t>(g.W) * g.C_in * 4,
+                                       static_cast<cuuint64_t>(g.H) * g.W * g.C_in * 4};
+        const cuuint32_t box[4] = {32, static_cast<cuuint32_t>(pl->dw.in_w), static_cast<cuuint32_t>(pl->dw.in_h), 1};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        r = g_encode_tiled(&pl->map_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(x), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return CONV_ERR_CUDA;
+    }
+    pl->cache_x = x;
+    pl->cache_w = w;
+    pl->cache_valid = true;
+    return CONV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+conv_status conv_plan_create(conv_plan** out, int N, int C_in, int H, int W, int C_out, int Kh, int Kw, int S,
+                             int P, int D, int G, conv_dtype dtype, unsigned flags) {
+    if (out == nullptr) return CONV_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (N <= 0 || C_in <= 0 || H <= 0 || W <= 0 || C_out <= 0 || Kh <= 0 || Kw <= 0 || S <= 0 || P < 0 || D <= 0 ||
+        G <= 0)
+        return CONV_ERR_INVALID_ARG;
+    if (C_in % G != 0 || C_out % G != 0) return CONV_ERR_INVALID_ARG;
+    if (dtype != CONV_F32 && dtype != CONV_BF16) return CONV_ERR_INVALID_ARG;
+    if (flags & ~(CONV_FLAG_BIAS | CONV_FLAG_RELU | CONV_FLAG_OUT_BF16)) return CONV_ERR_INVALID_ARG;
+    if ((flags & CONV_FLAG_OUT_BF16) && dtype != CONV_F32) return CONV_ERR_INVALID_ARG;
+    const int Ho = out_extent(H, Kh, S, P, D), Wo = out_extent(W, Kw, S, P, D);
+    if (Ho < 1 || Wo < 1) return CONV_ERR_INVALID_ARG;
+
+    conv_plan* pl = new (std::nothrow) conv_plan();
+    if (pl == nullptr) return CONV_ERR_NO_MEMORY;
+    ConvGeom& g = pl->g;
+    g.N = N; g.C_in = C_in; g.H = H; g.W = W; g.C_out = C_out;
+    g.Kh = Kh; g.Kw = Kw; g.S = S; g.P = P; g.D = D; g.G = G;
+    g.H_out = Ho; g.W_out = Wo;
+    g.cin_g = C_in / G; g.cout_g = C_out / G;
+    g.pixels = static_cast<long long>(N) * Ho * Wo;
+    pl->dtype = dtype;
+    pl->flags = flags;
+    pl->cache_valid = false;
+
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) {
+        // No device: a host-only plan (shape checks and kernel choice against
+        // a 152-SM, 227 KB-per-block part).  conv_forward on it fails with
+        // CONV_ERR_CUDA; nothing falls back to the host.
+        cudaGetLastError();
+        pl->device = -1;
+        pl->num_sms = 152;
+        pl->smem_optin = 232448;
+        pl->status = nullptr;
+    } else if (cudaGetDevice(&pl->device) != cudaSuccess ||
+               cudaDeviceGetAttribute(&pl->num_sms, cudaDevAttrMultiProcessorCount, pl->device) != cudaSuccess ||
+               cudaDeviceGetAttribute(&pl->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, pl->device) !=
+                   cudaSuccess ||
+               cudaGetSymbolAddress(reinterpret_cast<void**>(&pl->status), g_conv_status_word) != cudaSuccess) {
+        cudaGetLastError();
+        delete pl;
+        return CONV_ERR_CUDA;
+    }
+
+    pl->path = CONV_PATH_DIRECT;
+    if (dtype == CONV_F32) {
+        if (configure_depthwise(pl)) pl->path = CONV_PATH_DEPTHWISE;
+    } else {
+        const bool pointwise = Kh == 1 && Kw == 1 && S == 1 && P == 0 && G == 1;
+        if (pointwise && configure_tc(pl, true))
+            pl->path = CONV_PATH_GEMM_1X1;
+        else if (configure_tc(pl, false))
+            pl->path = CONV_PATH_IMPLICIT_GEMM;
+        else if (configure_smallk(pl))
+            pl->path = CONV_PATH_SMALL_K_GEMM;
+    }
+    *out = pl;
+    return CONV_OK;
+}
+
+conv_status conv_plan_output_shape(const conv_plan* p, int* H_out, int* W_out) {
+    if (p == nullptr || H_out == nullptr || W_out == nullptr) return CONV_ERR_INVALID_ARG;
+    *H_out = p->g.H_out;
+    *W_out = p->g.W_out;
+    return CONV_OK;
+}
+
+conv_status conv_plan_info(const conv_plan* p, int* path, long long* gemm_m, long long* gemm_n, long long* gemm_k) {
+    if (p == nullptr) return CONV_ERR_INVALID_ARG;
+    if (path) *path = p->path;
+    if (gemm_m) *gemm_m = p->g.C_out;
+    if (gemm_n) *gemm_n = p->g.pixels;
+    if (gemm_k) *gemm_k = static_cast<long long>(p->g.cin_g) * p->g.Kh * p->g.Kw;
+    return CONV_OK;
+}
+
+int conv_plan_num_sms(const conv_plan* p) { return p ? p->num_sms : 0; }
+
+conv_status conv_forward(conv_plan* p, const void* x, const void* w, const void* bias, void* y, void* stream) {
+    if (p == nullptr || x == nullptr || w == nullptr || y == nullptr) return CONV_ERR_INVALID_ARG;
+    if (p->device < 0) return CONV_ERR_CUDA;  // host-only plan: no device to run on
+    const bool has_bias = (p->flags & CONV_FLAG_BIAS) != 0;
+    if (has_bias && bias == nullptr) return CONV_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (has_bias && !aligned16(bias)))
+        return CONV_ERR_MISALIGNED;
+    const float* b = has_bias ? static_cast<const float*>(bias) : nullptr;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    switch (p->path) {
+        case CONV_PATH_GEMM_1X1:
+        case CONV_PATH_IMPLICIT_GEMM: {
+            conv_status s = encode_maps(p, x, w);
+            if (s != CONV_OK) return s;
+            TcGemmParams t = p->tc;
+            t.bias = b;
+            t.y = static_cast<__nv_bfloat16*>(y);
+            const int grid = t.num_tiles < p->num_sms ? t.num_tiles : p->num_sms;
+            e = launch_tc_gemm(p->map_a, p->map_b, t, grid, st);
+            break;
+        }
+        case CONV_PATH_SMALL_K_GEMM: {
+            SmallKParams s = p->sk;
+            s.x = static_cast<const __nv_bfloat16*>(x);
+            s.w = static_cast<const __nv_bfloat16*>(w);
+            s.bias = b;
+            s.y = static_cast<__nv_bfloat16*>(y);
+            const int grid = s.num_tiles < p->num_sms ? s.num_tiles : p->num_sms;
+            e = launch_tc_smallk(s, grid, st);
+            break;
+        }
+        case CONV_PATH_DEPTHWISE: {
+            conv_status s = encode_maps(p, x, w);
+            if (s != CONV_OK) return s;
+            DepthwiseParams d = p->dw;
+            d.w = static_cast<const float*>(w);
+            d.bias = b;
+            d.y = y;
+            e = launch_depthwise(p->map_a, d, st);
+            break;
+        }
+        default: {
+            DirectParams d;
+            d.g = p->g;
+            d.x = x;
+            d.w = w;
+            d.bias = b;
+            d.y = y;
+            d.relu = (p->flags & CONV_FLAG_RELU) ? 1 : 0;
+            d.in_bf16 = p->dtype == CONV_BF16 ? 1 : 0;
+            d.out_bf16 = (p->dtype == CONV_BF16 || (p->flags & CONV_FLAG_OUT_BF16)) ? 1 : 0;
+            e = launch_direct(d, st);
+            break;
+        }
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return CONV_ERR_CUDA;
+    }
+    return CONV_OK;
+}
+
+conv_status conv_plan_destroy(conv_plan* p) {
+    delete p;
+    return CONV_OK;
+}
+
+const char* conv_status_string(conv_status s) {
+    switch (s) {
+        case CONV_OK: return "ok";
+        case CONV_ERR_INVALID_ARG: return "invalid argument";
+        case CONV_ERR_UNSUPPORTED: return "unsupported convolution";
+        case CONV_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+        case CONV_ERR_CUDA: return "CUDA call failed";
+        case CONV_ERR_NO_MEMORY: return "host allocation failed";
+        case CONV_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+conv_status conv_device_status(int* code) {
+    if (code == nullptr) return CONV_ERR_INVALID_ARG;
+    *code = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return CONV_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_conv_status_word, sizeof(v)) != cudaSuccess) return CONV_ERR_CUDA;
+    if (v != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_conv_status_word, &zero, sizeof(zero)) != cudaSuccess) return CONV_ERR_CUDA;
+    }
+    *code = static_cast<int>(v);
+    return v ? CONV_ERR_TIMEOUT : CONV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,266 @@
+// tc_gemm.cu -- BF16 convolution as an implicit GEMM on tcgen05 tensor cores.
+//
+// The convolution-as-GEMM mapping of "GPU lesson 9: how a GPU executes
+// neural-network convolution" (lincklin.cn), section 19 (M = C_out,
+// N = N*H_out*W_out, K = C_in*Kh*Kw), computed as an implicit GEMM (section
+// 11; "Convolution variants and their matrix operations", lpnh.cn/news/2674933,
+// section 3.3): the im2col matrix is never stored.  Each K-step is one kernel
+// tap (kh, kw) and one 64-channel block; the TMA engine gathers the 128 input
+// pixels of that tap straight from the NHWC tensor in im2col mode, with its
+// out-of-bounds zero fill standing in for the padding (lesson 9, section 26)
+// and the tap offset (kh*D, kw*D) gathering only the Kh*Kw live taps of a
+// dilated kernel (variants page, section 4.2).  A 1x1 / stride-1 / pad-0
+// convolution is a plain GEMM (lesson 9, section 21) and uses a 2-D tiled map.
+//
+// Operand roles on the tensor core: the MMA's M side is the pixel tile (128
+// TMEM lanes), its N side the output channels; D = Y^T of the logical GEMM, so
+// each TMEM lane holds one output pixel's contiguous NHWC channel vector.
+// Groups are independent GEMMs (variants page, sections 2.2 and 4.3): a tile
+// packs `gpc` groups side by side in TMEM columns, each with its own K loop.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over tiles):
+//   warp 0      TMA producer (one lane): A (pixels x 64 ch) and B (C_out x 64) per K-step
+//   warp 1      TMEM allocator; one lane issues tcgen05.mma and commits
+//   warps 2..5  epilogue: tcgen05.ld -> +bias -> ReLU -> BF16 -> NHWC store
+// Shared memory holds a ring of `stages` (A, B) buffers; TMEM holds two
+// accumulators so the epilogue of tile i overlaps the MMAs of tile i+1.
+#include "conv_internal.h"
+#include "tc_common.cuh"
+
+namespace convgb {
+
+namespace {
+
+constexpr uint32_t kABytes = kTcBlockM * kTcBlockK * 2;  // 16 KB
+
+struct TcSmem {
+    uint8_t* a;
+    uint8_t* b;
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* tfull;
+    uint64_t* tempty;
+    uint64_t* drain;
+    uint32_t* tmem_slot;
+    int* abort;
+};
+
+__device__ __forceinline__ TcSmem carve(uint8_t* raw, const TcGemmParams& p) {
+    TcSmem s;
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t b_bytes = static_cast<uint32_t>(p.mma_n) * 128u;
+    s.a = base;
+    s.b = base + p.stages * kABytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s.b + p.stages * b_bytes);
+    s.full = bars;
+    s.empty = bars + p.stages;
+    s.tfull = bars + 2 * p.stages;
+    s.tempty = s.tfull + 2;
+    s.drain = s.tempty + 2;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
+    s.abort = reinterpret_cast<int*>(s.tmem_slot + 1);
+    return s;
+}
+
+// Sub-GEMM j of n-tile nt: its group, first weight row, and TMEM column offset.
+__device__ __forceinline__ void sub_gemm(const TcGemmParams& p, int nt, int j, int& grp, int& brow) {
+    if (p.g.cout_g >= p.n_tile) {  // one group spans one or more n-tiles
+        brow = nt * p.n_tile;
+        grp = brow / p.g.cout_g;
+    } else {                       // several groups packed in one n-tile
+        grp = nt * p.gpc + j;
+        brow = grp * p.g.cout_g;
+    }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_conv_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
+                   const TcGemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const TcSmem sm = carve(smem_raw, p);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    volatile int* abort = sm.abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm.tfull[b], 1);
+            mbar_init(&sm.tempty[b], 4 * 32);
+        }
+        mbar_init(sm.drain, 1);
+        *sm.abort = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&a_map);
+        tma_prefetch_desc(&b_map);
+    }
+    if (warp == 1) {
+        tmem_alloc(sm.tmem_slot, p.tmem_cols);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *sm.tmem_slot;
+
+    const int HWo = p.g.H_out * p.g.W_out;
+    const uint32_t b_bytes = static_cast<uint32_t>(p.mma_n) * 128u;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+                const int m = tile / p.num_n_tiles;
+                const int nt = tile - m * p.num_n_tiles;
+                const long long pix0 = static_cast<long long>(m) * kTcBlockM;
+                const int n0 = static_cast<int>(pix0 / HWo);
+                const int rem = static_cast<int>(pix0 - static_cast<long long>(n0) * HWo);
+                const int ho0 = rem / p.g.W_out;
+                const int wo0 = rem - ho0 * p.g.W_out;
+                for (int j = 0; j < p.gpc && ok; ++j) {
+                    int grp, brow;
+                    sub_gemm(p, nt, j, grp, brow);
+                    for (int ks = 0; ks < p.ksteps; ++ks) {
+                        if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
+                            record_status(p.status, kStatusTimeoutProducer, abort);
+                            ok = false;
+                            break;
+                        }
+                        const int tap = ks / p.kblk;
+                        const int kb = ks - tap * p.kblk;
+                        const int kh = tap / p.g.Kw;
+                        const int kw = tap - kh * p.g.Kw;
+                        const int c = grp * p.g.cin_g + kb * kTcBlockK;
+                        uint8_t* a_dst = sm.a + stage * kABytes;
+                        uint8_t* b_dst = sm.b + stage * b_bytes;
+                        mbar_arrive_expect_tx(&sm.full[stage], kABytes + b_bytes);
+                        if (p.mode == kTcMode1x1) {
+                            tma_load_2d(a_dst, &a_map, &sm.full[stage], c, static_cast<int>(pix0));
+                        } else {
+                            tma_load_im2col_4d(a_dst, &a_map, &sm.full[stage], c, wo0 * p.g.S - p.g.P,
+                                               ho0 * p.g.S - p.g.P, n0, static_cast<uint16_t>(kw * p.g.D),
+                                               static_cast<uint16_t>(kh * p.g.D));
+                        }
+                        tma_load_2d(b_dst, &b_map, &sm.full[stage], tap * p.g.cin_g + kb * kTcBlockK, brow);
+                        ++issued;
+                        if (++stage == p.stages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
+            // Drain: every issued fill must have landed before the CTA may exit.
+            for (int s = 0; s < p.stages; ++s) {
+                const long long fills = issued / p.stages + (s < issued % p.stages ? 1 : 0);
+                if (fills > 0 && !mbar_wait(&sm.full[s], static_cast<uint32_t>((fills - 1) & 1), nullptr))
+                    record_status(p.status, kStatusTimeoutDrain, abort);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kTcBlockM, p.mma_n);
+            int stage = 0;
+            uint32_t phase = 0;
+            int local = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x, ++local) {
+                const int buf = local & 1;
+                const uint32_t use = static_cast<uint32_t>(local >> 1) & 1u;
+                if (!mbar_wait(&sm.tempty[buf], use ^ 1u, abort)) {
+                    record_status(p.status, kStatusTimeoutMma, abort);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_base = tmem_base + static_cast<uint32_t>(buf * p.n_tile);
+                for (int j = 0; j < p.gpc && ok; ++j) {
+                    const uint32_t d = d_base + static_cast<uint32_t>(j * p.mma_n);
+                    for (int ks = 0; ks < p.ksteps; ++ks) {
+                        if (!mbar_wait(&sm.full[stage], phase, abort)) {
+                            record_status(p.status, kStatusTimeoutMma, abort);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t adesc = sdesc_sw128(smem_addr(sm.a + stage * kABytes));
+                        const uint64_t bdesc = sdesc_sw128(smem_addr(sm.b + stage * b_bytes));
+#pragma unroll
+                        for (int k = 0; k < kTcBlockK / 16; ++k) {
+                            // +32 bytes along K inside the swizzle row = +2 in the >>4 address field
+                            mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
+                        }
+                        mma_commit(&sm.empty[stage]);
+                        if (++stage == p.stages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+                if (ok) mma_commit(&sm.tfull[buf]);
+            }
+            // Drain: all MMAs this thread issued complete before TMEM is freed.
+            mma_commit(sm.drain);
+            if (!mbar_wait(sm.drain, 0, nullptr)) record_status(p.status, kStatusTimeoutDrain, abort);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+        const int row = quarter * 32 + lane;
+        int local = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+            const int buf = local & 1;
+            const uint32_t use = static_cast<uint32_t>(local >> 1) & 1u;
+            // warp-uniform outcome, so the .sync.aligned TMEM loads below stay converged
+            const bool ready = __all_sync(0xffffffffu, mbar_wait(&sm.tfull[buf], use, abort));
+            if (!ready) {
+                record_status(p.status, kStatusTimeoutEpilogue, abort);
+                break;
+            }
+            tc_fence_after();
+            const int m = tile / p.num_n_tiles;
+            const int nt = tile - m * p.num_n_tiles;
+            const long long pix = static_cast<long long>(m) * kTcBlockM + row;
+            const bool valid = pix < p.g.pixels;
+            const int co0 = nt * p.n_tile;
+            __nv_bfloat16* yrow = p.y + (valid ? pix : 0) * p.g.C_out + co0;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(buf * p.n_tile);
+            for (int c = 0; c < p.n_tile; c += 32) {
+                uint32_t v[32];
+                __syncwarp();
+                tmem_ld32(t_row + static_cast<uint32_t>(c), v);
+                tmem_ld_wait();
+                epilogue_store32(v, p.bias ? p.bias + co0 + c : nullptr, p.relu, yrow + c, valid);
+            }
+            tc_fence_before();
+            mbar_arrive(&sm.tempty[buf]);
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, p.tmem_cols);
+    }
+}
+
+cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, const TcGemmParams& p, int grid,
+                           cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(tc_conv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
+    if (e != cudaSuccess) return e;
+    tc_conv_kernel<<<grid, kTcThreads, p.smem_bytes, stream>>>(a_map, b_map, p);
+    return cudaGetLastError();
+}
+
+}  // namespace convgb

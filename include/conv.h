@@ -1,0 +1,139 @@
+/*
+ * conv.h -- C ABI of the GB300 (sm_103a) forward 2D convolution library.
+ *
+ * Operation (one call = one layer):
+ *
+ *   y[n][ho][wo][co] = act( bias[co] + sum_{ci'<C_in/G} sum_{kh<Kh} sum_{kw<Kw}
+ *                             x[n][ho*S + kh*D - P][wo*S + kw*D - P][g*C_in/G + ci']
+ *                           * w[co][kh][kw][ci'] ),     g = co / (C_out/G)
+ *
+ * Input coordinates outside [0,H) x [0,W) read as zero.  act is ReLU when
+ * CONV_FLAG_RELU is set, else identity.  Depthwise convolution is the case
+ * G = C_in = C_out.
+ *
+ * Sources: the dot-product definition and index map of "GPU lesson 9: how a
+ * GPU executes neural-network convolution" (lincklin.cn), section 2; zero
+ * padding as an address test, section 26; the conv-as-GEMM mapping
+ * M = C_out, N = N*H_out*W_out, K = C_in*Kh*Kw, section 19; bias and
+ * activation fused after the sum, section 31.  Dilation, groups and the output
+ * size H_out = floor((H + 2P - D(Kh-1) - 1)/S) + 1 follow "Convolution variants
+ * and their matrix operations" (lpnh.cn/news/2674933), sections 2.2, 2.3, 4.2,
+ * 4.3 and 6.2.  The same S, P, D apply to both spatial axes.
+ *
+ * Layouts (all dense, row-major, caller-owned device memory):
+ *   x    [N][H][W][C_in]              (NHWC)
+ *   w    [C_out][Kh][Kw][C_in/G]      (K order kh, kw, ci)
+ *   bias [C_out], always FP32          (read only when CONV_FLAG_BIAS is set)
+ *   y    [N][H_out][W_out][C_out]     (NHWC)
+ * Element types: CONV_F32 -> x, w, y FP32 (y BF16 when CONV_FLAG_OUT_BF16);
+ *                CONV_BF16 -> x, w, y BF16.  Accumulation is always FP32.
+ *
+ * Ownership: the plan is host memory owned by the caller between
+ * conv_plan_create and conv_plan_destroy.  It owns no device memory and
+ * allocates none.  A plan may be reused for any number of forwards with any
+ * pointers of the right size, but not from two host threads at once (it caches
+ * TMA descriptors keyed by pointer).
+ *
+ * Errors: every call returns a conv_status; no call prints, traps or aborts.
+ * conv_forward is asynchronous on the given stream and never synchronises;
+ * device-side wait timeouts (a safety net that fires only on a hang) are
+ * latched in a device word read by conv_device_status.
+ */
+#ifndef CONV_GB300_CONV_H
+#define CONV_GB300_CONV_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct conv_plan conv_plan;     /* opaque, host-owned */
+
+typedef enum { CONV_F32 = 0, CONV_BF16 = 1 } conv_dtype;
+
+enum {
+    CONV_FLAG_BIAS = 1u,       /* add bias[co] after the sum                          */
+    CONV_FLAG_RELU = 2u,       /* max(., 0) after the bias                            */
+    CONV_FLAG_OUT_BF16 = 4u    /* CONV_F32 only: write y as BF16 (round to nearest even) */
+};
+
+typedef enum {
+    CONV_OK = 0,
+    CONV_ERR_INVALID_ARG = 1,  /* bad size, NULL pointer or NULL plan                 */
+    CONV_ERR_UNSUPPORTED = 2,  /* valid convolution this library does not run          */
+    CONV_ERR_MISALIGNED = 3,   /* a device pointer is not 16-byte aligned              */
+    CONV_ERR_CUDA = 4,         /* a CUDA runtime / driver call failed                  */
+    CONV_ERR_NO_MEMORY = 5,    /* host allocation of the plan failed                   */
+    CONV_ERR_TIMEOUT = 6       /* a device-side wait gave up (reported by conv_device_status) */
+} conv_status;
+
+/* Which kernel a plan runs (conv_plan_info). */
+typedef enum {
+    CONV_PATH_DIRECT = 0,         /* CUDA-core direct loop, any shape                      */
+    CONV_PATH_DEPTHWISE = 1,      /* FP32 depthwise, TMA halo tile in shared memory        */
+    CONV_PATH_GEMM_1X1 = 2,       /* BF16 1x1 / stride 1 / pad 0: tcgen05 GEMM, tiled TMA  */
+    CONV_PATH_IMPLICIT_GEMM = 3,  /* BF16 implicit GEMM: TMA im2col + tcgen05 + TMEM        */
+    CONV_PATH_SMALL_K_GEMM = 4    /* BF16, C_in*Kh*Kw <= 64 (e.g. a 3-channel stem): rows
+                                     staged by bulk copy, K gathered in shared memory,
+                                     tcgen05 + TMEM                                     */
+} conv_path;
+
+/*
+ * Create a plan for one convolution shape.  Validates the shape (all sizes
+ * > 0, P >= 0, C_in % G == 0, C_out % G == 0, H_out >= 1, W_out >= 1,
+ * CONV_FLAG_OUT_BF16 only with CONV_F32) and chooses the kernel.  Returns
+ * CONV_ERR_INVALID_ARG for a bad shape or out == NULL, CONV_ERR_NO_MEMORY if
+ * the host allocation fails, CONV_ERR_CUDA if the current device cannot be
+ * queried.  On error *out is set to NULL.  The plan is tied to the CUDA device
+ * current at creation.
+ */
+conv_status conv_plan_create(conv_plan **out, int N, int C_in, int H, int W, int C_out,
+                             int Kh, int Kw, int S, int P, int D, int G,
+                             conv_dtype dtype, unsigned flags);
+
+/* Output extent, floor((H + 2P - D(K-1) - 1)/S) + 1 per axis. */
+conv_status conv_plan_output_shape(const conv_plan *p, int *H_out, int *W_out);
+
+/*
+ * The chosen kernel (conv_path) and the logical GEMM extents of section 19 of
+ * lesson 9: M = C_out, N = N*H_out*W_out, K = (C_in/G)*Kh*Kw (per group).
+ * Any output pointer may be NULL.
+ */
+conv_status conv_plan_info(const conv_plan *p, int *path, long long *gemm_m,
+                           long long *gemm_n, long long *gemm_k);
+
+/*
+ * Run the convolution on `stream` (a cudaStream_t; NULL = the legacy default
+ * stream).  x, w, y must be non-NULL device pointers, 16-byte aligned; bias
+ * must be a non-NULL 16-byte aligned device pointer when CONV_FLAG_BIAS is set
+ * and is ignored otherwise.  y must not overlap x, w or bias.  Returns
+ * CONV_ERR_INVALID_ARG / CONV_ERR_MISALIGNED without launching anything,
+ * CONV_ERR_CUDA if a descriptor encode or the launch fails.  Asynchronous: the
+ * return value does not cover faults that happen after the launch.
+ */
+conv_status conv_forward(conv_plan *p, const void *x, const void *w, const void *bias,
+                         void *y, void *stream);
+
+/* Free the plan (host memory only).  NULL is accepted. */
+conv_status conv_plan_destroy(conv_plan *p);
+
+/* Static English text for a status code; never NULL. */
+const char *conv_status_string(conv_status s);
+
+/*
+ * Synchronise the current device, then read and clear the library's device
+ * status word for it.  *code receives 0 when no kernel hit a wait timeout
+ * since the last call, else a non-zero bit set naming the waits that gave up.
+ * Returns CONV_ERR_TIMEOUT when *code != 0, CONV_ERR_CUDA if the
+ * synchronisation or read fails (a sticky fault from an earlier launch shows
+ * up here), else CONV_OK.
+ */
+conv_status conv_device_status(int *code);
+
+/* Number of SMs the plan's grid sizing uses (device property of the plan's device). */
+int conv_plan_num_sms(const conv_plan *p);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONV_GB300_CONV_H */

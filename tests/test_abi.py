@@ -1,0 +1,111 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every symbol include/conv.h declares, validates shapes, and picks kernels."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import cnn_convolution_implicit_gb300 as cg
+from cnn_convolution_implicit_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "conv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(conv_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    L = cg.lib()
+    declared = header_functions()
+    assert set(declared) == set(binding.EXPORTS)
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_status_strings():
+    L = cg.lib()
+    for code in range(7):
+        assert L.conv_status_string(code)
+    assert L.conv_status_string(99) == b"unknown status"
+
+
+def _create(*args):
+    L = cg.lib()
+    h = ctypes.c_void_p(1234)
+    st = L.conv_plan_create(ctypes.byref(h), *args)
+    return st, h
+
+
+@pytest.mark.parametrize("args", [
+    (0, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 0),        # N = 0
+    (1, 3, 8, 8, 4, 3, 3, 0, 1, 1, 1, 0, 0),        # S = 0
+    (1, 3, 8, 8, 4, 3, 3, 1, -1, 1, 1, 0, 0),       # P < 0
+    (1, 3, 8, 8, 4, 3, 3, 1, 1, 0, 1, 0, 0),        # D = 0
+    (1, 6, 8, 8, 4, 3, 3, 1, 1, 1, 4, 0, 0),        # C_in % G
+    (1, 8, 8, 8, 6, 3, 3, 1, 1, 1, 4, 0, 0),        # C_out % G
+    (1, 3, 2, 2, 4, 5, 5, 1, 0, 1, 1, 0, 0),        # empty output
+    (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 1, 4),        # OUT_BF16 with BF16 input
+    (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 2, 0),        # bad dtype
+    (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 64),       # unknown flag
+])
+def test_create_rejects_bad_shapes(args):
+    st, h = _create(*args)
+    assert st == 1 and h.value is None
+
+
+def test_create_null_out_and_null_plan_calls():
+    L = cg.lib()
+    assert L.conv_plan_create(None, 1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 0) == 1
+    assert L.conv_plan_destroy(None) == 0
+    a, b = ctypes.c_int(), ctypes.c_int()
+    assert L.conv_plan_output_shape(None, ctypes.byref(a), ctypes.byref(b)) == 1
+    assert L.conv_forward(None, 16, 16, None, 16, None) == 1
+    assert L.conv_device_status(None) == 1
+
+
+@pytest.mark.parametrize("shape,path", [
+    ((32, 128, 112, 112, 256, 3, 3, 1, 1, 1, 1, "bf16"), "implicit_gemm"),
+    ((32, 3, 224, 224, 32, 3, 3, 2, 1, 1, 1, "bf16"), "small_k_gemm"),
+    ((64, 256, 56, 56, 256, 3, 3, 1, 1, 1, 256, "f32"), "depthwise"),
+    ((64, 256, 56, 56, 512, 1, 1, 1, 0, 1, 1, "bf16"), "gemm_1x1"),
+    ((16, 256, 64, 64, 256, 3, 3, 1, 2, 2, 4, "bf16"), "implicit_gemm"),
+    ((1, 3, 32, 32, 8, 3, 3, 1, 1, 1, 1, "f32"), "direct"),
+    ((2, 64, 9, 9, 24, 3, 3, 1, 1, 1, 1, "bf16"), "direct"),          # C_out % 16 != 0
+    ((2, 96, 9, 9, 64, 3, 3, 1, 1, 1, 1, "bf16"), "direct"),          # C_in not a multiple of 64, K > 64
+    ((2, 128, 9, 9, 64, 1, 1, 2, 0, 1, 1, "bf16"), "implicit_gemm"),  # strided 1x1 -> im2col
+    ((2, 128, 9, 9, 64, 3, 3, 1, 1, 1, 2, "bf16"), "implicit_gemm"),  # 2 groups packed per tile
+    ((2, 48, 9, 9, 48, 3, 3, 1, 1, 1, 48, "f32"), "direct"),          # depthwise, C % 32 != 0
+    ((2, 64, 9, 9, 64, 3, 3, 1, 1, 1, 64, "bf16"), "direct"),         # BF16 depthwise
+    ((2, 4, 30, 300, 64, 3, 3, 1, 1, 1, 1, "bf16"), "small_k_gemm"),  # 3 segments per row
+])
+def test_kernel_choice(shape, path):
+    *dims, dtype = shape
+    p = cg.ConvPlan(*dims, dtype=dtype, bias=True, relu=True)
+    assert p.path == path
+
+
+def test_gemm_extents_body_layer():
+    """Per image, the 112x112x128 -> 256 3x3 layer is a 256 x 12544 x 1152 GEMM
+    ("Convolution variants and their matrix operations", section 3.3)."""
+    p = cg.ConvPlan(1, 128, 112, 112, 256, 3, 3, 1, 1, 1, 1, "bf16")
+    assert p.gemm_mnk == (256, 12544, 1152)
+    assert (p.H_out, p.W_out) == (112, 112)
+
+
+def test_output_shape_matches_formula():
+    for (H, K, S, P, D) in [(224, 3, 2, 1, 1), (64, 3, 1, 2, 2), (7, 5, 3, 0, 1), (9, 2, 2, 3, 3)]:
+        p = cg.ConvPlan(1, 8, H, H, 8, K, K, S, P, D, 1, "f32")
+        exp = (H + 2 * P - D * (K - 1) - 1) // S + 1
+        assert (p.H_out, p.W_out) == (exp, exp)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device behaviour")
+def test_forward_without_device_fails_loudly():
+    p = cg.ConvPlan(1, 8, 8, 8, 8, 3, 3, 1, 1, 1, 1, "f32")
+    L = cg.lib()
+    assert L.conv_forward(p._plan, 256, 256, 256, 256, None) == 4  # CONV_ERR_CUDA, nothing launched

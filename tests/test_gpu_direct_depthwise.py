@@ -1,0 +1,73 @@
+"""GPU parity: direct CUDA-core kernel and FP32 depthwise halo-tile kernel
+against the FP64 oracle (elementwise, tolerance in tests/parity.py)."""
+import numpy as np
+import pytest
+import torch
+
+from parity import F32_TOL, check_full, check_points, oracle_full, run, sample_points
+from workloads import ConvShape, draw, inputs, random_shape
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_fp32_layer_full():
+    """N=1, 3->8, 32x32, 3x3 s1 p1, FP32 with bias: every output."""
+    s, x, w, b = inputs("tiny_f32")
+    plan, y = run(s, x, w, b)
+    assert plan.path == "direct"
+    check_full(s, y, oracle_full(s, x, w, b))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_direct_random_sweep(dtype):
+    """Random small shapes over K in {1,2,3,5}, S, P, D, G (all taken by the direct kernel)."""
+    rng = np.random.default_rng(11 if dtype == "f32" else 12)
+    for i in range(40):
+        s = random_shape(rng, dtype)
+        x, w, b = draw(s, (100 + i, 200 + i, 300 + i), "uniform", "uniform", "uniform")
+        plan, y = run(s, x, w, b)
+        check_full(s, y, oracle_full(s, x, w, b))
+
+
+def test_depthwise_full_size_layer():
+    """N=64, C=256, 56x56, depthwise 3x3 s1 p1 FP32: every output (0.46 G MACs in FP64)."""
+    s, x, w, b = inputs("dw")
+    plan, y = run(s, x, w, b)
+    assert plan.path == "depthwise"
+    check_full(s, y, oracle_full(s, x, w, b))
+
+
+@pytest.mark.parametrize("C,H,W,K,S,P,D,bias,relu", [
+    (32, 14, 14, 3, 1, 1, 1, False, False),      # one tile exactly
+    (64, 17, 23, 3, 1, 1, 1, True, True),        # ragged tiles on both axes
+    (32, 16, 16, 5, 1, 2, 1, True, False),       # 5x5, generic-K kernel
+    (32, 31, 29, 3, 2, 1, 1, False, True),       # stride 2
+    (96, 20, 20, 3, 1, 2, 2, True, True),        # dilation 2: 9 live taps of a 5x5 window
+    (32, 9, 40, 3, 1, 0, 1, False, False),       # no padding
+    (32, 1, 1, 3, 1, 1, 1, True, False),         # 1x1 image: only the centre tap is live
+    (32, 12, 12, 1, 1, 0, 1, True, True),        # 1x1 depthwise = per-channel scale
+])
+def test_depthwise_shapes(C, H, W, K, S, P, D, bias, relu):
+    s = ConvShape(2, C, H, W, C, K, K, S, P, D, C, "f32", bias, relu)
+    x, w, b = draw(s, (7, 8, 9), "normal", "kaiming", "uniform")
+    plan, y = run(s, x, w, b)
+    assert plan.path == "depthwise"
+    check_full(s, y, oracle_full(s, x, w, b))
+
+
+def test_depthwise_bf16_output_block_mode():
+    """FP32 depthwise writing BF16 (the intermediate of the depthwise-separable block)."""
+    s = ConvShape(3, 64, 21, 19, 64, 3, 3, 1, 1, 1, 64, "f32", True, True, out_bf16=True)
+    x, w, b = draw(s, (21, 22, 23))
+    plan, y = run(s, x, w, b)
+    assert plan.path == "depthwise" and y.dtype == torch.bfloat16
+    check_full(s, y, oracle_full(s, x, w, b))
+
+
+def test_depthwise_full_size_sampled_in_bench_launch_config():
+    """The same plan object twice (descriptor cache hit) and sampled points."""
+    s, x, w, b = inputs("dw")
+    plan, y1 = run(s, x, w, b)
+    plan, y2 = run(s, x, w, b, plan=plan)
+    assert torch.equal(y1, y2)
+    check_points(s, y2, x, w, b, sample_points(s, 4096, 5))

@@ -1,0 +1,112 @@
+"""GPU parity: the tcgen05 paths (implicit GEMM with TMA im2col, 1x1 GEMM,
+small-K stem kernel) against the FP64 oracle.  BF16 inputs, FP32 accumulate,
+BF16 output; tolerance |y - y_ref| <= 2e-2 * (1 + |y_ref|)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import check_full, check_points, oracle_full, run, sample_points
+from workloads import ConvShape, draw, inputs
+
+pytestmark = pytest.mark.gpu
+
+
+# ----------------------------------------------------------------- small shapes, every output
+@pytest.mark.parametrize("shape,path", [
+    # implicit GEMM, several K-steps per tap, ragged last pixel tile
+    (ConvShape(2, 64, 13, 11, 32, 3, 3, 1, 1, 1, 1, "bf16", True, True), "implicit_gemm"),
+    (ConvShape(1, 128, 9, 11, 256, 3, 3, 2, 1, 1, 1, "bf16", True, False), "implicit_gemm"),  # stride 2
+    (ConvShape(2, 64, 12, 12, 64, 5, 5, 1, 2, 1, 1, "bf16", False, True), "implicit_gemm"),   # 5x5
+    (ConvShape(2, 64, 15, 13, 64, 3, 3, 1, 3, 3, 1, "bf16", True, True), "implicit_gemm"),    # dilation 3
+    (ConvShape(2, 64, 10, 14, 64, 1, 3, 1, 1, 1, 1, "bf16", True, False), "implicit_gemm"),   # 1x3, Kh != Kw
+    (ConvShape(2, 64, 14, 10, 64, 3, 1, 1, 1, 1, 1, "bf16", True, False), "implicit_gemm"),   # 3x1
+    (ConvShape(2, 64, 11, 9, 32, 3, 3, 2, 0, 1, 1, "bf16", True, True), "implicit_gemm"),     # no padding
+    (ConvShape(1, 64, 7, 9, 32, 3, 3, 1, 1, 1, 1, "bf16", True, True), "implicit_gemm"),      # < 1 tile
+    (ConvShape(2, 128, 9, 9, 64, 1, 1, 2, 0, 1, 1, "bf16", True, True), "implicit_gemm"),     # strided 1x1
+    # groups: packed per tile, and one group spanning a tile
+    (ConvShape(2, 128, 9, 9, 64, 3, 3, 1, 1, 1, 2, "bf16", True, True), "implicit_gemm"),
+    (ConvShape(2, 512, 8, 8, 128, 3, 3, 1, 2, 2, 8, "bf16", True, True), "implicit_gemm"),
+    (ConvShape(1, 256, 8, 8, 256, 3, 3, 1, 2, 2, 4, "bf16", True, True), "implicit_gemm"),
+    # 1x1 GEMM path, including two N-tiles and a ragged pixel tail
+    (ConvShape(2, 64, 7, 9, 32, 1, 1, 1, 0, 1, 1, "bf16", True, True), "gemm_1x1"),
+    (ConvShape(3, 256, 9, 13, 512, 1, 1, 1, 0, 1, 1, "bf16", True, True), "gemm_1x1"),
+    (ConvShape(1, 128, 5, 5, 96, 1, 1, 1, 0, 1, 1, "bf16", False, False), "gemm_1x1"),
+    # small-K kernel
+    (ConvShape(2, 3, 40, 40, 32, 3, 3, 2, 1, 1, 1, "bf16", True, True), "small_k_gemm"),
+    (ConvShape(2, 3, 17, 24, 64, 3, 3, 1, 1, 1, 1, "bf16", True, False), "small_k_gemm"),
+    (ConvShape(1, 4, 6, 300, 32, 3, 3, 1, 1, 1, 1, "bf16", True, True), "small_k_gemm"),      # 3 segments
+    (ConvShape(2, 1, 20, 32, 32, 7, 7, 2, 3, 1, 1, "bf16", True, True), "small_k_gemm"),      # 49 taps
+    (ConvShape(1, 8, 12, 16, 256, 2, 2, 1, 0, 2, 1, "bf16", False, True), "small_k_gemm"),    # dilation
+])
+def test_tensor_core_small_shapes_full(shape, path):
+    x, w, b = draw(shape, (31, 32, 33))
+    plan, y = run(shape, x, w, b)
+    assert plan.path == path
+    check_full(shape, y, oracle_full(shape, x, w, b))
+
+
+def test_two_calls_same_plan_are_identical():
+    s = ConvShape(2, 128, 13, 13, 256, 3, 3, 1, 1, 1, 1, "bf16", True, True)
+    x, w, b = draw(s, (41, 42, 43))
+    plan, y1 = run(s, x, w, b)
+    plan, y2 = run(s, x, w, b, plan=plan)
+    assert torch.equal(y1, y2)
+
+
+# ----------------------------------------------------------------- full-size layers
+def test_stem_full_size_all_outputs():
+    """N=32, 3->32, 224 -> 112, 3x3 s2 p1, bias+ReLU: every output against the oracle."""
+    s, x, w, b = inputs("stem")
+    plan, y = run(s, x, w, b)
+    assert plan.path == "small_k_gemm"
+    check_full(s, y, oracle_full(s, x, w, b))
+
+
+def test_body_full_size():
+    """N=32, 128->256, 112x112, 3x3 s1 p1, bias+ReLU: image 31 in full, plus seeded
+    points over the whole batch (every corner included)."""
+    s, x, w, b = inputs("body")
+    plan, y = run(s, x, w, b)
+    assert plan.path == "implicit_gemm"
+    check_points(s, y, x, w, b, sample_points(s, 8192, 3))
+    ref31 = oracle.conv2d(x[31:32], w, b, 1, 1, 1, 1, True)
+    check_full(s, y[31:32], ref31)
+
+
+def test_pointwise_full_size():
+    s, x, w, b = inputs("pw")
+    plan, y = run(s, x, w, b)
+    assert plan.path == "gemm_1x1"
+    check_points(s, y, x, w, b, sample_points(s, 8192, 4))
+    check_full(s, y[:1], oracle.conv2d(x[:1], w, b, 1, 0, 1, 1, True))
+
+
+def test_dilated_grouped_full_size():
+    s, x, w, b = inputs("dilated")
+    plan, y = run(s, x, w, b)
+    assert plan.path == "implicit_gemm"
+    check_points(s, y, x, w, b, sample_points(s, 8192, 5))
+    check_full(s, y[:1], oracle.conv2d(x[:1], w, b, 1, 2, 2, 4, True))
+
+
+def test_depthwise_separable_block():
+    """DW 3x3 (FP32, BF16 out) then PW 1x1 256->512 + bias + ReLU on the full-size block.
+    The PW output is checked against the oracle fed the BF16 intermediate, and the
+    block end to end against the FP64 oracle of both layers."""
+    from cnn_convolution_implicit_gb300 import ConvPlan
+    from workloads import WORKLOADS, b_device, w_device, x_device
+    sd, x, wd, _ = inputs("dw")
+    sp, _, wp, bp = inputs("pw")
+    dw_plan = ConvPlan(sd.N, sd.C_in, sd.H, sd.W, sd.C_out, 3, 3, 1, 1, 1, sd.G, "f32", False, False,
+                       out_bf16=True)
+    pw_plan = ConvPlan.for_shape(sp)
+    mid = dw_plan.forward(x_device(x, "f32"), w_device(wd, "f32"))
+    y = pw_plan.forward(mid, w_device(wp, "bf16"), b_device(bp))
+    torch.cuda.synchronize()
+    mid_nchw = mid.float().cpu().permute(0, 3, 1, 2).contiguous().double().numpy()
+    pts = sample_points(sp, 4096, 6)
+    check_points(sp, y, mid_nchw, wp, bp, pts)
+    # end to end: FP64 depthwise, FP64 pointwise
+    ref_mid = oracle.conv2d(x, wd, None, 1, 1, 1, sd.G, False)
+    check_points(sp, y, ref_mid, wp, bp, pts)
