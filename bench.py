@@ -223,9 +223,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=sorted(WORKLOADS), default=None,
+                    help="time one layer alone (no oracle, no e2e); used for ncu captures")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.only:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+        r, _ = measure_layer(args.only, args.steps, args.warmup, flush, load_peaks())
+        print(json.dumps(r))
+        return
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -44,9 +44,11 @@ struct conv_plan {
     // descriptor cache, keyed by the pointers it was encoded for
     const void* cache_x;
     const void* cache_w;
+    const void* cache_y;
     bool cache_valid;
     CUtensorMap map_a;  // the type carries its own 64-byte alignment
     CUtensorMap map_b;
+    CUtensorMap map_y;
 };
 
 namespace {
@@ -133,7 +135,7 @@ bool configure_tc(conv_plan* pl, bool one_by_one) {
     t.num_n_tiles = g.C_out / n_tile;
     t.num_tiles = t.num_m_tiles * t.num_n_tiles;
     const int stage_bytes = kTcBlockM * kTcBlockK * 2 + mma_n * 128;
-    const int fixed = 1024 + 256;
+    const int fixed = 1024 + 256 + 4 * 2 * 32 * 64;  // alignment, barriers, epilogue store tiles
     int stages = (pl->smem_optin - fixed) / stage_bytes;
     if (stages > 8) stages = 8;
     if (stages < 2) return false;
@@ -166,7 +168,7 @@ bool configure_smallk(conv_plan* pl) {
     s.num_tiles = static_cast<int>(tiles);
     s.row_bytes = static_cast<int>(row_bytes);
     s.raw_bytes = static_cast<int>(raw);
-    const int fixed = 1024 + g.C_out * 128 + 512;
+    const int fixed = 1024 + g.C_out * 128 + 512 + 3 * 64 * 4 + g.C_out * 4 + 4 * 2 * 32 * 64;
     const int stage_bytes = 128 * 128 + s.raw_bytes;
     int stages = (pl->smem_optin - fixed) / stage_bytes;
     if (stages > 8) stages = 8;
@@ -184,25 +186,38 @@ bool configure_depthwise(conv_plan* pl) {
     DepthwiseParams& d = pl->dw;
     if (!(g.G == g.C_in && g.C_out == g.C_in)) return false;
     if (g.C_in % 32 != 0) return false;
-    const int t = depthwise_tile_for(g);
-    if (t == 0) return false;
+    if (!depthwise_config(g, pl->smem_optin, d)) return false;
     d.g = g;
-    d.tile = t;
-    d.tiles_h = (g.H_out + t - 1) / t;
-    d.tiles_w = (g.W_out + t - 1) / t;
-    d.cblocks = g.C_in / 32;
-    d.in_h = (t - 1) * g.S + (g.Kh - 1) * g.D + 1;
-    d.in_w = (t - 1) * g.S + (g.Kw - 1) * g.D + 1;
-    const long long blocks = static_cast<long long>(g.N) * d.tiles_h * d.tiles_w * d.cblocks;
-    if (blocks > 0x7fffffffLL) return false;
     d.relu = (pl->flags & CONV_FLAG_RELU) ? 1 : 0;
     d.out_bf16 = (pl->flags & CONV_FLAG_OUT_BF16) ? 1 : 0;
     d.status = pl->status;
     return true;
 }
 
-conv_status encode_maps(conv_plan* pl, const void* x, const void* w) {
-    if (pl->cache_valid && pl->cache_x == x && pl->cache_w == w) return CONV_OK;
+// Y store map of the tcgen05 paths: BF16, boxes of 32 channels x 32 pixels, 64-byte swizzle.
+CUresult encode_y_map(conv_plan* pl, void* y) {
+    const ConvGeom& g = pl->g;
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (pl->path == CONV_PATH_SMALL_K_GEMM) {  // {C_out, W_out, N*H_out}: a row segment never spills
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(g.C_out), static_cast<cuuint64_t>(g.W_out),
+                                    static_cast<cuuint64_t>(g.N) * g.H_out};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(g.C_out) * 2,
+                                       static_cast<cuuint64_t>(g.W_out) * g.C_out * 2};
+        return g_encode_tiled(&pl->map_y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, y, dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.C_out), static_cast<cuuint64_t>(g.pixels)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(g.C_out) * 2};
+    return g_encode_tiled(&pl->map_y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+conv_status encode_maps(conv_plan* pl, const void* x, const void* w, void* y) {
+    if (pl->cache_valid && pl->cache_x == x && pl->cache_w == w && pl->cache_y == y) return CONV_OK;
+    pl->cache_valid = false;
     if (!load_entry_points()) return CONV_ERR_CUDA;
     const ConvGeom& g = pl->g;
     CUresult r = CUDA_SUCCESS;
@@ -239,6 +254,9 @@ conv_status encode_maps(conv_plan* pl, const void* x, const void* w) {
                            bbox, bestr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return CONV_ERR_CUDA;
+        if (encode_y_map(pl, y) != CUDA_SUCCESS) return CONV_ERR_CUDA;
+    } else if (pl->path == CONV_PATH_SMALL_K_GEMM) {
+        if (encode_y_map(pl, y) != CUDA_SUCCESS) return CONV_ERR_CUDA;
     } else if (pl->path == CONV_PATH_DEPTHWISE) {
         const cuuint64_t dims[4] = {static_cast<cuuint64_t>(g.C_in), static_cast<cuuint64_t>(g.W),
                                     static_cast<cuuint64_t>(g.H), static_cast<cuuint64_t>(g.N)};
@@ -253,6 +271,7 @@ conv_status encode_maps(conv_plan* pl, const void* x, const void* w) {
     }
     pl->cache_x = x;
     pl->cache_w = w;
+    pl->cache_y = y;
     pl->cache_valid = true;
     return CONV_OK;
 }
@@ -354,33 +373,36 @@ conv_status conv_forward(conv_plan* p, const void* x, const void* w, const void*
     switch (p->path) {
         case CONV_PATH_GEMM_1X1:
         case CONV_PATH_IMPLICIT_GEMM: {
-            conv_status s = encode_maps(p, x, w);
+            conv_status s = encode_maps(p, x, w, y);
             if (s != CONV_OK) return s;
             TcGemmParams t = p->tc;
             t.bias = b;
             t.y = static_cast<__nv_bfloat16*>(y);
             const int grid = t.num_tiles < p->num_sms ? t.num_tiles : p->num_sms;
-            e = launch_tc_gemm(p->map_a, p->map_b, t, grid, st);
+            e = launch_tc_gemm(p->map_a, p->map_b, p->map_y, t, grid, st);
             break;
         }
         case CONV_PATH_SMALL_K_GEMM: {
+            conv_status cs = encode_maps(p, x, w, y);
+            if (cs != CONV_OK) return cs;
             SmallKParams s = p->sk;
             s.x = static_cast<const __nv_bfloat16*>(x);
             s.w = static_cast<const __nv_bfloat16*>(w);
             s.bias = b;
             s.y = static_cast<__nv_bfloat16*>(y);
             const int grid = s.num_tiles < p->num_sms ? s.num_tiles : p->num_sms;
-            e = launch_tc_smallk(s, grid, st);
+            e = launch_tc_smallk(p->map_y, s, grid, st);
             break;
         }
         case CONV_PATH_DEPTHWISE: {
-            conv_status s = encode_maps(p, x, w);
+            conv_status s = encode_maps(p, x, w, y);
             if (s != CONV_OK) return s;
             DepthwiseParams d = p->dw;
             d.w = static_cast<const float*>(w);
             d.bias = b;
             d.y = y;
-            e = launch_depthwise(p->map_a, d, st);
+            const int grid = d.num_tiles < p->num_sms ? d.num_tiles : p->num_sms;
+            e = launch_depthwise(p->map_a, d, grid, st);
             break;
         }
         default: {

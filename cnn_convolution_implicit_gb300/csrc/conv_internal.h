@@ -38,14 +38,16 @@ struct DepthwiseParams {
     void* y;
     int relu;
     int out_bf16;
-    int tile;           // output tile edge (tile x tile pixels) per CTA
-    int tiles_h, tiles_w, cblocks;
-    int in_h, in_w;     // halo box extent
+    int tile_h, tile_w;  // output pixels per tile (32 channels each)
+    int tiles_h, tiles_w, cblocks, num_tiles;
+    int in_h, in_w;      // halo box extent (TMA box {32, in_w, in_h, 1})
+    int stages;          // halo tiles in flight per CTA (<= 3)
+    int smem_bytes;
     unsigned* status;
 };
-// Box {32 channels, in_w, in_h, 1} of the 4-D NHWC map; 0 if the shape is not supported.
-int depthwise_tile_for(const ConvGeom& g);
-cudaError_t launch_depthwise(const CUtensorMap& x_map, const DepthwiseParams& p, cudaStream_t stream);
+// Fills the tiling fields of d; returns 0 if the shape does not fit the kernel.
+int depthwise_config(const ConvGeom& g, int smem_optin, DepthwiseParams& d);
+cudaError_t launch_depthwise(const CUtensorMap& x_map, const DepthwiseParams& p, int grid, cudaStream_t stream);
 
 // ---------------------------------------------------------------- tcgen05 GEMM (1x1 and implicit)
 constexpr int kTcBlockM = 128;    // pixels per tile (TMEM lanes)
@@ -71,11 +73,12 @@ struct TcGemmParams {
     __nv_bfloat16* y;
     unsigned* status;
 };
-cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, const TcGemmParams& p, int grid,
-                           cudaStream_t stream);
+// y_map: 2-D {C_out, pixels} BF16, box {32, 32}, 64-byte swizzle.
+cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, const CUtensorMap& y_map,
+                           const TcGemmParams& p, int grid, cudaStream_t stream);
 
 // ---------------------------------------------------------------- tcgen05 small-K (stem)
-constexpr int kSkThreads = 320;   // producer, MMA, 4 epilogue, 4 transform warps
+constexpr int kSkThreads = 448;   // producer, MMA, 4 epilogue, 8 transform warps
 
 struct SmallKParams {
     ConvGeom g;
@@ -95,6 +98,7 @@ struct SmallKParams {
     int smem_bytes;
     unsigned* status;
 };
-cudaError_t launch_tc_smallk(const SmallKParams& p, int grid, cudaStream_t stream);
+// y_map: 3-D {C_out, W_out, N*H_out} BF16, box {32, 32, 1}, 64-byte swizzle.
+cudaError_t launch_tc_smallk(const CUtensorMap& y_map, const SmallKParams& p, int grid, cudaStream_t stream);
 
 }  // namespace convgb

@@ -21,7 +21,7 @@
 // Warp roles (192 threads, one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer (one lane): A (pixels x 64 ch) and B (C_out x 64) per K-step
 //   warp 1      TMEM allocator; one lane issues tcgen05.mma and commits
-//   warps 2..5  epilogue: tcgen05.ld -> +bias -> ReLU -> BF16 -> NHWC store
+//   warps 2..5  epilogue: tcgen05.ld -> +bias -> ReLU -> BF16 -> smem -> TMA store (NHWC)
 // Shared memory holds a ring of `stages` (A, B) buffers; TMEM holds two
 // accumulators so the epilogue of tile i overlaps the MMAs of tile i+1.
 #include "conv_internal.h"
@@ -33,9 +33,12 @@ namespace {
 
 constexpr uint32_t kABytes = kTcBlockM * kTcBlockK * 2;  // 16 KB
 
+constexpr uint32_t kStageOutBytes = 32 * 64;  // one 32-row x 32-column BF16 store tile
+
 struct TcSmem {
     uint8_t* a;
     uint8_t* b;
+    uint8_t* out;  // per epilogue warp: two store tiles
     uint64_t* full;
     uint64_t* empty;
     uint64_t* tfull;
@@ -51,7 +54,8 @@ __device__ __forceinline__ TcSmem carve(uint8_t* raw, const TcGemmParams& p) {
     const uint32_t b_bytes = static_cast<uint32_t>(p.mma_n) * 128u;
     s.a = base;
     s.b = base + p.stages * kABytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s.b + p.stages * b_bytes);
+    s.out = s.b + p.stages * b_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s.out + 4 * 2 * kStageOutBytes);
     s.full = bars;
     s.empty = bars + p.stages;
     s.tfull = bars + 2 * p.stages;
@@ -77,7 +81,7 @@ __device__ __forceinline__ void sub_gemm(const TcGemmParams& p, int nt, int j, i
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_conv_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
-                   const TcGemmParams p) {
+                   const __grid_constant__ CUtensorMap y_map, const TcGemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     const TcSmem sm = carve(smem_raw, p);
     const int warp = threadIdx.x >> 5;
@@ -98,6 +102,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_barrier_init();
         tma_prefetch_desc(&a_map);
         tma_prefetch_desc(&b_map);
+        tma_prefetch_desc(&y_map);
     }
     if (warp == 1) {
         tmem_alloc(sm.tmem_slot, p.tmem_cols);
@@ -214,8 +219,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        // TMEM -> registers (+bias, ReLU, BF16) -> swizzled smem tile -> TMA store,
+        // 32 pixels x 32 channels at a time, two store tiles in flight per warp.
         const int quarter = warp & 3;  // TMEM lane quarter this warp may access
-        const int row = quarter * 32 + lane;
+        uint8_t* stg = sm.out + (warp - 2) * 2 * kStageOutBytes;
+        int sbuf = 0;
         int local = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
             const int buf = local & 1;
@@ -229,10 +237,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_after();
             const int m = tile / p.num_n_tiles;
             const int nt = tile - m * p.num_n_tiles;
-            const long long pix = static_cast<long long>(m) * kTcBlockM + row;
-            const bool valid = pix < p.g.pixels;
+            const long long row0 = static_cast<long long>(m) * kTcBlockM + quarter * 32;
+            const bool rows_exist = row0 < p.g.pixels;
             const int co0 = nt * p.n_tile;
-            __nv_bfloat16* yrow = p.y + (valid ? pix : 0) * p.g.C_out + co0;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(buf * p.n_tile);
             for (int c = 0; c < p.n_tile; c += 32) {
@@ -240,11 +247,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 __syncwarp();
                 tmem_ld32(t_row + static_cast<uint32_t>(c), v);
                 tmem_ld_wait();
-                epilogue_store32(v, p.bias ? p.bias + co0 + c : nullptr, p.relu, yrow + c, valid);
+                if (lane == 0) bulk_wait_read_le1();  // the tile written two chunks ago is free
+                __syncwarp();
+                uint8_t* dst = stg + sbuf * kStageOutBytes;
+                stage_row32(v, p.bias ? p.bias + co0 + c : nullptr, p.relu, dst, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && rows_exist) {
+                    tma_store_2d(&y_map, dst, co0 + c, static_cast<int>(row0));
+                    bulk_commit();
+                }
+                sbuf ^= 1;
             }
             tc_fence_before();
             mbar_arrive(&sm.tempty[buf]);
         }
+        if (lane == 0) bulk_wait_all();
     }
 
     __syncthreads();
@@ -255,11 +273,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 }
 
-cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, const TcGemmParams& p, int grid,
-                           cudaStream_t stream) {
+cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, const CUtensorMap& y_map,
+                           const TcGemmParams& p, int grid, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(tc_conv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
     if (e != cudaSuccess) return e;
-    tc_conv_kernel<<<grid, kTcThreads, p.smem_bytes, stream>>>(a_map, b_map, p);
+    tc_conv_kernel<<<grid, kTcThreads, p.smem_bytes, stream>>>(a_map, b_map, y_map, p);
     return cudaGetLastError();
 }
 

@@ -16,11 +16,13 @@
 // (section 26), writing the 128-byte-swizzled layout the MMA descriptor reads.
 // The whole weight matrix (C_out x K, K <= 64) stays in shared memory.
 //
-// Warp roles (320 threads, persistent):
-//   warp 0      bulk-copy producer (one lane)
-//   warp 1      TMEM allocator; one lane issues tcgen05.mma
-//   warps 2..5  epilogue (tcgen05.ld -> +bias -> ReLU -> BF16 -> NHWC store)
-//   warps 6..9  transform: raw rows -> swizzled A tile
+// Warp roles (448 threads, persistent):
+//   warp 0       bulk-copy producer (one lane)
+//   warp 1       TMEM allocator; one lane issues tcgen05.mma
+//   warps 2..5   epilogue (tcgen05.ld -> +bias -> ReLU -> BF16 -> smem -> TMA store)
+//   warps 6..13  transform: raw rows -> swizzled A tile (two threads per pixel row)
+// The 3-channel 3x3 case is compiled with its K decomposition as constants;
+// other shapes read it from a per-CTA table.
 #include "conv_internal.h"
 #include "tc_common.cuh"
 
@@ -29,11 +31,13 @@ namespace convgb {
 namespace {
 
 constexpr uint32_t kSkABytes = 128 * 128;  // 128 pixels x 64 BF16
+constexpr uint32_t kSkOutBytes = 32 * 64;  // one 32-row x 32-column BF16 store tile
 
 struct SkSmem {
     uint8_t* b;
     uint8_t* a;
     uint8_t* raw;
+    uint8_t* out;  // per epilogue warp: two store tiles
     uint64_t* raw_full;
     uint64_t* a_full;
     uint64_t* empty;
@@ -42,6 +46,10 @@ struct SkSmem {
     uint64_t* drain;
     uint32_t* tmem_slot;
     int* abort;
+    int* tab_off;    // per K index: kh*row_elems + kw*D*C_in + ci
+    int* tab_kwd;    // per K index: kw*D
+    int* tab_kh;     // per K index: kh, or -1 beyond the reduction (zero padding of K)
+    float* bias;     // [C_out] copy of the bias
 };
 
 __device__ __forceinline__ SkSmem carve(uint8_t* raw, const SmallKParams& p) {
@@ -50,7 +58,8 @@ __device__ __forceinline__ SkSmem carve(uint8_t* raw, const SmallKParams& p) {
     s.b = base;
     s.a = s.b + p.g.C_out * 128;
     s.raw = s.a + p.stages * kSkABytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s.raw + p.stages * p.raw_bytes);
+    s.out = s.raw + p.stages * p.raw_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s.out + 4 * 2 * kSkOutBytes);
     s.raw_full = bars;
     s.a_full = bars + p.stages;
     s.empty = bars + 2 * p.stages;
@@ -59,6 +68,10 @@ __device__ __forceinline__ SkSmem carve(uint8_t* raw, const SmallKParams& p) {
     s.drain = s.tempty + 2;
     s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
     s.abort = reinterpret_cast<int*>(s.tmem_slot + 1);
+    s.tab_off = s.abort + 1;
+    s.tab_kwd = s.tab_off + 64;
+    s.tab_kh = s.tab_kwd + 64;
+    s.bias = reinterpret_cast<float*>(s.tab_kh + 64);
     return s;
 }
 
@@ -85,7 +98,42 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int k) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kSkThreads, 1) tc_smallk_kernel(const SmallKParams p) {
+// Gather the 8 K-elements of chunk j for one pixel row.  CIN/KH/KW > 0: the
+// decomposition k -> (kh, kw, ci) is constant-folded; 0: read from the tables.
+template <int CIN, int KH, int KW>
+__device__ __forceinline__ uint4 gather_chunk(const SkSmem& sm, const SmallKParams& p, const uint16_t* src,
+                                              int j, int wbase, unsigned long long rowmask) {
+    uint32_t q[4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        uint32_t pair = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int k = j * 8 + e + h;
+            uint32_t v = 0;
+            if constexpr (CIN > 0) {
+                if (k < CIN * KH * KW) {
+                    const int ci = k % CIN, tap = k / CIN, kh = tap / KW, kw = tap % KW;
+                    const int wi = wbase + kw * p.g.D;
+                    if (((rowmask >> kh) & 1ull) && wi >= 0 && wi < p.g.W)
+                        v = src[kh * (p.row_bytes >> 1) + wi * CIN + ci];
+                }
+            } else {
+                const int kh = sm.tab_kh[k];
+                const int wi = wbase + sm.tab_kwd[k];
+                if (kh >= 0 && ((rowmask >> kh) & 1ull) && wi >= 0 && wi < p.g.W)
+                    v = src[wbase * p.g.C_in + sm.tab_off[k]];
+            }
+            pair |= v << (16 * h);
+        }
+        q[e >> 1] = pair;
+    }
+    return make_uint4(q[0], q[1], q[2], q[3]);
+}
+
+template <int CIN, int KH, int KW>
+__global__ void __launch_bounds__(kSkThreads, 1)
+    tc_smallk_kernel(const __grid_constant__ CUtensorMap y_map, const SmallKParams p) {
     extern __shared__ uint8_t smem_raw[];
     const SkSmem sm = carve(smem_raw, p);
     const int warp = threadIdx.x >> 5;
@@ -102,11 +150,26 @@ __global__ void __launch_bounds__(kSkThreads, 1) tc_smallk_kernel(const SmallKPa
             *reinterpret_cast<uint16_t*>(sm.b + sw128_offset(co, k)) = v;
         }
         fence_proxy_async_smem();
+        // K index -> (kh, kw, ci) decomposition, once per CTA (no divisions in the gather loop)
+        for (int k = threadIdx.x; k < 64; k += blockDim.x) {
+            if (k < p.ktot) {
+                const int ci = k % p.g.C_in, tap = k / p.g.C_in;
+                const int kh = tap / p.g.Kw, kw = tap - kh * p.g.Kw;
+                sm.tab_off[k] = kh * (p.row_bytes >> 1) + kw * p.g.D * p.g.C_in + ci;
+                sm.tab_kwd[k] = kw * p.g.D;
+                sm.tab_kh[k] = kh;
+            } else {
+                sm.tab_off[k] = 0;
+                sm.tab_kwd[k] = 0;
+                sm.tab_kh[k] = -1;
+            }
+        }
+        for (int c = threadIdx.x; c < p.g.C_out; c += blockDim.x) sm.bias[c] = p.bias ? p.bias[c] : 0.f;
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&sm.raw_full[s], 1);
-            mbar_init(&sm.a_full[s], 128);
+            mbar_init(&sm.a_full[s], 256);
             mbar_init(&sm.empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -197,7 +260,8 @@ __global__ void __launch_bounds__(kSkThreads, 1) tc_smallk_kernel(const SmallKPa
     } else if (warp < 6) {
         // ------------------------------------------------------------ epilogue
         const int quarter = warp & 3;
-        const int row = quarter * 32 + lane;
+        uint8_t* stg = sm.out + (warp - 2) * 2 * kSkOutBytes;
+        int sbuf = 0;
         int local = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
             const int buf = local & 1;
@@ -209,10 +273,8 @@ __global__ void __launch_bounds__(kSkThreads, 1) tc_smallk_kernel(const SmallKPa
             }
             tc_fence_after();
             const SkTile t = decode(p, tile);
-            const bool valid = row < t.npix;
-            const long long pix =
-                (static_cast<long long>(t.n) * p.g.H_out + t.ho) * p.g.W_out + t.wo0 + (valid ? row : 0);
-            __nv_bfloat16* yrow = p.y + pix * p.g.C_out;
+            const int wo_row0 = t.wo0 + quarter * 32;          // first output column of this warp's rows
+            const bool rows_exist = quarter * 32 < t.npix;
             const uint32_t t_row =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * n_tile);
             for (int c = 0; c < n_tile; c += 32) {
@@ -220,17 +282,29 @@ __global__ void __launch_bounds__(kSkThreads, 1) tc_smallk_kernel(const SmallKPa
                 __syncwarp();
                 tmem_ld32(t_row + static_cast<uint32_t>(c), v);
                 tmem_ld_wait();
-                epilogue_store32(v, p.bias ? p.bias + c : nullptr, p.relu, yrow + c, valid);
+                if (lane == 0) bulk_wait_read_le1();
+                __syncwarp();
+                uint8_t* dst = stg + sbuf * kSkOutBytes;
+                stage_row32(v, p.bias ? sm.bias + c : nullptr, p.relu, dst, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && rows_exist) {  // columns past W_out fall outside the map: not written
+                    tma_store_3d(&y_map, dst, c, wo_row0, t.n * p.g.H_out + t.ho);
+                    bulk_commit();
+                }
+                sbuf ^= 1;
             }
             tc_fence_before();
             mbar_arrive(&sm.tempty[buf]);
         }
+        if (lane == 0) bulk_wait_all();
     } else {
         // ------------------------------------------------------------ transform (im2col in smem)
-        const int r = threadIdx.x - 192;  // A row = pixel within the tile
+        const int r = (threadIdx.x - 192) & 127;   // A row = pixel within the tile
+        const int half = (threadIdx.x - 192) >> 7;  // this thread builds chunks half, half+2, ...
         const uint16_t* raw16 = reinterpret_cast<const uint16_t*>(sm.raw);
-        const int row_elems = p.row_bytes >> 1;
         const int raw_elems = p.raw_bytes >> 1;
+        const int nchunks = 2 * p.kmma;
         int stage = 0;
         uint32_t phase = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
@@ -241,32 +315,25 @@ __global__ void __launch_bounds__(kSkThreads, 1) tc_smallk_kernel(const SmallKPa
             const SkTile t = decode(p, tile);
             const uint16_t* src = raw16 + stage * raw_elems;
             uint8_t* arow = sm.a + stage * kSkABytes;
-            const int wo = t.wo0 + r;
-            const bool pix_ok = r < t.npix;
-            for (int j = 0; j < 2 * p.kmma; ++j) {  // 16-byte chunks of 8 K-elements
-                uint32_t q[4];
+            // input rows of this tile that exist (the rest read as zero)
+            unsigned long long rowmask = 0;
+            for (int kh = 0; kh < p.g.Kh; ++kh) {
+                const int hi = t.ho * p.g.S - p.g.P + kh * p.g.D;
+                if (hi >= 0 && hi < p.g.H) rowmask |= 1ull << kh;
+            }
+            const int wbase = (t.wo0 + r) * p.g.S - p.g.P;  // input column of tap kw = 0
+            if (r >= t.npix) rowmask = 0;                   // rows past the segment: zeros
+            if constexpr (CIN > 0) {
+                constexpr int kChunks = ((CIN * KH * KW + 15) / 16) * 2;
 #pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    uint32_t pair = 0;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int k = j * 8 + e + h;
-                        uint32_t v = 0;
-                        if (pix_ok && k < p.ktot) {
-                            const int ci = k % p.g.C_in;
-                            const int tap = k / p.g.C_in;
-                            const int kh = tap / p.g.Kw;
-                            const int kw = tap - kh * p.g.Kw;
-                            const int hi = t.ho * p.g.S - p.g.P + kh * p.g.D;
-                            const int wi = wo * p.g.S - p.g.P + kw * p.g.D;
-                            if (hi >= 0 && hi < p.g.H && wi >= 0 && wi < p.g.W)
-                                v = src[kh * row_elems + wi * p.g.C_in + ci];
-                        }
-                        pair |= v << (16 * h);
-                    }
-                    q[e >> 1] = pair;
-                }
-                *reinterpret_cast<uint4*>(arow + sw128_offset(r, j * 8)) = make_uint4(q[0], q[1], q[2], q[3]);
+                for (int j = 0; j < kChunks; ++j)
+                    if ((j & 1) == half)
+                        *reinterpret_cast<uint4*>(arow + sw128_offset(r, j * 8)) =
+                            gather_chunk<CIN, KH, KW>(sm, p, src, j, wbase, rowmask);
+            } else {
+                for (int j = half; j < nchunks; j += 2)
+                    *reinterpret_cast<uint4*>(arow + sw128_offset(r, j * 8)) =
+                        gather_chunk<0, 0, 0>(sm, p, src, j, wbase, rowmask);
             }
             fence_proxy_async_smem();
             mbar_arrive(&sm.a_full[stage]);
@@ -285,12 +352,18 @@ __global__ void __launch_bounds__(kSkThreads, 1) tc_smallk_kernel(const SmallKPa
     }
 }
 
-cudaError_t launch_tc_smallk(const SmallKParams& p, int grid, cudaStream_t stream) {
-    cudaError_t e =
-        cudaFuncSetAttribute(tc_smallk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
+template <int CIN, int KH, int KW>
+static cudaError_t launch_sk(const CUtensorMap& y_map, const SmallKParams& p, int grid, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(tc_smallk_kernel<CIN, KH, KW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         p.smem_bytes);
     if (e != cudaSuccess) return e;
-    tc_smallk_kernel<<<grid, kSkThreads, p.smem_bytes, stream>>>(p);
+    tc_smallk_kernel<CIN, KH, KW><<<grid, kSkThreads, p.smem_bytes, stream>>>(y_map, p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_tc_smallk(const CUtensorMap& y_map, const SmallKParams& p, int grid, cudaStream_t stream) {
+    if (p.g.C_in == 3 && p.g.Kh == 3 && p.g.Kw == 3) return launch_sk<3, 3, 3>(y_map, p, grid, stream);
+    return launch_sk<0, 0, 0>(y_map, p, grid, stream);
 }
 
 }  // namespace convgb
