@@ -186,7 +186,7 @@ bool configure_depthwise(conv_plan* pl) {
     DepthwiseParams& d = pl->dw;
     if (!(g.G == g.C_in && g.C_out == g.C_in)) return false;
     if (g.C_in % 32 != 0) return false;
-    if (!depthwise_config(g, pl->smem_optin, d)) return false;
+    if (!depthwise_config(g, pl->smem_optin, pl->num_sms, d)) return false;
     d.g = g;
     d.relu = (pl->flags & CONV_FLAG_RELU) ? 1 : 0;
     d.out_bf16 = (pl->flags & CONV_FLAG_OUT_BF16) ? 1 : 0;
@@ -401,8 +401,7 @@ conv_status conv_forward(conv_plan* p, const void* x, const void* w, const void*
             d.w = static_cast<const float*>(w);
             d.bias = b;
             d.y = y;
-            const int grid = d.num_tiles < p->num_sms ? d.num_tiles : p->num_sms;
-            e = launch_depthwise(p->map_a, d, grid, st);
+            e = launch_depthwise(p->map_a, d, st);
             break;
         }
         default: {

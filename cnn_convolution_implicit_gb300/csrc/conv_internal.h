@@ -41,13 +41,15 @@ struct DepthwiseParams {
     int tile_h, tile_w;  // output pixels per tile (32 channels each)
     int tiles_h, tiles_w, cblocks, num_tiles;
     int in_h, in_w;      // halo box extent (TMA box {32, in_w, in_h, 1})
-    int stages;          // halo tiles in flight per CTA (<= 3)
+    int stages;          // halo tiles in flight per CTA (<= 8)
     int smem_bytes;
+    int fixed_cb;        // each CTA keeps one channel block (grid a multiple of cblocks)
+    int grid;
     unsigned* status;
 };
 // Fills the tiling fields of d; returns 0 if the shape does not fit the kernel.
-int depthwise_config(const ConvGeom& g, int smem_optin, DepthwiseParams& d);
-cudaError_t launch_depthwise(const CUtensorMap& x_map, const DepthwiseParams& p, int grid, cudaStream_t stream);
+int depthwise_config(const ConvGeom& g, int smem_optin, int num_sms, DepthwiseParams& d);
+cudaError_t launch_depthwise(const CUtensorMap& x_map, const DepthwiseParams& p, cudaStream_t stream);
 
 // ---------------------------------------------------------------- tcgen05 GEMM (1x1 and implicit)
 constexpr int kTcBlockM = 128;    // pixels per tile (TMEM lanes)

@@ -14,12 +14,13 @@
 //
 // The kernel is persistent (one CTA per SM) and keeps a ring of `stages` halo
 // tiles in flight, so HBM reads of the next tiles overlap the arithmetic and
-// stores of the current one.  Each of the 256 threads owns 4 channels (one
-// float4: 128-bit shared loads and global stores) of one output column and
-// walks a run of output rows.  For stride 1 / dilation 1 it keeps the last Kh-1 input rows of its
-// Kh x Kw window in registers and reads one new row per output row (lesson 9,
-// sections 6 and 17-18: input reuse held in registers, several outputs per
-// thread); weights live in registers.
+// stores of the current one.  When the channel blocks fit in the grid, every
+// CTA stays on one 32-channel block, so its weights are read once.  Each of
+// the 256 threads owns 4 channels (one float4: 128-bit shared loads and global
+// stores) of one output column and walks a run of output rows.  For stride 1
+// and dilation 1 with a 3x3 kernel it keeps the last two input rows of its
+// window in registers and reads one new row per output row (lesson 9, sections
+// 6 and 17-18: input reuse held in registers, several outputs per thread).
 #include "conv_internal.h"
 #include "ptx.cuh"
 
@@ -29,6 +30,7 @@ namespace {
 
 constexpr int kDwChannels = 32;  // channels per tile: one 128-byte TMA row
 constexpr int kDwThreads = 256;  // 8 channel quads x TW columns x (32 / TW) row groups
+constexpr int kDwMaxStages = 8;
 
 __device__ __forceinline__ void fma4(float4& acc, const float4& a, const float4& w) {
     acc.x = fmaf(a.x, w.x, acc.x);
@@ -38,40 +40,90 @@ __device__ __forceinline__ void fma4(float4& acc, const float4& a, const float4&
 }
 
 struct DwTile {
-    int n, ho0, wo0, c0;
+    int n, ho0, wo0, cb;
 };
 
-__device__ __forceinline__ DwTile dw_decode(const DepthwiseParams& p, int t) {
+// Tile `i` of this CTA.  With fixed_cb the CTA's channel block is
+// blockIdx.x % cblocks and it walks the spatial tiles; otherwise it walks the
+// flat tile list (channel block fastest).
+__device__ __forceinline__ DwTile dw_tile(const DepthwiseParams& p, int i) {
+    int t, cb;
+    if (p.fixed_cb) {
+        const int per = gridDim.x / p.cblocks;
+        cb = blockIdx.x % p.cblocks;
+        t = blockIdx.x / p.cblocks + i * per;
+    } else {
+        const int flat = blockIdx.x + i * gridDim.x;
+        cb = flat % p.cblocks;
+        t = flat / p.cblocks;
+    }
     DwTile d;
-    const int cb = t % p.cblocks;
-    t /= p.cblocks;
+    d.cb = cb;
     const int tw = t % p.tiles_w;
     t /= p.tiles_w;
     const int th = t % p.tiles_h;
     d.n = t / p.tiles_h;
     d.ho0 = th * p.tile_h;
     d.wo0 = tw * p.tile_w;
-    d.c0 = cb * kDwChannels;
     return d;
 }
 
-__device__ __forceinline__ void dw_store(const DepthwiseParams& p, int n, int ho, int wo, int c, float4 acc) {
-    if (p.relu) {
+__device__ __forceinline__ int dw_count(const DepthwiseParams& p) {
+    if (p.fixed_cb) {
+        const int per = gridDim.x / p.cblocks;
+        const int first = blockIdx.x / p.cblocks;
+        const int spatial = p.num_tiles / p.cblocks;
+        return first < spatial ? (spatial - 1 - first) / per + 1 : 0;
+    }
+    return blockIdx.x < p.num_tiles ? (p.num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+}
+
+struct DwOut {
+    float* yf;
+    __nv_bfloat16* yb;
+    long long stride;  // elements between consecutive output rows
+    int relu, out_bf16;
+};
+
+__device__ __forceinline__ void dw_emit(DwOut& o, float4 acc, bool ok) {
+    if (o.relu) {
         acc.x = fmaxf(acc.x, 0.f);
         acc.y = fmaxf(acc.y, 0.f);
         acc.z = fmaxf(acc.z, 0.f);
         acc.w = fmaxf(acc.w, 0.f);
     }
-    if (ho >= p.g.H_out || wo >= p.g.W_out) return;
-    const long long o = ((static_cast<long long>(n) * p.g.H_out + ho) * p.g.W_out + wo) * p.g.C_out + c;
-    if (p.out_bf16) {
-        uint2 q;
-        q.x = pack_bf16x2(acc.x, acc.y);
-        q.y = pack_bf16x2(acc.z, acc.w);
-        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.y) + o) = q;
-    } else {
-        *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.y) + o) = acc;
+    if (ok) {
+        if (o.out_bf16) {
+            uint2 q;
+            q.x = pack_bf16x2(acc.x, acc.y);
+            q.y = pack_bf16x2(acc.z, acc.w);
+            *reinterpret_cast<uint2*>(o.yb) = q;
+        } else {
+            *reinterpret_cast<float4*>(o.yf) = acc;
+        }
     }
+    o.yf += o.stride;
+    o.yb += o.stride;
+}
+
+// One output row of the 3x3 stride-1 window: rows (r0, r1) from registers,
+// the new row r2 read from shared memory into `n`.
+__device__ __forceinline__ float4 dw_row3(const float4 (&w)[9], const float4& bias, const float4 (&r0)[3],
+                                          const float4 (&r1)[3], float4 (&n)[3], const float4* src) {
+    n[0] = src[0];
+    n[1] = src[8];
+    n[2] = src[16];
+    float4 acc = bias;
+    fma4(acc, r0[0], w[0]);
+    fma4(acc, r0[1], w[1]);
+    fma4(acc, r0[2], w[2]);
+    fma4(acc, r1[0], w[3]);
+    fma4(acc, r1[1], w[4]);
+    fma4(acc, r1[2], w[5]);
+    fma4(acc, n[0], w[6]);
+    fma4(acc, n[1], w[7]);
+    fma4(acc, n[2], w[8]);
+    return acc;
 }
 
 }  // namespace
@@ -81,8 +133,9 @@ template <int K, int TW>
 __global__ void __launch_bounds__(kDwThreads, 1)
     depthwise_kernel(const __grid_constant__ CUtensorMap x_map, const DepthwiseParams p) {
     constexpr int kRowGroups = kDwThreads / (8 * TW);
+    constexpr int kTaps = K > 0 ? K * K : 1;
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    __shared__ uint64_t full[8];
+    __shared__ uint64_t full[kDwMaxStages];
     __shared__ int abort_flag;
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
 
@@ -90,9 +143,7 @@ __global__ void __launch_bounds__(kDwThreads, 1)
     const int Kw = K > 0 ? K : p.g.Kw;
     const int S = p.g.S, D = p.g.D;
     const int stage_bytes = p.in_h * p.in_w * kDwChannels * 4;
-    const uint32_t box_bytes = static_cast<uint32_t>(stage_bytes);
-    const int num_tiles = p.num_tiles;
-    const int my_count = blockIdx.x < num_tiles ? (num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int my_count = dw_count(p);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) mbar_init(&full[s], 1);
@@ -100,13 +151,14 @@ __global__ void __launch_bounds__(kDwThreads, 1)
         fence_barrier_init();
     }
     __syncthreads();
-    int issued = 0;            // tiles whose TMA thread 0 has issued
-    auto issue = [&](int i) {  // TMA of this CTA's i-th tile into slot i % stages
+    int issued = 0;  // tiles whose TMA thread 0 has issued
+    auto issue = [&](int i) {
         const int slot = i % p.stages;
         issued = i + 1;
-        const DwTile t = dw_decode(p, blockIdx.x + i * gridDim.x);
-        mbar_arrive_expect_tx(&full[slot], box_bytes);
-        tma_load_4d(ring + slot * stage_bytes, &x_map, &full[slot], t.c0, t.wo0 * S - p.g.P, t.ho0 * S - p.g.P, t.n);
+        const DwTile t = dw_tile(p, i);
+        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(stage_bytes));
+        tma_load_4d(ring + slot * stage_bytes, &x_map, &full[slot], t.cb * kDwChannels, t.wo0 * S - p.g.P,
+                    t.ho0 * S - p.g.P, t.n);
     };
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&x_map);
@@ -118,22 +170,25 @@ __global__ void __launch_bounds__(kDwThreads, 1)
     const int rg = (threadIdx.x >> 3) / TW;
     const int rows = p.tile_h / kRowGroups;
     const bool rolling = K == 3 && S == 1 && D == 1;
-    constexpr int kTaps = K > 0 ? K * K : 1;
     const int in_row4 = p.in_w * (kDwChannels / 4);  // float4 per input row
 
+    float4 wreg[kTaps];
+    float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);
+    int cur_cb = -1;
+
     for (int i = 0; i < my_count; ++i) {
-        const DwTile t = dw_decode(p, blockIdx.x + i * gridDim.x);
-        const int c = t.c0 + 4 * c4;
-        // weights and bias of this thread's 4 channels (L1-resident), before the wait
-        float4 wreg[kTaps];
-        if (K > 0) {
+        const DwTile t = dw_tile(p, i);
+        const int c = t.cb * kDwChannels + 4 * c4;
+        if (t.cb != cur_cb) {  // weights and bias of this thread's 4 channels
+            cur_cb = t.cb;
+            if (K > 0) {
 #pragma unroll
-            for (int k = 0; k < kTaps; ++k)
-                wreg[k] = make_float4(__ldg(p.w + (c + 0) * kTaps + k), __ldg(p.w + (c + 1) * kTaps + k),
-                                      __ldg(p.w + (c + 2) * kTaps + k), __ldg(p.w + (c + 3) * kTaps + k));
+                for (int k = 0; k < kTaps; ++k)
+                    wreg[k] = make_float4(__ldg(p.w + (c + 0) * kTaps + k), __ldg(p.w + (c + 1) * kTaps + k),
+                                          __ldg(p.w + (c + 2) * kTaps + k), __ldg(p.w + (c + 3) * kTaps + k));
+            }
+            if (p.bias) bias = __ldg(reinterpret_cast<const float4*>(p.bias + c));
         }
-        float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (p.bias) bias = __ldg(reinterpret_cast<const float4*>(p.bias + c));
 
         const int slot = i % p.stages;
         const bool ok = mbar_wait(&full[slot], static_cast<uint32_t>((i / p.stages) & 1), &abort_flag);
@@ -144,57 +199,47 @@ __global__ void __launch_bounds__(kDwThreads, 1)
         const float4* t4 = reinterpret_cast<const float4*>(ring + slot * stage_bytes);
         const int wo = t.wo0 + col;
         const int lr0 = rg * rows;
+        const int ho_first = t.ho0 + lr0;
+        const int nrows = min(rows, p.g.H_out - ho_first);  // rows of this thread inside the image
+        const bool col_ok = wo < p.g.W_out;
+        DwOut o;
+        const long long o0 =
+            ((static_cast<long long>(t.n) * p.g.H_out + ho_first) * p.g.W_out + wo) * p.g.C_out + c;
+        o.yf = reinterpret_cast<float*>(p.y) + o0;
+        o.yb = reinterpret_cast<__nv_bfloat16*>(p.y) + o0;
+        o.stride = static_cast<long long>(p.g.W_out) * p.g.C_out;
+        o.relu = p.relu;
+        o.out_bf16 = p.out_bf16;
 
-        if (rolling) {
-            // window rows r, r+1 held in registers; one new input row per output row
-            const float4* base = t4 + (lr0 * p.in_w + col) * (kDwChannels / 4) + c4;
-            float4 a0 = base[0], a1 = base[8], a2 = base[16];
-            float4 b0 = base[in_row4], b1 = base[in_row4 + 8], b2 = base[in_row4 + 16];
-            const int ho_first = t.ho0 + lr0;
-            const int nrows = min(rows, p.g.H_out - ho_first);  // rows of this thread inside the image
-            const long long row_stride = static_cast<long long>(p.g.W_out) * p.g.C_out;
-            const long long o0 = ((static_cast<long long>(t.n) * p.g.H_out + ho_first) * p.g.W_out + wo) * p.g.C_out + c;
-            const bool col_ok = wo < p.g.W_out;
-            float* yf = reinterpret_cast<float*>(p.y) + o0;
-            __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(p.y) + o0;
-            const float4* cr = base + 2 * in_row4;
-#pragma unroll 2
-            for (int r = 0; r < nrows; ++r) {
-                const float4 d0 = cr[0], d1 = cr[8], d2 = cr[16];
-                cr += in_row4;
-                float4 acc = bias;
-                fma4(acc, a0, wreg[0]);
-                fma4(acc, a1, wreg[1 % kTaps]);
-                fma4(acc, a2, wreg[2 % kTaps]);
-                fma4(acc, b0, wreg[3 % kTaps]);
-                fma4(acc, b1, wreg[4 % kTaps]);
-                fma4(acc, b2, wreg[5 % kTaps]);
-                fma4(acc, d0, wreg[6 % kTaps]);
-                fma4(acc, d1, wreg[7 % kTaps]);
-                fma4(acc, d2, wreg[8 % kTaps]);
-                if (p.relu) {
-                    acc.x = fmaxf(acc.x, 0.f);
-                    acc.y = fmaxf(acc.y, 0.f);
-                    acc.z = fmaxf(acc.z, 0.f);
-                    acc.w = fmaxf(acc.w, 0.f);
+        bool done = false;
+        if constexpr (K == 3) {
+            if (rolling) {
+                // three register rows cycle through the roles (top, middle, new): no copies
+                const float4* src = t4 + (lr0 * p.in_w + col) * (kDwChannels / 4) + c4;
+                float4 ra[3] = {src[0], src[8], src[16]};
+                src += in_row4;
+                float4 rb[3] = {src[0], src[8], src[16]};
+                src += in_row4;
+                float4 rc[3];
+                int r = 0;
+                for (; r + 3 <= nrows; r += 3) {
+                    dw_emit(o, dw_row3(wreg, bias, ra, rb, rc, src), col_ok);
+                    src += in_row4;
+                    dw_emit(o, dw_row3(wreg, bias, rb, rc, ra, src), col_ok);
+                    src += in_row4;
+                    dw_emit(o, dw_row3(wreg, bias, rc, ra, rb, src), col_ok);
+                    src += in_row4;
                 }
-                if (col_ok) {
-                    if (p.out_bf16) {
-                        uint2 q;
-                        q.x = pack_bf16x2(acc.x, acc.y);
-                        q.y = pack_bf16x2(acc.z, acc.w);
-                        *reinterpret_cast<uint2*>(yb) = q;
-                    } else {
-                        *reinterpret_cast<float4*>(yf) = acc;
-                    }
+                if (r < nrows) {
+                    dw_emit(o, dw_row3(wreg, bias, ra, rb, rc, src), col_ok);
+                    src += in_row4;
+                    if (r + 1 < nrows) dw_emit(o, dw_row3(wreg, bias, rb, rc, ra, src), col_ok);
                 }
-                yf += row_stride;
-                yb += row_stride;
-                a0 = b0; a1 = b1; a2 = b2;
-                b0 = d0; b1 = d1; b2 = d2;
+                done = true;
             }
-        } else {
-            for (int r = 0; r < rows; ++r) {
+        }
+        if (!done) {
+            for (int r = 0; r < nrows; ++r) {
                 const int lr = lr0 + r;
                 float4 acc = bias;
                 for (int kh = 0; kh < Kh; ++kh)
@@ -210,7 +255,7 @@ __global__ void __launch_bounds__(kDwThreads, 1)
                         }
                         fma4(acc, t4[(ih * p.in_w + iw) * (kDwChannels / 4) + c4], wv);
                     }
-                dw_store(p, t.n, t.ho0 + lr, wo, c, acc);
+                dw_emit(o, acc, col_ok);
             }
         }
         __syncthreads();  // every thread is done with this slot
@@ -226,7 +271,7 @@ __global__ void __launch_bounds__(kDwThreads, 1)
     }
 }
 
-int depthwise_config(const ConvGeom& g, int smem_optin, DepthwiseParams& d) {
+int depthwise_config(const ConvGeom& g, int smem_optin, int num_sms, DepthwiseParams& d) {
     // Tile width 8 or 16 columns (a warp never straddles two row groups),
     // height from {32, 28, 24, 16} with the least ragged-edge waste, then as
     // many ring stages (<= 8) as fit in shared memory; shrink the height if
@@ -243,7 +288,7 @@ int depthwise_config(const ConvGeom& g, int smem_optin, DepthwiseParams& d) {
         const int in_w = (tw - 1) * g.S + (g.Kw - 1) * g.D + 1;
         const long long stage = static_cast<long long>(in_h) * in_w * kDwChannels * 4;
         long long stages = (smem_optin - 1024 - 128) / stage;
-        if (stages > 8) stages = 8;
+        if (stages > kDwMaxStages) stages = kDwMaxStages;
         if (in_h <= 256 && in_w <= 256 && (stages >= 2 || (th <= rg && stages >= 1))) {
             d.tile_w = tw;
             d.tile_h = th;
@@ -262,22 +307,28 @@ int depthwise_config(const ConvGeom& g, int smem_optin, DepthwiseParams& d) {
     const long long tiles = static_cast<long long>(g.N) * d.tiles_h * d.tiles_w * d.cblocks;
     if (tiles > 0x7fffffffLL) return 0;
     d.num_tiles = static_cast<int>(tiles);
+    // grid: one CTA per SM; a multiple of the channel blocks when they fit, so
+    // each CTA keeps one channel block (and its weights) for its whole run
+    d.fixed_cb = d.cblocks <= num_sms ? 1 : 0;
+    int grid = d.fixed_cb ? (num_sms / d.cblocks) * d.cblocks : num_sms;
+    if (grid > d.num_tiles) grid = d.num_tiles;  // still a multiple of cblocks
+    d.grid = grid;
     return 1;
 }
 
 template <int K, int TW>
-static cudaError_t launch_dw(const CUtensorMap& x_map, const DepthwiseParams& p, int grid, cudaStream_t stream) {
+static cudaError_t launch_dw(const CUtensorMap& x_map, const DepthwiseParams& p, cudaStream_t stream) {
     cudaError_t e =
         cudaFuncSetAttribute(depthwise_kernel<K, TW>, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
     if (e != cudaSuccess) return e;
-    depthwise_kernel<K, TW><<<grid, kDwThreads, p.smem_bytes, stream>>>(x_map, p);
+    depthwise_kernel<K, TW><<<p.grid, kDwThreads, p.smem_bytes, stream>>>(x_map, p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_depthwise(const CUtensorMap& x_map, const DepthwiseParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_depthwise(const CUtensorMap& x_map, const DepthwiseParams& p, cudaStream_t stream) {
     const bool k3 = p.g.Kh == 3 && p.g.Kw == 3;
-    if (p.tile_w == 8) return k3 ? launch_dw<3, 8>(x_map, p, grid, stream) : launch_dw<0, 8>(x_map, p, grid, stream);
-    return k3 ? launch_dw<3, 16>(x_map, p, grid, stream) : launch_dw<0, 16>(x_map, p, grid, stream);
+    if (p.tile_w == 8) return k3 ? launch_dw<3, 8>(x_map, p, stream) : launch_dw<0, 8>(x_map, p, stream);
+    return k3 ? launch_dw<3, 16>(x_map, p, stream) : launch_dw<0, 16>(x_map, p, stream);
 }
 
 }  // namespace convgb
