@@ -61,11 +61,22 @@ def load_traffic():
     return out
 
 
-def kernel_source_hash():
+# Source files that make up each kernel (for matching ncu traffic to the code it was taken from).
+KERNEL_SOURCES = {
+    "body": ["tc_gemm.cu", "tc_common.cuh", "ptx.cuh", "conv_internal.h"],
+    "pw": ["tc_gemm.cu", "tc_common.cuh", "ptx.cuh", "conv_internal.h"],
+    "dilated": ["tc_gemm.cu", "tc_common.cuh", "ptx.cuh", "conv_internal.h"],
+    "stem": ["tc_smallk.cu", "tc_common.cuh", "ptx.cuh", "conv_internal.h"],
+    "dw": ["depthwise.cu", "ptx.cuh", "conv_internal.h"],
+    "tiny_f32": ["direct.cu", "conv_internal.h"],
+}
+
+
+def kernel_source_hash(workload):
     import hashlib
     h = hashlib.sha256()
     cdir = os.path.join(ROOT, "cnn_convolution_implicit_gb300", "csrc")
-    for name in sorted(os.listdir(cdir)):
+    for name in KERNEL_SOURCES[workload]:
         with open(os.path.join(cdir, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:12]
@@ -91,7 +102,8 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
-        except (OSError, FileNotFoundError):
+        except (OSError, FileNotFoundError) as e:
+            sys.stderr.write("clock sampler unavailable: %s\n" % e)
             self.proc = None
 
     def _read(self):
@@ -122,6 +134,8 @@ class ClockSampler:
                 if v.lower() in ("active", "1", "yes"):
                     reasons.add(name)
         if not sm:
+            sys.stderr.write("clock sampler: no parsable nvidia-smi lines (%d read): %r\n"
+                             % (len(self.lines), self.lines[:3]))
             return None
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "samples": len(sm),
                 "reasons": sorted(reasons)}
@@ -170,7 +184,8 @@ def measure_layer(name, steps, warmup, flush, peaks):
     bound = "hbm" if s.flops / s.algorithmic_bytes < peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9) \
         or s.dtype == "f32" else "tensor"
     res = {"workload": name, "kernel": plan.path, "ms": t * 1e3, "tflops": tflops, "gbs": gbs,
-           "bound": bound, "flops": s.flops, "bytes": s.algorithmic_bytes, "launches": steps}
+           "bound": bound, "flops": s.flops, "bytes": s.algorithmic_bytes, "launches": steps,
+           "source_hash": kernel_source_hash(name)}
     if bound == "tensor":
         res["frac"] = tflops / peaks["bf16_tflops"]
     else:
@@ -178,41 +193,51 @@ def measure_layer(name, steps, warmup, flush, peaks):
     return res, (s, plan, host, (xd, wd, bd, y))
 
 
-def oracle_sample(name, seconds_target=12.0):
-    """Time the FP64 oracle (as it stands) on a bounded sample of a workload's
-    outputs, on this host's cores.  Returns (TFLOP/s, GB/s-equivalent, threads, sample text)."""
-    import oracle
-    s, x, w, b = inputs(name)
-    rng = np.random.default_rng(77)
-    per_pt_flops = 2 * (s.C_in // s.G) * s.Kh * s.Kw
+class OracleSampler:
+    """Times the FP64 oracle (as it stands, never tuned) on bounded seeded samples
+    of a workload's outputs, on this host's cores.  Inputs are drawn once."""
 
-    def pts(n):
-        return np.stack([rng.integers(0, s.N, n), rng.integers(0, s.C_out, n),
-                         rng.integers(0, s.H_out, n), rng.integers(0, s.W_out, n)], 1)
+    def __init__(self, name):
+        import oracle
+        self.oracle = oracle
+        self.name = name
+        s, x, w, b = inputs(name)
+        self.s = s
+        self.xf = np.ascontiguousarray(x, dtype=np.float64)
+        self.wf = np.ascontiguousarray(w, dtype=np.float64)
+        self.bf = None if b is None else np.ascontiguousarray(b, dtype=np.float64)
+        self.rng = np.random.default_rng(77)
+        self.per_pt_flops = 2 * (s.C_in // s.G) * s.Kh * s.Kw
+        self.rate = None  # points per second
+        n = 2048
+        while True:  # calibrate on growing samples until one takes 0.5 s
+            dt = self._run(n)
+            if dt > 0.5 or n >= 1 << 26:
+                break
+            n *= 4
+        self.rate = n / dt
 
-    xf = np.ascontiguousarray(x, dtype=np.float64)
-    wf = np.ascontiguousarray(w, dtype=np.float64)
-    bf = None if b is None else np.ascontiguousarray(b, dtype=np.float64)
-    n = 2048
-    while True:
-        p = pts(n)
+    def _points(self, n):
+        s = self.s
+        return np.stack([self.rng.integers(0, s.N, n), self.rng.integers(0, s.C_out, n),
+                         self.rng.integers(0, s.H_out, n), self.rng.integers(0, s.W_out, n)], 1)
+
+    def _run(self, n):
+        s = self.s
+        p = self._points(n)
         t0 = time.perf_counter()
-        oracle.conv2d_points(xf, wf, bf, p, s.S, s.P, s.D, s.G, s.relu)
-        dt = time.perf_counter() - t0
-        if dt > 1.0 or n >= 1 << 26:
-            break
-        n *= 4
-    n_final = max(n, int(n * seconds_target / max(dt, 1e-6)))
-    p = pts(n_final)
-    t0 = time.perf_counter()
-    oracle.conv2d_points(xf, wf, bf, p, s.S, s.P, s.D, s.G, s.relu)
-    dt = time.perf_counter() - t0
-    flops = per_pt_flops * n_final
-    frac_outputs = n_final / (s.pixels * s.C_out)
-    bytes_equiv = s.algorithmic_bytes * frac_outputs
-    sample = "%d seeded output points of %s (%.4f%% of the layer's outputs), FP64, %.1f s" % (
-        n_final, name, 100 * frac_outputs, dt)
-    return flops / dt / 1e12, bytes_equiv / dt / 1e9, oracle.max_threads(), sample, dt
+        self.oracle.conv2d_points(self.xf, self.wf, self.bf, p, s.S, s.P, s.D, s.G, s.relu)
+        return time.perf_counter() - t0
+
+    def step(self, seconds):
+        """One bounded sample of about `seconds`; returns (TFLOP/s, threads, description)."""
+        s = self.s
+        n = max(256, int(self.rate * seconds))
+        dt = self._run(n)
+        frac = n / (s.pixels * s.C_out)
+        sample = "%d seeded output points of %s (%.4f%% of the layer's outputs), FP64, %.2f s" % (
+            n, self.name, 100 * frac, dt)
+        return self.per_pt_flops * n / dt / 1e12, self.oracle.max_threads(), sample
 
 
 # ----------------------------------------------------------------------------- main
@@ -248,17 +273,24 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        tf, _, cores, sample, _ = oracle_sample("body")
-        per_step = []
-        for _ in range(max(1, min(args.steps, 3))):
-            per_step.append(tf)
-        v = float(np.mean(per_step))
+        # the oracle as it stands, on this host's cores; each step is a bounded
+        # seeded sample of the body layer's outputs, sized so the run takes ~1-2 min
+        per_step_s = max(0.5, 90.0 / (args.steps + args.warmup))
+        sampler = OracleSampler("body")
+        for _ in range(args.warmup):
+            sampler.step(0.2)
+        vals, samples = [], []
+        for _ in range(args.steps):
+            tf, cores, sample = sampler.step(per_step_s)
+            vals.append(tf)
+            samples.append(sample)
+        v = float(np.mean(vals))
         line = {"impl": "reference", "metric": "conv2d TFLOP/s (body 3x3 layer)", "value": v,
-                "unit": "TFLOP/s", "n_gpus": 0, "steps": len(per_step), "warmup": 0,
+                "unit": "TFLOP/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
                 "higher_is_better": True, "dtype": "f64", "data": "synthetic (seeded)",
                 "config": config,
                 "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                                 "sample": sample},
+                                 "sample": "per step: " + samples[-1]},
                 "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -325,23 +357,23 @@ def main():
         others[name] = r
 
     traffic = load_traffic()
-    src_hash = kernel_source_hash()
     tr = traffic.get("body")
     roofline = {"bound": "tensor", "achieved": kern_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": kern_tflops / peaks["bf16_tflops"],
                 "peak_source": "%s bf16_tflops (burst, kernel timed alone)" % peaks["source"],
-                "traffic": (tr[0] if tr and tr[1] == src_hash else None),
+                "traffic": (tr[0] if tr and tr[1] == kernel_source_hash("body") else None),
                 "kernel": "tc_conv_kernel (implicit GEMM, TMA im2col, tcgen05)",
                 "algorithmic_flops_per_launch": s.flops}
     dwr = others["dw"]
     trd = traffic.get("dw")
     dw_roof = {"bound": "hbm", "achieved": dwr["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
-               "frac": dwr["gbs"] / peaks["hbm_gbs"], "traffic": (trd[0] if trd and trd[1] == src_hash else None),
+               "frac": dwr["gbs"] / peaks["hbm_gbs"],
+               "traffic": (trd[0] if trd and trd[1] == kernel_source_hash("dw") else None),
                "kernel": "depthwise_kernel (TMA halo tile)", "algorithmic_bytes_per_launch": dwr["bytes"]}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        tf, _, cores, sample, _ = oracle_sample("body")
+        tf, cores, sample = OracleSampler("body").step(12.0)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
 
     if rank == 0:
@@ -353,7 +385,8 @@ def main():
                 "gpu_launches": args.steps, "clocks": clk,
                 "depthwise": {"value": dwr["gbs"], "unit": "GB/s", "ms": dwr["ms"], "roofline": dw_roof,
                               "workload": WORKLOADS["dw"].description},
-                "layers": others, "peaks": peaks, "kernel_source_hash": src_hash}
+                "layers": others, "peaks": peaks,
+                "kernel_source_hash": {k: kernel_source_hash(k) for k in ("body", "dw", "stem")}}
         print(json.dumps(line))
     if dist:
         dist.destroy_process_group()
