@@ -36,6 +36,7 @@ struct conv_plan {
     int device;
     int num_sms;
     int smem_optin;
+    int pair_clusters;  // co-resident 2-CTA clusters of the pair kernel (0: unknown)
     unsigned* status;
     // per-path configuration
     TcGemmParams tc;
@@ -134,7 +135,11 @@ bool configure_tc(conv_plan* pl, bool one_by_one) {
     t.num_m_tiles = static_cast<int>((g.pixels + kTcBlockM - 1) / kTcBlockM);
     t.num_n_tiles = g.C_out / n_tile;
     t.num_tiles = t.num_m_tiles * t.num_n_tiles;
-    const int stage_bytes = kTcBlockM * kTcBlockK * 2 + mma_n * 128;
+    // SM pairs (one MMA over 2 x 128 pixels, weight rows split between the two
+    // CTAs) whenever there are at least two pixel tiles to pair up.
+    t.pair = (t.num_m_tiles >= 2 && !(pl->flags & CONV_FLAG_SINGLE_SM)) ? 1 : 0;
+    const int b_rows = t.pair ? mma_n / 2 : mma_n;
+    const int stage_bytes = kTcBlockM * kTcBlockK * 2 + b_rows * 128;
     const int fixed = 1024 + 256 + 4 * 2 * 32 * 64;  // alignment, barriers, epilogue store tiles
     int stages = (pl->smem_optin - fixed) / stage_bytes;
     if (stages > 8) stages = 8;
@@ -248,7 +253,8 @@ conv_status encode_maps(conv_plan* pl, const void* x, const void* w, void* y) {
         const long long ktot = static_cast<long long>(g.cin_g) * g.Kh * g.Kw;
         const cuuint64_t bdims[2] = {static_cast<cuuint64_t>(ktot), static_cast<cuuint64_t>(g.C_out)};
         const cuuint64_t bstrides[1] = {static_cast<cuuint64_t>(ktot) * 2};
-        const cuuint32_t bbox[2] = {kTcBlockK, static_cast<cuuint32_t>(pl->tc.mma_n)};
+        const cuuint32_t bbox[2] = {kTcBlockK,
+                                    static_cast<cuuint32_t>(pl->tc.pair ? pl->tc.mma_n / 2 : pl->tc.mma_n)};
         const cuuint32_t bestr[2] = {1, 1};
         r = g_encode_tiled(&pl->map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), bdims, bstrides,
                            bbox, bestr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -289,7 +295,8 @@ conv_status conv_plan_create(conv_plan** out, int N, int C_in, int H, int W, int
         return CONV_ERR_INVALID_ARG;
     if (C_in % G != 0 || C_out % G != 0) return CONV_ERR_INVALID_ARG;
     if (dtype != CONV_F32 && dtype != CONV_BF16) return CONV_ERR_INVALID_ARG;
-    if (flags & ~(CONV_FLAG_BIAS | CONV_FLAG_RELU | CONV_FLAG_OUT_BF16)) return CONV_ERR_INVALID_ARG;
+    if (flags & ~(CONV_FLAG_BIAS | CONV_FLAG_RELU | CONV_FLAG_OUT_BF16 | CONV_FLAG_SINGLE_SM))
+        return CONV_ERR_INVALID_ARG;
     if ((flags & CONV_FLAG_OUT_BF16) && dtype != CONV_F32) return CONV_ERR_INVALID_ARG;
     const int Ho = out_extent(H, Kh, S, P, D), Wo = out_extent(W, Kw, S, P, D);
     if (Ho < 1 || Wo < 1) return CONV_ERR_INVALID_ARG;
@@ -327,6 +334,7 @@ conv_status conv_plan_create(conv_plan** out, int N, int C_in, int H, int W, int
     }
 
     pl->path = CONV_PATH_DIRECT;
+    pl->pair_clusters = 0;
     if (dtype == CONV_F32) {
         if (configure_depthwise(pl)) pl->path = CONV_PATH_DEPTHWISE;
     } else {
@@ -335,6 +343,9 @@ conv_status conv_plan_create(conv_plan** out, int N, int C_in, int H, int W, int
             pl->path = CONV_PATH_GEMM_1X1;
         else if (configure_tc(pl, false))
             pl->path = CONV_PATH_IMPLICIT_GEMM;
+        if ((pl->path == CONV_PATH_GEMM_1X1 || pl->path == CONV_PATH_IMPLICIT_GEMM) && pl->tc.pair &&
+            pl->device >= 0)
+            pl->pair_clusters = tc_gemm_pair_max_clusters(pl->tc);
         else if (configure_smallk(pl))
             pl->path = CONV_PATH_SMALL_K_GEMM;
     }
@@ -378,8 +389,15 @@ conv_status conv_forward(conv_plan* p, const void* x, const void* w, const void*
             TcGemmParams t = p->tc;
             t.bias = b;
             t.y = static_cast<__nv_bfloat16*>(y);
-            const int grid = t.num_tiles < p->num_sms ? t.num_tiles : p->num_sms;
-            e = launch_tc_gemm(p->map_a, p->map_b, p->map_y, t, grid, st);
+            if (t.pair) {
+                const int pair_tiles = ((t.num_m_tiles + 1) / 2) * t.num_n_tiles;
+                int clusters = p->pair_clusters > 0 ? p->pair_clusters : p->num_sms / 2;
+                if (clusters > pair_tiles) clusters = pair_tiles;
+                e = launch_tc_gemm_pair(p->map_a, p->map_b, p->map_y, t, 2 * clusters, st);
+            } else {
+                const int grid = t.num_tiles < p->num_sms ? t.num_tiles : p->num_sms;
+                e = launch_tc_gemm(p->map_a, p->map_b, p->map_y, t, grid, st);
+            }
             break;
         }
         case CONV_PATH_SMALL_K_GEMM: {

@@ -70,6 +70,7 @@ struct TcGemmParams {
     int stages;
     int tmem_cols;     // power of two >= 2 * n_tile
     int smem_bytes;
+    int pair;          // 1: CTA-pair kernel (B rows split across the two CTAs)
     int relu;
     const float* bias;
     __nv_bfloat16* y;
@@ -78,6 +79,13 @@ struct TcGemmParams {
 // y_map: 2-D {C_out, pixels} BF16, box {32, 32}, 64-byte swizzle.
 cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, const CUtensorMap& y_map,
                            const TcGemmParams& p, int grid, cudaStream_t stream);
+
+// CTA-pair variant (clusters of 2, tcgen05.mma.cta_group::2, M = 256 per pair);
+// p.stages / p.smem_bytes sized for B buffers of mma_n / 2 rows.  grid is even.
+cudaError_t launch_tc_gemm_pair(const CUtensorMap& a_map, const CUtensorMap& b_map, const CUtensorMap& y_map,
+                                const TcGemmParams& p, int grid, cudaStream_t stream);
+// Co-resident 2-CTA clusters of the pair kernel at p.smem_bytes (0 if unknown).
+int tc_gemm_pair_max_clusters(const TcGemmParams& p);
 
 // ---------------------------------------------------------------- tcgen05 small-K (stem)
 constexpr int kSkThreads = 448;   // producer, MMA, 4 epilogue, 8 transform warps

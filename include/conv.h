@@ -53,7 +53,9 @@ typedef enum { CONV_F32 = 0, CONV_BF16 = 1 } conv_dtype;
 enum {
     CONV_FLAG_BIAS = 1u,       /* add bias[co] after the sum                          */
     CONV_FLAG_RELU = 2u,       /* max(., 0) after the bias                            */
-    CONV_FLAG_OUT_BF16 = 4u    /* CONV_F32 only: write y as BF16 (round to nearest even) */
+    CONV_FLAG_OUT_BF16 = 4u,   /* CONV_F32 only: write y as BF16 (round to nearest even) */
+    CONV_FLAG_SINGLE_SM = 8u   /* tensor-core paths: one CTA per tile, never an SM pair
+                                  (default: SM pairs whenever the shape has >= 2 pixel tiles) */
 };
 
 typedef enum {

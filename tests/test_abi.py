@@ -52,6 +52,7 @@ def _create(*args):
     (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 1, 4),        # OUT_BF16 with BF16 input
     (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 2, 0),        # bad dtype
     (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 64),       # unknown flag
+    (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 16),       # unknown flag
 ])
 def test_create_rejects_bad_shapes(args):
     st, h = _create(*args)
