@@ -99,10 +99,13 @@ struct SmallKParams {
     int relu;
     int ktot;          // C_in * Kh * Kw  (<= 64)
     int kmma;          // number of K=16 MMAs (ceil(ktot / 16))
+    int a_row_bytes;   // 64 (K <= 32, 64-byte swizzle) or 128 (128-byte swizzle)
     int segs;          // 128-pixel segments per output row
-    int num_tiles;
+    int rows_per_tile; // row segments (MMAs of M = 128) per pipeline stage
+    int num_segments;  // N * H_out * segs
+    int num_tiles;     // ceil(num_segments / rows_per_tile)
     int row_bytes;     // W * C_in * 2
-    int raw_bytes;     // Kh * row_bytes rounded up to 1024
+    int raw_bytes;     // rows_per_tile * Kh * row_bytes rounded up to 1024
     int stages;
     int tmem_cols;
     int smem_bytes;

@@ -9,18 +9,22 @@
 // is padded with zeros up to the next multiple of 16 and the layer stays bound
 // by memory traffic, not by the MMA.
 //
-// One tile = up to 128 output pixels of one output row (n, ho).  The Kh input
-// rows it reads (h_i = ho*S + kh*D - P) are whole, contiguous NHWC rows and
-// come in by bulk copy; transform warps then build the 128 x K operand with
+// A row segment is up to 128 output pixels of one output row (n, ho).  The Kh
+// input rows it reads (h_i = ho*S + kh*D - P) are whole, contiguous NHWC rows
+// and come in by bulk copy; transform warps then build its 128 x K operand with
 // the index map of lesson 9 section 2 and zero padding as an address test
-// (section 26), writing the 128-byte-swizzled layout the MMA descriptor reads.
-// The whole weight matrix (C_out x K, K <= 64) stays in shared memory.
+// (section 26), writing the swizzled K-major layout the MMA descriptor reads
+// (64-byte rows with the 64-byte swizzle when K <= 32, else 128-byte rows).
+// One pipeline stage carries `rows_per_tile` segments (one M = 128 MMA each,
+// side by side in TMEM), so the per-stage barrier and epilogue costs are
+// shared by several rows.  The whole weight matrix (C_out x K) stays in shared
+// memory.
 //
 // Warp roles (448 threads, persistent):
 //   warp 0       bulk-copy producer (one lane)
 //   warp 1       TMEM allocator; one lane issues tcgen05.mma
 //   warps 2..5   epilogue (tcgen05.ld -> +bias -> ReLU -> BF16 -> smem -> TMA store)
-//   warps 6..13  transform: raw rows -> swizzled A tile (two threads per pixel row)
+//   warps 6..13  transform: raw rows -> swizzled A tiles
 // The 3-channel 3x3 case is compiled with its K decomposition as constants;
 // other shapes read it from a per-CTA table.
 #include "conv_internal.h"
@@ -30,7 +34,6 @@ namespace convgb {
 
 namespace {
 
-constexpr uint32_t kSkABytes = 128 * 128;  // 128 pixels x 64 BF16
 constexpr uint32_t kSkOutBytes = 32 * 64;  // one 32-row x 32-column BF16 store tile
 
 struct SkSmem {
@@ -52,12 +55,15 @@ struct SkSmem {
     float* bias;     // [C_out] copy of the bias
 };
 
+__device__ __forceinline__ uint32_t a_tile_bytes(const SmallKParams& p) { return 128u * p.a_row_bytes; }
+
 __device__ __forceinline__ SkSmem carve(uint8_t* raw, const SmallKParams& p) {
     SkSmem s;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.b = base;
-    s.a = s.b + p.g.C_out * 128;
-    s.raw = s.a + p.stages * kSkABytes;
+    const uint32_t b_bytes = (static_cast<uint32_t>(p.g.C_out * p.a_row_bytes) + 1023u) & ~1023u;
+    s.a = s.b + b_bytes;
+    s.raw = s.a + p.stages * p.rows_per_tile * a_tile_bytes(p);
     s.out = s.raw + p.stages * p.raw_bytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(s.out + 4 * 2 * kSkOutBytes);
     s.raw_full = bars;
@@ -75,15 +81,16 @@ __device__ __forceinline__ SkSmem carve(uint8_t* raw, const SmallKParams& p) {
     return s;
 }
 
-struct SkTile {
+struct SkSeg {
     int n, ho, wo0, npix;
 };
 
-__device__ __forceinline__ SkTile decode(const SmallKParams& p, int tile) {
-    SkTile t;
+// Row segment u: output row (n, ho), pixels [wo0, wo0 + npix).
+__device__ __forceinline__ SkSeg segment(const SmallKParams& p, int u) {
+    SkSeg t;
     const int per_img = p.g.H_out * p.segs;
-    t.n = tile / per_img;
-    const int r = tile - t.n * per_img;
+    t.n = u / per_img;
+    const int r = u - t.n * per_img;
     t.ho = r / p.segs;
     const int seg = r - t.ho * p.segs;
     t.wo0 = seg * 128;
@@ -91,18 +98,30 @@ __device__ __forceinline__ SkTile decode(const SmallKParams& p, int tile) {
     return t;
 }
 
-// Byte offset of element k of row r in a 128-byte-swizzled K-major tile.
-__device__ __forceinline__ uint32_t sw128_offset(int r, int k) {
-    return static_cast<uint32_t>(r * 128 + ((((k >> 3) ^ (r & 7)) & 7) << 4) + ((k & 7) << 1));
+// Byte offset of element k of row r in a swizzled K-major tile with 64- or
+// 128-byte rows (16-byte chunk j of row r sits at chunk j ^ f(r)).
+__device__ __forceinline__ uint32_t sw_offset(int r, int k, int row_bytes) {
+    if (row_bytes == 128) return static_cast<uint32_t>(r * 128 + ((((k >> 3) ^ (r & 7)) & 7) << 4) + ((k & 7) << 1));
+    return static_cast<uint32_t>(r * 64 + ((((k >> 3) ^ (r >> 1)) & 3) << 4) + ((k & 7) << 1));
 }
 
-}  // namespace
+// Shared-memory descriptor for a K-major tile of 64-byte rows, 64-byte swizzle:
+// stride byte offset 8 rows x 64 B = 512 (>> 4 = 32), swizzle mode 4.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(512 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(4) << 61);
+}
+
+__device__ __forceinline__ uint64_t a_desc(const SmallKParams& p, uint32_t saddr) {
+    return p.a_row_bytes == 128 ? sdesc_sw128(saddr) : sdesc_sw64(saddr);
+}
 
 // Gather the 8 K-elements of chunk j for one pixel row.  CIN/KH/KW > 0: the
 // decomposition k -> (kh, kw, ci) is constant-folded; 0: read from the tables.
 template <int CIN, int KH, int KW>
-__device__ __forceinline__ uint4 gather_chunk(const SkSmem& sm, const SmallKParams& p, const uint16_t* src,
-                                              int j, int wbase, unsigned long long rowmask) {
+__device__ __forceinline__ uint4 gather_chunk(const SkSmem& sm, const SmallKParams& p, const uint16_t* src, int j,
+                                              int wbase, unsigned long long rowmask) {
     uint32_t q[4];
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
@@ -131,6 +150,8 @@ __device__ __forceinline__ uint4 gather_chunk(const SkSmem& sm, const SmallKPara
     return make_uint4(q[0], q[1], q[2], q[3]);
 }
 
+}  // namespace
+
 template <int CIN, int KH, int KW>
 __global__ void __launch_bounds__(kSkThreads, 1)
     tc_smallk_kernel(const __grid_constant__ CUtensorMap y_map, const SmallKParams p) {
@@ -139,24 +160,27 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     volatile int* abort = sm.abort;
+    const int R = p.rows_per_tile;
+    const int n_tile = p.g.C_out;
 
     // Resident weights: row co = w[co][0..ktot), zero beyond ktot, swizzled.
     {
         const uint16_t* w16 = reinterpret_cast<const uint16_t*>(p.w);
-        for (int idx = threadIdx.x; idx < p.g.C_out * 64; idx += blockDim.x) {
-            const int co = idx >> 6;
-            const int k = idx & 63;
+        const int kw = p.a_row_bytes / 2;
+        for (int idx = threadIdx.x; idx < p.g.C_out * kw; idx += blockDim.x) {
+            const int co = idx / kw;
+            const int k = idx - co * kw;
             const uint16_t v = k < p.ktot ? w16[static_cast<long long>(co) * p.ktot + k] : uint16_t(0);
-            *reinterpret_cast<uint16_t*>(sm.b + sw128_offset(co, k)) = v;
+            *reinterpret_cast<uint16_t*>(sm.b + sw_offset(co, k, p.a_row_bytes)) = v;
         }
         fence_proxy_async_smem();
         // K index -> (kh, kw, ci) decomposition, once per CTA (no divisions in the gather loop)
         for (int k = threadIdx.x; k < 64; k += blockDim.x) {
             if (k < p.ktot) {
                 const int ci = k % p.g.C_in, tap = k / p.g.C_in;
-                const int kh = tap / p.g.Kw, kw = tap - kh * p.g.Kw;
-                sm.tab_off[k] = kh * (p.row_bytes >> 1) + kw * p.g.D * p.g.C_in + ci;
-                sm.tab_kwd[k] = kw * p.g.D;
+                const int kh = tap / p.g.Kw, kwi = tap - kh * p.g.Kw;
+                sm.tab_off[k] = kh * (p.row_bytes >> 1) + kwi * p.g.D * p.g.C_in + ci;
+                sm.tab_kwd[k] = kwi * p.g.D;
                 sm.tab_kh[k] = kh;
             } else {
                 sm.tab_off[k] = 0;
@@ -188,7 +212,6 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *sm.tmem_slot;
-    const int n_tile = p.g.C_out;
 
     if (warp == 0) {
         // ------------------------------------------------------------ bulk-copy producer
@@ -202,19 +225,29 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                     record_status(p.status, kStatusTimeoutProducer, abort);
                     break;
                 }
-                const SkTile t = decode(p, tile);
                 uint32_t bytes = 0;
-                for (int kh = 0; kh < p.g.Kh; ++kh) {
-                    const int hi = t.ho * p.g.S - p.g.P + kh * p.g.D;
-                    if (hi >= 0 && hi < p.g.H) bytes += static_cast<uint32_t>(p.row_bytes);
+                for (int j = 0; j < R; ++j) {
+                    const int u = tile * R + j;
+                    if (u >= p.num_segments) break;
+                    const SkSeg t = segment(p, u);
+                    for (int kh = 0; kh < p.g.Kh; ++kh) {
+                        const int hi = t.ho * p.g.S - p.g.P + kh * p.g.D;
+                        if (hi >= 0 && hi < p.g.H) bytes += static_cast<uint32_t>(p.row_bytes);
+                    }
                 }
                 mbar_arrive_expect_tx(&sm.raw_full[stage], bytes);
                 uint8_t* dst = sm.raw + stage * p.raw_bytes;
-                for (int kh = 0; kh < p.g.Kh; ++kh) {
-                    const int hi = t.ho * p.g.S - p.g.P + kh * p.g.D;
-                    if (hi < 0 || hi >= p.g.H) continue;
-                    const char* src = xb + (static_cast<long long>(t.n) * p.g.H + hi) * p.row_bytes;
-                    bulk_load(dst + kh * p.row_bytes, src, static_cast<uint32_t>(p.row_bytes), &sm.raw_full[stage]);
+                for (int j = 0; j < R; ++j) {
+                    const int u = tile * R + j;
+                    if (u >= p.num_segments) break;
+                    const SkSeg t = segment(p, u);
+                    for (int kh = 0; kh < p.g.Kh; ++kh) {
+                        const int hi = t.ho * p.g.S - p.g.P + kh * p.g.D;
+                        if (hi < 0 || hi >= p.g.H) continue;
+                        const char* src = xb + (static_cast<long long>(t.n) * p.g.H + hi) * p.row_bytes;
+                        bulk_load(dst + (j * p.g.Kh + kh) * p.row_bytes, src, static_cast<uint32_t>(p.row_bytes),
+                                  &sm.raw_full[stage]);
+                    }
                 }
                 ++issued;
                 if (++stage == p.stages) {
@@ -232,7 +265,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(128, n_tile);
-            const uint64_t bdesc = sdesc_sw128(smem_addr(sm.b));
+            const uint64_t bdesc = a_desc(p, smem_addr(sm.b));
             int stage = 0;
             uint32_t phase = 0;
             int local = 0;
@@ -244,9 +277,13 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint64_t adesc = sdesc_sw128(smem_addr(sm.a + stage * kSkABytes));
-                const uint32_t d = tmem_base + static_cast<uint32_t>(buf * n_tile);
-                for (int k = 0; k < p.kmma; ++k) mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, k != 0 ? 1u : 0u);
+                const int rows = min(R, p.num_segments - tile * R);
+                for (int j = 0; j < rows; ++j) {
+                    const uint64_t adesc = a_desc(p, smem_addr(sm.a + (stage * R + j) * a_tile_bytes(p)));
+                    const uint32_t d = tmem_base + static_cast<uint32_t>((buf * R + j) * n_tile);
+                    for (int k = 0; k < p.kmma; ++k)
+                        mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, k != 0 ? 1u : 0u);
+                }
                 mma_commit(&sm.empty[stage]);
                 mma_commit(&sm.tfull[buf]);
                 if (++stage == p.stages) {
@@ -272,27 +309,30 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 break;
             }
             tc_fence_after();
-            const SkTile t = decode(p, tile);
-            const int wo_row0 = t.wo0 + quarter * 32;          // first output column of this warp's rows
-            const bool rows_exist = quarter * 32 < t.npix;
-            const uint32_t t_row =
-                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * n_tile);
-            for (int c = 0; c < n_tile; c += 32) {
-                uint32_t v[32];
-                __syncwarp();
-                tmem_ld32(t_row + static_cast<uint32_t>(c), v);
-                tmem_ld_wait();
-                if (lane == 0) bulk_wait_read_le1();
-                __syncwarp();
-                uint8_t* dst = stg + sbuf * kSkOutBytes;
-                stage_row32(v, p.bias ? sm.bias + c : nullptr, p.relu, dst, lane);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0 && rows_exist) {  // columns past W_out fall outside the map: not written
-                    tma_store_3d(&y_map, dst, c, wo_row0, t.n * p.g.H_out + t.ho);
-                    bulk_commit();
+            const int rows = min(R, p.num_segments - tile * R);
+            for (int j = 0; j < rows; ++j) {
+                const SkSeg t = segment(p, tile * R + j);
+                const int wo_row0 = t.wo0 + quarter * 32;  // first output column of this warp's rows
+                const bool rows_exist = quarter * 32 < t.npix;
+                const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                       static_cast<uint32_t>((buf * R + j) * n_tile);
+                for (int c = 0; c < n_tile; c += 32) {
+                    uint32_t v[32];
+                    __syncwarp();
+                    tmem_ld32(t_row + static_cast<uint32_t>(c), v);
+                    tmem_ld_wait();
+                    if (lane == 0) bulk_wait_read_le1();
+                    __syncwarp();
+                    uint8_t* dst = stg + sbuf * kSkOutBytes;
+                    stage_row32(v, p.bias ? sm.bias + c : nullptr, p.relu, dst, lane);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && rows_exist) {  // columns past W_out fall outside the map: not written
+                        tma_store_3d(&y_map, dst, c, wo_row0, t.n * p.g.H_out + t.ho);
+                        bulk_commit();
+                    }
+                    sbuf ^= 1;
                 }
-                sbuf ^= 1;
             }
             tc_fence_before();
             mbar_arrive(&sm.tempty[buf]);
@@ -300,10 +340,10 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         if (lane == 0) bulk_wait_all();
     } else {
         // ------------------------------------------------------------ transform (im2col in smem)
-        const int r = (threadIdx.x - 192) & 127;   // A row = pixel within the tile
-        const int half = (threadIdx.x - 192) >> 7;  // this thread builds chunks half, half+2, ...
+        const int tid = threadIdx.x - 192;  // 0..255
         const uint16_t* raw16 = reinterpret_cast<const uint16_t*>(sm.raw);
         const int raw_elems = p.raw_bytes >> 1;
+        const int row_elems = p.row_bytes >> 1;
         const int nchunks = 2 * p.kmma;
         int stage = 0;
         uint32_t phase = 0;
@@ -312,28 +352,34 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 record_status(p.status, kStatusTimeoutTransform, abort);
                 break;
             }
-            const SkTile t = decode(p, tile);
-            const uint16_t* src = raw16 + stage * raw_elems;
-            uint8_t* arow = sm.a + stage * kSkABytes;
-            // input rows of this tile that exist (the rest read as zero)
-            unsigned long long rowmask = 0;
-            for (int kh = 0; kh < p.g.Kh; ++kh) {
-                const int hi = t.ho * p.g.S - p.g.P + kh * p.g.D;
-                if (hi >= 0 && hi < p.g.H) rowmask |= 1ull << kh;
-            }
-            const int wbase = (t.wo0 + r) * p.g.S - p.g.P;  // input column of tap kw = 0
-            if (r >= t.npix) rowmask = 0;                   // rows past the segment: zeros
-            if constexpr (CIN > 0) {
-                constexpr int kChunks = ((CIN * KH * KW + 15) / 16) * 2;
+            for (int idx = tid; idx < R * 128; idx += 256) {
+                const int j = idx >> 7;   // row segment within the stage
+                const int r = idx & 127;  // A row = pixel within the segment
+                const int u = tile * R + j;
+                uint8_t* arow = sm.a + (stage * R + j) * a_tile_bytes(p);
+                unsigned long long rowmask = 0;  // input rows that exist (the rest read as zero)
+                int wbase = 0;
+                if (u < p.num_segments) {
+                    const SkSeg t = segment(p, u);
+                    for (int kh = 0; kh < p.g.Kh; ++kh) {
+                        const int hi = t.ho * p.g.S - p.g.P + kh * p.g.D;
+                        if (hi >= 0 && hi < p.g.H) rowmask |= 1ull << kh;
+                    }
+                    wbase = (t.wo0 + r) * p.g.S - p.g.P;  // input column of tap kw = 0
+                    if (r >= t.npix) rowmask = 0;         // rows past the segment: zeros
+                }
+                const uint16_t* src = raw16 + stage * raw_elems + j * p.g.Kh * row_elems;
+                if constexpr (CIN > 0) {
+                    constexpr int kChunks = ((CIN * KH * KW + 15) / 16) * 2;
 #pragma unroll
-                for (int j = 0; j < kChunks; ++j)
-                    if ((j & 1) == half)
-                        *reinterpret_cast<uint4*>(arow + sw128_offset(r, j * 8)) =
-                            gather_chunk<CIN, KH, KW>(sm, p, src, j, wbase, rowmask);
-            } else {
-                for (int j = half; j < nchunks; j += 2)
-                    *reinterpret_cast<uint4*>(arow + sw128_offset(r, j * 8)) =
-                        gather_chunk<0, 0, 0>(sm, p, src, j, wbase, rowmask);
+                    for (int c = 0; c < kChunks; ++c)
+                        *reinterpret_cast<uint4*>(arow + sw_offset(r, c * 8, p.a_row_bytes)) =
+                            gather_chunk<CIN, KH, KW>(sm, p, src, c, wbase, rowmask);
+                } else {
+                    for (int c = 0; c < nchunks; ++c)
+                        *reinterpret_cast<uint4*>(arow + sw_offset(r, c * 8, p.a_row_bytes)) =
+                            gather_chunk<0, 0, 0>(sm, p, src, c, wbase, rowmask);
+                }
             }
             fence_proxy_async_smem();
             mbar_arrive(&sm.a_full[stage]);
