@@ -185,7 +185,7 @@ def measure_layer(name, steps, warmup, flush, peaks):
         or s.dtype == "f32" else "tensor"
     res = {"workload": name, "kernel": plan.path, "ms": t * 1e3, "tflops": tflops, "gbs": gbs,
            "bound": bound, "flops": s.flops, "bytes": s.algorithmic_bytes, "launches": steps,
-           "source_hash": kernel_source_hash(name)}
+           "source_hash": kernel_source_hash(name), "launch": plan.launch}
     if bound == "tensor":
         res["frac"] = tflops / peaks["bf16_tflops"]
     else:

@@ -22,7 +22,8 @@ PATHS = {0: "direct", 1: "depthwise", 2: "gemm_1x1", 3: "implicit_gemm", 4: "sma
 
 # Every symbol include/conv.h declares.
 EXPORTS = ("conv_plan_create", "conv_plan_output_shape", "conv_plan_info", "conv_forward",
-           "conv_plan_destroy", "conv_status_string", "conv_device_status", "conv_plan_num_sms")
+           "conv_plan_destroy", "conv_status_string", "conv_device_status", "conv_plan_num_sms",
+           "conv_plan_launch_info")
 
 _lock = threading.Lock()
 _lib = None
@@ -68,6 +69,8 @@ def lib():
             L.conv_device_status.restype = c_int
             L.conv_plan_num_sms.argtypes = [vp]
             L.conv_plan_num_sms.restype = c_int
+            L.conv_plan_launch_info.argtypes = [vp] + [ctypes.POINTER(c_int)] * 5
+            L.conv_plan_launch_info.restype = c_int
             _lib = L
         return _lib
 
@@ -111,6 +114,9 @@ class ConvPlan:
         self.path = PATHS[path.value]
         self.gemm_mnk = (m.value, n.value, k.value)
         self.num_sms = L.conv_plan_num_sms(h)
+        li = [ctypes.c_int() for _ in range(5)]
+        L.conv_plan_launch_info(h, *[ctypes.byref(v) for v in li])
+        self.launch = dict(zip(("grid", "block", "smem_bytes", "stages", "cluster"), [v.value for v in li]))
 
     @classmethod
     def for_shape(cls, s, single_sm=False):

@@ -348,11 +348,11 @@ conv_status conv_plan_create(conv_plan** out, int N, int C_in, int H, int W, int
             pl->path = CONV_PATH_GEMM_1X1;
         else if (configure_tc(pl, false))
             pl->path = CONV_PATH_IMPLICIT_GEMM;
+        else if (configure_smallk(pl))
+            pl->path = CONV_PATH_SMALL_K_GEMM;
         if ((pl->path == CONV_PATH_GEMM_1X1 || pl->path == CONV_PATH_IMPLICIT_GEMM) && pl->tc.pair &&
             pl->device >= 0)
             pl->pair_clusters = tc_gemm_pair_max_clusters(pl->tc);
-        else if (configure_smallk(pl))
-            pl->path = CONV_PATH_SMALL_K_GEMM;
     }
     *out = pl;
     return CONV_OK;
@@ -376,6 +376,56 @@ conv_status conv_plan_info(const conv_plan* p, int* path, long long* gemm_m, lon
 
 int conv_plan_num_sms(const conv_plan* p) { return p ? p->num_sms : 0; }
 
+conv_status conv_plan_launch_info(const conv_plan* p, int* grid, int* block, int* smem_bytes, int* stages,
+                                  int* cluster) {
+    if (p == nullptr) return CONV_ERR_INVALID_ARG;
+    int gr = 0, bl = 0, sm = 0, st = 0, cl = 1;
+    switch (p->path) {
+        case CONV_PATH_GEMM_1X1:
+        case CONV_PATH_IMPLICIT_GEMM: {
+            const TcGemmParams& t = p->tc;
+            bl = kTcThreads;
+            sm = t.smem_bytes;
+            st = t.stages;
+            if (t.pair) {
+                const int pair_tiles = ((t.num_m_tiles + 1) / 2) * t.num_n_tiles;
+                int clusters = p->pair_clusters > 0 ? p->pair_clusters : p->num_sms / 2;
+                if (clusters > pair_tiles) clusters = pair_tiles;
+                gr = 2 * clusters;
+                cl = 2;
+            } else {
+                gr = t.num_tiles < p->num_sms ? t.num_tiles : p->num_sms;
+            }
+            break;
+        }
+        case CONV_PATH_SMALL_K_GEMM:
+            bl = kSkThreads;
+            sm = p->sk.smem_bytes;
+            st = p->sk.stages;
+            gr = p->sk.num_tiles < p->num_sms ? p->sk.num_tiles : p->num_sms;
+            break;
+        case CONV_PATH_DEPTHWISE:
+            bl = 256;
+            sm = p->dw.smem_bytes;
+            st = p->dw.stages;
+            gr = p->dw.grid;
+            break;
+        default: {
+            const long long total = p->g.pixels * p->g.C_out;
+            const long long blocks = (total + 255) / 256;
+            gr = static_cast<int>(blocks < (1ll << 20) ? blocks : (1ll << 20));
+            bl = 256;
+            break;
+        }
+    }
+    if (grid) *grid = gr;
+    if (block) *block = bl;
+    if (smem_bytes) *smem_bytes = sm;
+    if (stages) *stages = st;
+    if (cluster) *cluster = cl;
+    return CONV_OK;
+}
+
 conv_status conv_forward(conv_plan* p, const void* x, const void* w, const void* bias, void* y, void* stream) {
     if (p == nullptr || x == nullptr || w == nullptr || y == nullptr) return CONV_ERR_INVALID_ARG;
     if (p->device < 0) return CONV_ERR_CUDA;  // host-only plan: no device to run on
@@ -394,15 +444,10 @@ conv_status conv_forward(conv_plan* p, const void* x, const void* w, const void*
             TcGemmParams t = p->tc;
             t.bias = b;
             t.y = static_cast<__nv_bfloat16*>(y);
-            if (t.pair) {
-                const int pair_tiles = ((t.num_m_tiles + 1) / 2) * t.num_n_tiles;
-                int clusters = p->pair_clusters > 0 ? p->pair_clusters : p->num_sms / 2;
-                if (clusters > pair_tiles) clusters = pair_tiles;
-                e = launch_tc_gemm_pair(p->map_a, p->map_b, p->map_y, t, 2 * clusters, st);
-            } else {
-                const int grid = t.num_tiles < p->num_sms ? t.num_tiles : p->num_sms;
-                e = launch_tc_gemm(p->map_a, p->map_b, p->map_y, t, grid, st);
-            }
+            int grid = 0;
+            conv_plan_launch_info(p, &grid, nullptr, nullptr, nullptr, nullptr);
+            e = t.pair ? launch_tc_gemm_pair(p->map_a, p->map_b, p->map_y, t, grid, st)
+                       : launch_tc_gemm(p->map_a, p->map_b, p->map_y, t, grid, st);
             break;
         }
         case CONV_PATH_SMALL_K_GEMM: {

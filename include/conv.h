@@ -134,6 +134,15 @@ conv_status conv_device_status(int *code);
 /* Number of SMs the plan's grid sizing uses (device property of the plan's device). */
 int conv_plan_num_sms(const conv_plan *p);
 
+/*
+ * Launch configuration conv_forward uses for this plan: grid and block size
+ * (CTAs, threads), dynamic shared memory per CTA in bytes, pipeline stages,
+ * and CTAs per cluster (2 for SM pairs, else 1).  Any output pointer may be
+ * NULL.  Returns CONV_ERR_INVALID_ARG for a NULL plan.
+ */
+conv_status conv_plan_launch_info(const conv_plan *p, int *grid, int *block, int *smem_bytes,
+                                  int *stages, int *cluster);
+
 #ifdef __cplusplus
 }
 #endif
