@@ -178,7 +178,7 @@ bool configure_smallk(conv_plan* pl) {
     s.row_bytes = static_cast<int>(row_bytes);
     s.raw_bytes = static_cast<int>(raw);
     const int b_bytes = (g.C_out * s.a_row_bytes + 1023) / 1024 * 1024;
-    const int fixed = 1024 + b_bytes + 4 * 2 * 32 * 64 + 1024 + 3 * 64 * 4 + g.C_out * 4;
+    const int fixed = 1024 + b_bytes + 4 * 2 * 32 * 64 + 1024 + 3 * 64 * 4 + 16 + g.C_out * 4;
     const int stage_bytes = rows * 128 * s.a_row_bytes + s.raw_bytes;
     int stages = (pl->smem_optin - fixed) / stage_bytes;
     if (stages > 8) stages = 8;

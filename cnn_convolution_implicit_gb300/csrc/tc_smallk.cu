@@ -77,7 +77,8 @@ __device__ __forceinline__ SkSmem carve(uint8_t* raw, const SmallKParams& p) {
     s.tab_off = s.abort + 1;
     s.tab_kwd = s.tab_off + 64;
     s.tab_kh = s.tab_kwd + 64;
-    s.bias = reinterpret_cast<float*>(s.tab_kh + 64);
+    // 16-byte aligned: the epilogue reads it as float4 (the barrier count above varies with `stages`)
+    s.bias = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(s.tab_kh + 64) + 15) & ~uintptr_t(15));
     return s;
 }
 
