@@ -126,21 +126,45 @@ bool configure_tc(conv_plan* pl, bool one_by_one) {
     }
     if (g.pixels > 0x7fffffffLL) return false;
     t.g = g;
-    t.mode = one_by_one ? kTcMode1x1 : kTcModeIm2col;
+    t.mode = one_by_one ? kTcMode1x1 : (g.S == 1 ? kTcModeRect : kTcModeIm2col);
     t.n_tile = n_tile;
     t.mma_n = mma_n;
     t.gpc = gpc;
     t.kblk = g.cin_g / kTcBlockK;
     t.ksteps = g.Kh * g.Kw * t.kblk;
-    t.num_m_tiles = static_cast<int>((g.pixels + kTcBlockM - 1) / kTcBlockM);
+    if (t.mode == kTcModeRect) {
+        // 128-pixel rectangle, 8 / 16 / 32 wide: the one that pads the image least
+        // (ties go to 16 x 8).  A warp's 32 TMEM lanes are 32/TW whole rows of it.
+        auto padded = [](int extent, int t) { return static_cast<long long>((extent + t - 1) / t) * t; };
+        int best = 16;
+        long long best_area = padded(g.W_out, 16) * padded(g.H_out, 8);
+        for (int tw : {8, 32}) {
+            const long long area = padded(g.W_out, tw) * padded(g.H_out, kTcBlockM / tw);
+            if (area < best_area) {
+                best = tw;
+                best_area = area;
+            }
+        }
+        t.rect_w = best;
+        t.rect_h = kTcBlockM / best;
+        t.rect_tiles_w = (g.W_out + t.rect_w - 1) / t.rect_w;
+        t.rect_tiles_h = (g.H_out + t.rect_h - 1) / t.rect_h;
+        const long long m_tiles = static_cast<long long>(g.N) * t.rect_tiles_w * t.rect_tiles_h;
+        if (m_tiles > 0x3fffffffLL) return false;
+        t.num_m_tiles = static_cast<int>(m_tiles);
+    } else {
+        t.rect_w = t.rect_h = t.rect_tiles_w = t.rect_tiles_h = 0;
+        t.num_m_tiles = static_cast<int>((g.pixels + kTcBlockM - 1) / kTcBlockM);
+    }
     t.num_n_tiles = g.C_out / n_tile;
     t.num_tiles = t.num_m_tiles * t.num_n_tiles;
+    t.ychunk = n_tile % 64 == 0 ? 64 : 32;
     // SM pairs (one MMA over 2 x 128 pixels, weight rows split between the two
-    // CTAs) whenever there are at least two pixel tiles to pair up.
-    t.pair = (t.num_m_tiles >= 2 && !(pl->flags & CONV_FLAG_SINGLE_SM)) ? 1 : 0;
+    // CTAs) on request, when there are at least two pixel tiles to pair up.
+    t.pair = (t.num_m_tiles >= 2 && (pl->flags & CONV_FLAG_SM_PAIRS)) ? 1 : 0;
     const int b_rows = t.pair ? mma_n / 2 : mma_n;
     const int stage_bytes = kTcBlockM * kTcBlockK * 2 + b_rows * 128;
-    const int fixed = 1024 + 256 + 4 * 2 * 32 * 64;  // alignment, barriers, epilogue store tiles
+    const int fixed = 1024 + 256 + 4 * 2 * 32 * 128;  // alignment, barriers, epilogue store tiles
     int stages = (pl->smem_optin - fixed) / stage_bytes;
     if (stages > 8) stages = 8;
     if (stages < 2) return false;
@@ -204,12 +228,13 @@ bool configure_depthwise(conv_plan* pl) {
     return true;
 }
 
-// Y store map of the tcgen05 paths: BF16, boxes of 32 channels x 32 pixels, 64-byte swizzle.
+// Y store map of the tcgen05 paths: BF16, boxes of `ychunk` channels x 32
+// pixels, 128-byte swizzle (64 channels) or 64-byte swizzle (32 channels).
 CUresult encode_y_map(conv_plan* pl, void* y) {
     const ConvGeom& g = pl->g;
-    const cuuint32_t box[3] = {32, 32, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
     if (pl->path == CONV_PATH_SMALL_K_GEMM) {  // {C_out, W_out, N*H_out}: a row segment never spills
+        const cuuint32_t box[3] = {32, 32, 1};
+        const cuuint32_t estr[3] = {1, 1, 1};
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(g.C_out), static_cast<cuuint64_t>(g.W_out),
                                     static_cast<cuuint64_t>(g.N) * g.H_out};
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(g.C_out) * 2,
@@ -218,10 +243,27 @@ CUresult encode_y_map(conv_plan* pl, void* y) {
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
+    const TcGemmParams& t = pl->tc;
+    const CUtensorMapSwizzle sw = t.ychunk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (t.mode == kTcModeRect) {  // {C_out, W_out, H_out, N}: 32/TW rows of TW pixels per store
+        const cuuint32_t box[4] = {static_cast<cuuint32_t>(t.ychunk), static_cast<cuuint32_t>(t.rect_w),
+                                   static_cast<cuuint32_t>(32 / t.rect_w), 1};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        const cuuint64_t dims[4] = {static_cast<cuuint64_t>(g.C_out), static_cast<cuuint64_t>(g.W_out),
+                                    static_cast<cuuint64_t>(g.H_out), static_cast<cuuint64_t>(g.N)};
+        const cuuint64_t strides[3] = {static_cast<cuuint64_t>(g.C_out) * 2,
+                                       static_cast<cuuint64_t>(g.W_out) * g.C_out * 2,
+                                       static_cast<cuuint64_t>(g.H_out) * g.W_out * g.C_out * 2};
+        return g_encode_tiled(&pl->map_y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, y, dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(t.ychunk), 32};
+    const cuuint32_t estr[2] = {1, 1};
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.C_out), static_cast<cuuint64_t>(g.pixels)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(g.C_out) * 2};
     return g_encode_tiled(&pl->map_y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
@@ -238,6 +280,18 @@ conv_status encode_maps(conv_plan* pl, const void* x, const void* w, void* y) {
             const cuuint32_t box[2] = {kTcBlockK, kTcBlockM};
             const cuuint32_t estr[2] = {1, 1};
             r = g_encode_tiled(&pl->map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides,
+                               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        } else if (pl->tc.mode == kTcModeRect) {
+            const cuuint64_t dims[4] = {static_cast<cuuint64_t>(g.C_in), static_cast<cuuint64_t>(g.W),
+                                        static_cast<cuuint64_t>(g.H), static_cast<cuuint64_t>(g.N)};
+            const cuuint64_t strides[3] = {static_cast<cuuint64_t>(g.C_in) * 2,
+                                           static_cast<cuuint64_t>(g.W) * g.C_in * 2,
+                                           static_cast<cuuint64_t>(g.H) * g.W * g.C_in * 2};
+            const cuuint32_t box[4] = {kTcBlockK, static_cast<cuuint32_t>(pl->tc.rect_w),
+                                       static_cast<cuuint32_t>(pl->tc.rect_h), 1};
+            const cuuint32_t estr[4] = {1, 1, 1, 1};
+            r = g_encode_tiled(&pl->map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides,
                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         } else {
@@ -300,7 +354,7 @@ conv_status conv_plan_create(conv_plan** out, int N, int C_in, int H, int W, int
         return CONV_ERR_INVALID_ARG;
     if (C_in % G != 0 || C_out % G != 0) return CONV_ERR_INVALID_ARG;
     if (dtype != CONV_F32 && dtype != CONV_BF16) return CONV_ERR_INVALID_ARG;
-    if (flags & ~(CONV_FLAG_BIAS | CONV_FLAG_RELU | CONV_FLAG_OUT_BF16 | CONV_FLAG_SINGLE_SM))
+    if (flags & ~(CONV_FLAG_BIAS | CONV_FLAG_RELU | CONV_FLAG_OUT_BF16 | CONV_FLAG_SM_PAIRS))
         return CONV_ERR_INVALID_ARG;
     if ((flags & CONV_FLAG_OUT_BF16) && dtype != CONV_F32) return CONV_ERR_INVALID_ARG;
     const int Ho = out_extent(H, Kh, S, P, D), Wo = out_extent(W, Kw, S, P, D);
@@ -446,8 +500,7 @@ conv_status conv_forward(conv_plan* p, const void* x, const void* w, const void*
             t.y = static_cast<__nv_bfloat16*>(y);
             int grid = 0;
             conv_plan_launch_info(p, &grid, nullptr, nullptr, nullptr, nullptr);
-            e = t.pair ? launch_tc_gemm_pair(p->map_a, p->map_b, p->map_y, t, grid, st)
-                       : launch_tc_gemm(p->map_a, p->map_b, p->map_y, t, grid, st);
+            e = launch_tc_gemm(p->map_a, p->map_b, p->map_y, t, grid, st);
             break;
         }
         case CONV_PATH_SMALL_K_GEMM: {

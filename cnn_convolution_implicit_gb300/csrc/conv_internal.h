@@ -56,7 +56,7 @@ constexpr int kTcBlockM = 128;    // pixels per tile (TMEM lanes)
 constexpr int kTcBlockK = 64;     // BF16 elements per K-step (one 128-byte swizzle row)
 constexpr int kTcThreads = 192;   // producer warp, MMA warp, 4 epilogue warps
 
-enum TcMode { kTcMode1x1 = 0, kTcModeIm2col = 1 };
+enum TcMode { kTcMode1x1 = 0, kTcModeIm2col = 1, kTcModeRect = 2 };
 
 struct TcGemmParams {
     ConvGeom g;
@@ -67,6 +67,9 @@ struct TcGemmParams {
     int kblk;          // (C_in/G) / 64
     int ksteps;        // Kh * Kw * kblk K-steps per sub-GEMM
     int num_m_tiles, num_n_tiles, num_tiles;
+    int rect_w, rect_h;              // kTcModeRect: pixel tile = rect_h x rect_w output pixels
+    int rect_tiles_w, rect_tiles_h;  // rectangles per image row / column
+    int ychunk;                      // output channels per TMA store (64: 128-byte rows, or 32)
     int stages;
     int tmem_cols;     // power of two >= 2 * n_tile
     int smem_bytes;
@@ -76,14 +79,14 @@ struct TcGemmParams {
     __nv_bfloat16* y;
     unsigned* status;
 };
-// y_map: 2-D {C_out, pixels} BF16, box {32, 32}, 64-byte swizzle.
+// a_map: rect mode 4-D tiled {C_in, W, H, N} box {64, rect_w, rect_h, 1}; im2col
+// mode 4-D im2col; 1x1 mode 2-D {C_in, pixels} box {64, 128}; all 128-byte swizzle.
+// y_map: rect mode 4-D {C_out, W_out, H_out, N} box {ychunk, rect_w, 32/rect_w, 1},
+// else 2-D {C_out, pixels} box {ychunk, 32}; 128-byte swizzle for ychunk 64, 64-byte
+// for 32.  p.pair selects the CTA-pair kernel (grid even, clusters of 2).
 cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, const CUtensorMap& y_map,
                            const TcGemmParams& p, int grid, cudaStream_t stream);
 
-// CTA-pair variant (clusters of 2, tcgen05.mma.cta_group::2, M = 256 per pair);
-// p.stages / p.smem_bytes sized for B buffers of mma_n / 2 rows.  grid is even.
-cudaError_t launch_tc_gemm_pair(const CUtensorMap& a_map, const CUtensorMap& b_map, const CUtensorMap& y_map,
-                                const TcGemmParams& p, int grid, cudaStream_t stream);
 // Co-resident 2-CTA clusters of the pair kernel at p.smem_bytes (0 if unknown).
 int tc_gemm_pair_max_clusters(const TcGemmParams& p);
 

@@ -85,4 +85,41 @@ __device__ __forceinline__ void stage_row32(const uint32_t (&v)[32], const float
     }
 }
 
+// Half of a 64-column store tile with 128-byte rows (128-byte swizzle: chunk j
+// of row r at chunk j ^ (r & 7)): thread `r` writes columns [32*half, 32*half+32)
+// of its row.  The Y tensor map for these tiles uses a 64-channel box and
+// SWIZZLE_128B.
+__device__ __forceinline__ void stage_half_row64(const uint32_t (&v)[32], const float* bias, int relu, uint8_t* stg,
+                                                 int r, int half) {
+    float f[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+    if (bias != nullptr) {
+        const float4* b4 = reinterpret_cast<const float4*>(bias);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 b = b4[i];
+            f[4 * i + 0] += b.x;
+            f[4 * i + 1] += b.y;
+            f[4 * i + 2] += b.z;
+            f[4 * i + 3] += b.w;
+        }
+    }
+    if (relu) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) f[i] = fmaxf(f[i], 0.0f);
+    }
+    uint8_t* row = stg + r * 128;
+    const int sw = r & 7;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint4 q;
+        q.x = pack_bf16x2(f[8 * j + 0], f[8 * j + 1]);
+        q.y = pack_bf16x2(f[8 * j + 2], f[8 * j + 3]);
+        q.z = pack_bf16x2(f[8 * j + 4], f[8 * j + 5]);
+        q.w = pack_bf16x2(f[8 * j + 6], f[8 * j + 7]);
+        *reinterpret_cast<uint4*>(row + (((4 * half + j) ^ sw) << 4)) = q;
+    }
+}
+
 }  // namespace convgb

@@ -54,8 +54,9 @@ enum {
     CONV_FLAG_BIAS = 1u,       /* add bias[co] after the sum                          */
     CONV_FLAG_RELU = 2u,       /* max(., 0) after the bias                            */
     CONV_FLAG_OUT_BF16 = 4u,   /* CONV_F32 only: write y as BF16 (round to nearest even) */
-    CONV_FLAG_SINGLE_SM = 8u   /* tensor-core paths: one CTA per tile, never an SM pair
-                                  (default: SM pairs whenever the shape has >= 2 pixel tiles) */
+    CONV_FLAG_SM_PAIRS = 8u    /* tensor-core GEMM paths: run each MMA on an SM pair
+                                  (clusters of 2, 256 pixels per MMA, weight rows split
+                                  between the two SMs) instead of one SM per 128 pixels */
 };
 
 typedef enum {

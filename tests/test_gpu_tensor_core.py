@@ -39,13 +39,13 @@ pytestmark = pytest.mark.gpu
     (ConvShape(2, 1, 20, 32, 32, 7, 7, 2, 3, 1, 1, "bf16", True, True), "small_k_gemm"),      # 49 taps
     (ConvShape(1, 8, 12, 16, 256, 2, 2, 1, 0, 2, 1, "bf16", False, True), "small_k_gemm"),    # dilation
 ])
-@pytest.mark.parametrize("single_sm", [False, True], ids=["sm_pairs", "single_sm"])
-def test_tensor_core_small_shapes_full(shape, path, single_sm):
+@pytest.mark.parametrize("sm_pairs", [False, True], ids=["single_sm", "sm_pairs"])
+def test_tensor_core_small_shapes_full(shape, path, sm_pairs):
     """Every output, on both tcgen05 GEMM kernels: CTA pairs (cta_group::2, M = 256)
     and one CTA per tile (cta_group::1, M = 128)."""
     from cnn_convolution_implicit_gb300 import ConvPlan
     x, w, b = draw(shape, (31, 32, 33))
-    plan, y = run(shape, x, w, b, plan=ConvPlan.for_shape(shape, single_sm=single_sm))
+    plan, y = run(shape, x, w, b, plan=ConvPlan.for_shape(shape, sm_pairs=sm_pairs))
     assert plan.path == path
     check_full(shape, y, oracle_full(shape, x, w, b))
 
@@ -67,11 +67,11 @@ def test_stem_full_size_all_outputs():
     check_full(s, y, oracle_full(s, x, w, b))
 
 
-def test_body_full_size_single_sm_kernel():
-    """The single-CTA kernel on the full body layer: seeded points."""
+def test_body_full_size_sm_pairs_kernel():
+    """The SM-pair kernel on the full body layer: seeded points."""
     from cnn_convolution_implicit_gb300 import ConvPlan
     s, x, w, b = inputs("body")
-    plan, y = run(s, x, w, b, plan=ConvPlan.for_shape(s, single_sm=True))
+    plan, y = run(s, x, w, b, plan=ConvPlan.for_shape(s, sm_pairs=True))
     check_points(s, y, x, w, b, sample_points(s, 4096, 13))
 
 
