@@ -158,13 +158,13 @@ bool configure_tc(conv_plan* pl, bool one_by_one) {
     }
     t.num_n_tiles = g.C_out / n_tile;
     t.num_tiles = t.num_m_tiles * t.num_n_tiles;
-    t.ychunk = n_tile % 64 == 0 ? 64 : 32;
+    t.ychunk = 32;
     // SM pairs (one MMA over 2 x 128 pixels, weight rows split between the two
     // CTAs) on request, when there are at least two pixel tiles to pair up.
     t.pair = (t.num_m_tiles >= 2 && (pl->flags & CONV_FLAG_SM_PAIRS)) ? 1 : 0;
     const int b_rows = t.pair ? mma_n / 2 : mma_n;
     const int stage_bytes = kTcBlockM * kTcBlockK * 2 + b_rows * 128;
-    const int fixed = 1024 + 256 + 4 * 2 * 32 * 128;  // alignment, barriers, epilogue store tiles
+    const int fixed = 1024 + 256 + 8 * 2 * 32 * 64;  // alignment, barriers, epilogue store tiles
     int stages = (pl->smem_optin - fixed) / stage_bytes;
     if (stages > 8) stages = 8;
     if (stages < 2) return false;

@@ -54,7 +54,7 @@ cudaError_t launch_depthwise(const CUtensorMap& x_map, const DepthwiseParams& p,
 // ---------------------------------------------------------------- tcgen05 GEMM (1x1 and implicit)
 constexpr int kTcBlockM = 128;    // pixels per tile (TMEM lanes)
 constexpr int kTcBlockK = 64;     // BF16 elements per K-step (one 128-byte swizzle row)
-constexpr int kTcThreads = 192;   // producer warp, MMA warp, 4 epilogue warps
+constexpr int kTcThreads = 320;   // producer warp, MMA warp, 2 x 4 epilogue warps
 
 enum TcMode { kTcMode1x1 = 0, kTcModeIm2col = 1, kTcModeRect = 2 };
 
@@ -69,7 +69,7 @@ struct TcGemmParams {
     int num_m_tiles, num_n_tiles, num_tiles;
     int rect_w, rect_h;              // kTcModeRect: pixel tile = rect_h x rect_w output pixels
     int rect_tiles_w, rect_tiles_h;  // rectangles per image row / column
-    int ychunk;                      // output channels per TMA store (64: 128-byte rows, or 32)
+    int ychunk;                      // output channels per TMA store (32: 64-byte rows)
     int stages;
     int tmem_cols;     // power of two >= 2 * n_tile
     int smem_bytes;
@@ -81,9 +81,9 @@ struct TcGemmParams {
 };
 // a_map: rect mode 4-D tiled {C_in, W, H, N} box {64, rect_w, rect_h, 1}; im2col
 // mode 4-D im2col; 1x1 mode 2-D {C_in, pixels} box {64, 128}; all 128-byte swizzle.
-// y_map: rect mode 4-D {C_out, W_out, H_out, N} box {ychunk, rect_w, 32/rect_w, 1},
-// else 2-D {C_out, pixels} box {ychunk, 32}; 128-byte swizzle for ychunk 64, 64-byte
-// for 32.  p.pair selects the CTA-pair kernel (grid even, clusters of 2).
+// y_map: rect mode 4-D {C_out, W_out, H_out, N} box {32, rect_w, 32/rect_w, 1},
+// else 2-D {C_out, pixels} box {32, 32}; 64-byte swizzle.  p.pair selects the
+// CTA-pair kernel (grid even, clusters of 2).
 cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, const CUtensorMap& y_map,
                            const TcGemmParams& p, int grid, cudaStream_t stream);
 

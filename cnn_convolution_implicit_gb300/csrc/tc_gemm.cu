@@ -24,10 +24,11 @@
 // Groups are independent GEMMs (variants page, sections 2.2 and 4.3): a tile
 // packs `gpc` groups side by side in TMEM columns, each with its own K loop.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over tiles):
+// Warp roles (320 threads, one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer (one lane): A (pixels x 64 ch) and B (C_out x 64) per K-step
 //   warp 1      TMEM allocator; one lane issues tcgen05.mma and commits
-//   warps 2..5  epilogue: tcgen05.ld -> +bias -> ReLU -> BF16 -> swizzled smem -> TMA store
+//   warps 2..9  epilogue, two groups of four (one per TMEM accumulator):
+//               tcgen05.ld -> +bias -> ReLU -> BF16 -> swizzled smem -> TMA store
 // Shared memory holds a ring of `stages` (A, B) buffers; TMEM holds two
 // accumulators so the epilogue of tile i overlaps the MMAs of tile i+1.
 //
@@ -46,7 +47,7 @@ namespace convgb {
 namespace {
 
 constexpr uint32_t kABytes = kTcBlockM * kTcBlockK * 2;  // 16 KB
-constexpr uint32_t kOutTileBytes = 32 * 128;              // one store tile: 32 pixels x <= 128 bytes
+constexpr uint32_t kOutTileBytes = 32 * 64;               // one store tile: 32 pixels x 32 channels
 
 struct TcSmem {
     uint8_t* a;
@@ -67,7 +68,7 @@ __device__ __forceinline__ TcSmem carve(uint8_t* raw, const TcGemmParams& p, uin
     s.a = base;
     s.b = base + p.stages * kABytes;
     s.out = s.b + p.stages * b_bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s.out + 4 * 2 * kOutTileBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s.out + 8 * 2 * kOutTileBytes);
     s.full = bars;
     s.empty = bars + p.stages;
     s.tfull = bars + 2 * p.stages;
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.tfull[b], 1);
-            mbar_init(&sm.tempty[b], PAIR ? 2 * 4 : 4);  // one arrival per epilogue warp (of both CTAs)
+            mbar_init(&sm.tempty[b], PAIR ? 2 * 4 : 4);  // one arrival per warp of its epilogue group (both CTAs)
         }
         mbar_init(sm.drain, 1);
         *sm.abort = 0;
@@ -316,15 +317,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        // TMEM -> registers (+bias, ReLU, BF16) -> swizzled smem tile -> TMA store,
-        // 32 pixels x ychunk channels at a time, two store tiles in flight per warp.
-        const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+        // Two groups of four warps, one per TMEM accumulator: group e takes the
+        // tiles that land in buffer e, so two tiles drain at once.  Per 32-column
+        // chunk: tcgen05.ld (the next chunk's load is in flight while this one
+        // is processed) -> +bias, ReLU, BF16 -> swizzled smem tile -> TMA store;
+        // two store tiles in flight per warp.
+        const int quarter = warp & 3;             // TMEM lane quarter this warp may access
+        const int group = (warp - 2) >> 2;        // = the accumulator buffer it drains
         uint8_t* stg = sm.out + (warp - 2) * 2 * kOutTileBytes;
-        const int ychunk = p.ychunk;
         int sbuf = 0;
         int local = 0;
         for (int u = unit0; u < num_units; u += unit_step, ++local) {
             const int buf = local & 1;
+            if (buf != group) continue;
             const uint32_t use = static_cast<uint32_t>(local >> 1) & 1u;
             // warp-uniform outcome, so the .sync.aligned TMEM loads below stay converged
             const bool ready = __all_sync(0xffffffffu, mbar_wait(&sm.tfull[buf], use, abort));
@@ -355,32 +360,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int co0 = nt * p.n_tile;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(buf * p.n_tile);
-            for (int c = 0; c < p.n_tile; c += ychunk) {
-                uint32_t v[32];
-                if (lane == 0) bulk_wait_read_le1();  // the tile written two chunks ago is free
-                __syncwarp();
-                uint8_t* dst = stg + sbuf * kOutTileBytes;
-                for (int h = 0; h < ychunk; h += 32) {
+            uint32_t va[32], vb[32];
+            __syncwarp();
+            tmem_ld32(t_row, va);
+            for (int c = 0; c < p.n_tile; c += 64) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int cc = c + 32 * h;
+                    if (cc >= p.n_tile) break;
+                    uint32_t(&cur)[32] = h == 0 ? va : vb;
+                    uint32_t(&nxt)[32] = h == 0 ? vb : va;
+                    tmem_ld_wait(cur);                 // chunk cc is in registers
+                    if (cc + 32 < p.n_tile) {          // start the next chunk's load
+                        __syncwarp();
+                        tmem_ld32(t_row + static_cast<uint32_t>(cc + 32), nxt);
+                    }
+                    if (lane == 0) bulk_wait_read_le1();  // the tile written two chunks ago is free
                     __syncwarp();
-                    tmem_ld32(t_row + static_cast<uint32_t>(c + h), v);
-                    tmem_ld_wait();
-                    const float* bias = p.bias ? p.bias + co0 + c + h : nullptr;
-                    if (ychunk == 64)
-                        stage_half_row64(v, bias, p.relu, dst, lane, h >> 5);
-                    else
-                        stage_row32(v, bias, p.relu, dst, lane);
+                    uint8_t* dst = stg + sbuf * kOutTileBytes;
+                    stage_row32(cur, p.bias ? p.bias + co0 + cc : nullptr, p.relu, dst, lane);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && rows_exist) {
+                        if (p.mode == kTcModeRect)
+                            tma_store_4d(&y_map, dst, co0 + cc, yc1, yc2, yc3);
+                        else
+                            tma_store_2d(&y_map, dst, co0 + cc, yc1);
+                        bulk_commit();
+                    }
+                    sbuf ^= 1;
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0 && rows_exist) {
-                    if (p.mode == kTcModeRect)
-                        tma_store_4d(&y_map, dst, co0 + c, yc1, yc2, yc3);
-                    else
-                        tma_store_2d(&y_map, dst, co0 + c, yc1);
-                    bulk_commit();
-                }
-                sbuf ^= 1;
             }
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {

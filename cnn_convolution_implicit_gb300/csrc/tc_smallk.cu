@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                     uint32_t v[32];
                     __syncwarp();
                     tmem_ld32(t_row + static_cast<uint32_t>(c), v);
-                    tmem_ld_wait();
+                    tmem_ld_wait(v);
                     if (lane == 0) bulk_wait_read_le1();
                     __syncwarp();
                     uint8_t* dst = stg + sbuf * kSkOutBytes;
