@@ -141,6 +141,69 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+class NvmlClockSampler:
+    """SM clock and clock-event reasons read through NVML (ctypes, read-only)
+    every few ms from a background thread while the timed region runs."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid, period_s=0.004):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle for %s" % uuid)
+        self.reason_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))  # NVML_CLOCK_SM
+        self.max_mhz = mx.value
+        self.period = period_s
+        self.samples = []
+        self.reasons = 0
+        self._stop = threading.Event()
+
+    def _run(self):
+        ct = self.ct
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        while not self._stop.is_set():
+            if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if self.reason_fn(self.h, ct.byref(rs)) == 0:
+                self.reasons |= rs.value
+            time.sleep(self.period)
+
+    def start(self):
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+        time.sleep(2 * self.period)
+
+    def stop(self):
+        self._stop.set()
+        self.thread.join(timeout=2)
+        if not self.samples:
+            return None
+        return {"sm_mhz": float(np.median(self.samples)), "sm_max_mhz": float(self.max_mhz),
+                "samples": len(self.samples), "source": "nvml",
+                "reasons": sorted(v for k, v in self.REASONS.items() if self.reasons & k)}
+
+
+def clock_sampler(local):
+    """NVML sampler for this rank's GPU, else nvidia-smi."""
+    try:
+        gpu_id = "GPU-%s" % torch.cuda.get_device_properties(local).uuid
+    except Exception:
+        gpu_id = str(local)
+    try:
+        return NvmlClockSampler(gpu_id)
+    except Exception as e:
+        sys.stderr.write("NVML sampler unavailable (%s); using nvidia-smi\n" % e)
+        return ClockSampler(gpu_id)
+
+
 # ----------------------------------------------------------------------------- timing
 def time_steps(fn, steps, warmup, flush):
     """Per-step CUDA-event time of fn() on the current stream, L2 flushed
@@ -244,7 +307,7 @@ class OracleSampler:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -307,11 +370,7 @@ def main():
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    try:
-        gpu_id = "GPU-%s" % torch.cuda.get_device_properties(local).uuid
-    except Exception:
-        gpu_id = str(local)
-    clocks = ClockSampler(gpu_id)
+    clocks = clock_sampler(local)
     clocks.start()
     ms = time_steps(lambda: plan.forward(xd, wd, bd, y), args.steps, args.warmup, flush)
     clk = clocks.stop()
