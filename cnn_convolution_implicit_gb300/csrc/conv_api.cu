@@ -36,6 +36,7 @@ struct conv_plan {
     int device;
     int num_sms;
     int smem_optin;
+    int smem_per_sm;
     int pair_clusters;  // co-resident 2-CTA clusters of the pair kernel (0: unknown)
     unsigned* status;
     // per-path configuration
@@ -220,7 +221,7 @@ bool configure_depthwise(conv_plan* pl) {
     DepthwiseParams& d = pl->dw;
     if (!(g.G == g.C_in && g.C_out == g.C_in)) return false;
     if (g.C_in % 32 != 0) return false;
-    if (!depthwise_config(g, pl->smem_optin, pl->num_sms, d)) return false;
+    if (!depthwise_config(g, pl->smem_per_sm, pl->num_sms, d)) return false;
     d.g = g;
     d.relu = (pl->flags & CONV_FLAG_RELU) ? 1 : 0;
     d.out_bf16 = (pl->flags & CONV_FLAG_OUT_BF16) ? 1 : 0;
@@ -381,10 +382,13 @@ conv_status conv_plan_create(conv_plan** out, int N, int C_in, int H, int W, int
         pl->device = -1;
         pl->num_sms = 152;
         pl->smem_optin = 232448;
+        pl->smem_per_sm = 233472;
         pl->status = nullptr;
     } else if (cudaGetDevice(&pl->device) != cudaSuccess ||
                cudaDeviceGetAttribute(&pl->num_sms, cudaDevAttrMultiProcessorCount, pl->device) != cudaSuccess ||
                cudaDeviceGetAttribute(&pl->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, pl->device) !=
+                   cudaSuccess ||
+               cudaDeviceGetAttribute(&pl->smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, pl->device) !=
                    cudaSuccess ||
                cudaGetSymbolAddress(reinterpret_cast<void**>(&pl->status), g_conv_status_word) != cudaSuccess) {
         cudaGetLastError();

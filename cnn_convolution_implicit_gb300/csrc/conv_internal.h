@@ -48,7 +48,7 @@ struct DepthwiseParams {
     unsigned* status;
 };
 // Fills the tiling fields of d; returns 0 if the shape does not fit the kernel.
-int depthwise_config(const ConvGeom& g, int smem_optin, int num_sms, DepthwiseParams& d);
+int depthwise_config(const ConvGeom& g, int smem_per_sm, int num_sms, DepthwiseParams& d);
 cudaError_t launch_depthwise(const CUtensorMap& x_map, const DepthwiseParams& p, cudaStream_t stream);
 
 // ---------------------------------------------------------------- tcgen05 GEMM (1x1 and implicit)

@@ -12,9 +12,9 @@
 // the zero padding (section 26), and a dilated kernel reads only its Kh*Kw
 // live taps.
 //
-// The kernel is persistent (one CTA per SM) and keeps a ring of `stages` halo
-// tiles in flight, so HBM reads of the next tiles overlap the arithmetic and
-// stores of the current one.  When the channel blocks fit in the grid, every
+// The kernel is persistent (two CTAs per SM) and each CTA keeps a ring of
+// `stages` halo tiles in flight, so HBM reads of the next tiles overlap the
+// arithmetic and stores of the current one.  When the channel blocks fit in the grid, every
 // CTA stays on one 32-channel block, so its weights are read once.  Each of
 // the 256 threads owns 4 channels (one float4: 128-bit shared loads and global
 // stores) of one output column and walks a run of output rows.  For stride 1
@@ -31,6 +31,7 @@ namespace {
 constexpr int kDwChannels = 32;  // channels per tile: one 128-byte TMA row
 constexpr int kDwThreads = 256;  // 8 channel quads x TW columns x (32 / TW) row groups
 constexpr int kDwMaxStages = 8;
+constexpr int kDwCtasPerSm = 2;  // two resident CTAs: one computes and stores while the other's loads land
 
 __device__ __forceinline__ void fma4(float4& acc, const float4& a, const float4& w) {
     acc.x = fmaf(a.x, w.x, acc.x);
@@ -130,7 +131,7 @@ __device__ __forceinline__ float4 dw_row3(const float4 (&w)[9], const float4& bi
 
 // K > 0: square K x K kernel known at compile time; K == 0: any Kh x Kw.
 template <int K, int TW>
-__global__ void __launch_bounds__(kDwThreads, 1)
+__global__ void __launch_bounds__(kDwThreads, kDwCtasPerSm)
     depthwise_kernel(const __grid_constant__ CUtensorMap x_map, const DepthwiseParams p) {
     constexpr int kRowGroups = kDwThreads / (8 * TW);
     constexpr int kTaps = K > 0 ? K * K : 1;
@@ -271,11 +272,13 @@ __global__ void __launch_bounds__(kDwThreads, 1)
     }
 }
 
-int depthwise_config(const ConvGeom& g, int smem_optin, int num_sms, DepthwiseParams& d) {
+int depthwise_config(const ConvGeom& g, int smem_per_sm, int num_sms, DepthwiseParams& d) {
     // Tile width 8 or 16 columns (a warp never straddles two row groups),
     // height from {32, 28, 24, 16} with the least ragged-edge waste, then as
-    // many ring stages (<= 8) as fit in shared memory; shrink the height if
-    // fewer than two stages fit (large strides or dilations).
+    // many ring stages (<= 8) as fit in a CTA's share of shared memory (two
+    // CTAs per SM); shrink the height if fewer than two stages fit (large
+    // strides or dilations).
+    const int smem_per_cta = smem_per_sm / kDwCtasPerSm - 1024;  // 1 KB per CTA is reserved
     auto padded = [](int extent, int t) { return ((extent + t - 1) / t) * t; };
     const int tw = padded(g.W_out, 8) < padded(g.W_out, 16) ? 8 : 16;
     const int rg = kDwThreads / (8 * tw);
@@ -287,7 +290,7 @@ int depthwise_config(const ConvGeom& g, int smem_optin, int num_sms, DepthwisePa
         const int in_h = (th - 1) * g.S + (g.Kh - 1) * g.D + 1;
         const int in_w = (tw - 1) * g.S + (g.Kw - 1) * g.D + 1;
         const long long stage = static_cast<long long>(in_h) * in_w * kDwChannels * 4;
-        long long stages = (smem_optin - 1024 - 128) / stage;
+        long long stages = (smem_per_cta - 128 - 256) / stage;  // alignment slack, static barriers
         if (stages > kDwMaxStages) stages = kDwMaxStages;
         if (in_h <= 256 && in_w <= 256 && (stages >= 2 || (th <= rg && stages >= 1))) {
             d.tile_w = tw;
@@ -307,10 +310,11 @@ int depthwise_config(const ConvGeom& g, int smem_optin, int num_sms, DepthwisePa
     const long long tiles = static_cast<long long>(g.N) * d.tiles_h * d.tiles_w * d.cblocks;
     if (tiles > 0x7fffffffLL) return 0;
     d.num_tiles = static_cast<int>(tiles);
-    // grid: one CTA per SM; a multiple of the channel blocks when they fit, so
+    // grid: two CTAs per SM; a multiple of the channel blocks when they fit, so
     // each CTA keeps one channel block (and its weights) for its whole run
-    d.fixed_cb = d.cblocks <= num_sms ? 1 : 0;
-    int grid = d.fixed_cb ? (num_sms / d.cblocks) * d.cblocks : num_sms;
+    const int slots = kDwCtasPerSm * num_sms;
+    d.fixed_cb = d.cblocks <= slots ? 1 : 0;
+    int grid = d.fixed_cb ? (slots / d.cblocks) * d.cblocks : slots;
     if (grid > d.num_tiles) grid = d.num_tiles;  // still a multiple of cblocks
     d.grid = grid;
     return 1;
