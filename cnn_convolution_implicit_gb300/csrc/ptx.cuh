@@ -380,6 +380,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// max(., 0) then BF16 round-to-nearest-even of two values in one conversion
+// (`hi` lands in the upper 16 bits).
+__device__ __forceinline__ uint32_t pack_bf16x2_relu(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.relu.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
 __device__ __forceinline__ void record_status(unsigned* status, unsigned bits, volatile int* abort) {
     if (abort) *abort = 1;
     if (status) atomicOr(status, bits);

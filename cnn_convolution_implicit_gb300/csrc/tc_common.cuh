@@ -10,48 +10,14 @@
 
 namespace convgb {
 
-// v: 32 FP32 accumulators of one output pixel (columns co .. co+31, raw bits).
-// bias: bias + co, or nullptr.  dst: y + pixel*C_out + co (16-byte aligned).
-__device__ __forceinline__ void epilogue_store32(const uint32_t (&v)[32], const float* bias, int relu,
-                                                 __nv_bfloat16* dst, bool valid) {
-    float f[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-    if (bias != nullptr) {
-        const float4* b4 = reinterpret_cast<const float4*>(bias);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 b = __ldg(b4 + i);
-            f[4 * i + 0] += b.x;
-            f[4 * i + 1] += b.y;
-            f[4 * i + 2] += b.z;
-            f[4 * i + 3] += b.w;
-        }
-    }
-    if (relu) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) f[i] = fmaxf(f[i], 0.0f);
-    }
-    if (!valid) return;
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint4 q;
-        q.x = pack_bf16x2(f[8 * i + 0], f[8 * i + 1]);
-        q.y = pack_bf16x2(f[8 * i + 2], f[8 * i + 3]);
-        q.z = pack_bf16x2(f[8 * i + 4], f[8 * i + 5]);
-        q.w = pack_bf16x2(f[8 * i + 6], f[8 * i + 7]);
-        d4[i] = q;
-    }
-}
-
 // Staging of one 32-column chunk for a TMA store: thread `r` (0..31) writes the
 // bias + ReLU + BF16 result of its row (64 bytes) into a 32 x 64-byte tile laid
 // out in the 64-byte swizzle pattern (16-byte chunk j of row r at chunk
 // j ^ ((r >> 1) & 3)), which the Y tensor map (box 32 x 32, SWIZZLE_64B) reads.
 // Eight consecutive rows hit eight distinct bank groups, so the warp's stores
-// are conflict-free.
-// `bias` may point to global or shared memory (generic loads).
+// are conflict-free.  SMEM_BIAS: `bias` points to shared memory (else global,
+// read through the read-only path).
+template <bool SMEM_BIAS = false>
 __device__ __forceinline__ void stage_row32(const uint32_t (&v)[32], const float* bias, int relu, uint8_t* stg,
                                             int r) {
     float f[32];
@@ -61,64 +27,35 @@ __device__ __forceinline__ void stage_row32(const uint32_t (&v)[32], const float
         const float4* b4 = reinterpret_cast<const float4*>(bias);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float4 b = b4[i];
+            const float4 b = SMEM_BIAS ? b4[i] : __ldg(b4 + i);
             f[4 * i + 0] += b.x;
             f[4 * i + 1] += b.y;
             f[4 * i + 2] += b.z;
             f[4 * i + 3] += b.w;
         }
-    }
-    if (relu) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) f[i] = fmaxf(f[i], 0.0f);
     }
     uint8_t* row = stg + r * 64;
     const int sw = (r >> 1) & 3;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        uint4 q;
-        q.x = pack_bf16x2(f[8 * j + 0], f[8 * j + 1]);
-        q.y = pack_bf16x2(f[8 * j + 2], f[8 * j + 3]);
-        q.z = pack_bf16x2(f[8 * j + 4], f[8 * j + 5]);
-        q.w = pack_bf16x2(f[8 * j + 6], f[8 * j + 7]);
-        *reinterpret_cast<uint4*>(row + ((j ^ sw) << 4)) = q;
-    }
-}
-
-// Half of a 64-column store tile with 128-byte rows (128-byte swizzle: chunk j
-// of row r at chunk j ^ (r & 7)): thread `r` writes columns [32*half, 32*half+32)
-// of its row.  The Y tensor map for these tiles uses a 64-channel box and
-// SWIZZLE_128B.
-__device__ __forceinline__ void stage_half_row64(const uint32_t (&v)[32], const float* bias, int relu, uint8_t* stg,
-                                                 int r, int half) {
-    float f[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-    if (bias != nullptr) {
-        const float4* b4 = reinterpret_cast<const float4*>(bias);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 b = b4[i];
-            f[4 * i + 0] += b.x;
-            f[4 * i + 1] += b.y;
-            f[4 * i + 2] += b.z;
-            f[4 * i + 3] += b.w;
-        }
-    }
     if (relu) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) f[i] = fmaxf(f[i], 0.0f);
-    }
-    uint8_t* row = stg + r * 128;
-    const int sw = r & 7;
+        for (int j = 0; j < 4; ++j) {
+            uint4 q;
+            q.x = pack_bf16x2_relu(f[8 * j + 0], f[8 * j + 1]);
+            q.y = pack_bf16x2_relu(f[8 * j + 2], f[8 * j + 3]);
+            q.z = pack_bf16x2_relu(f[8 * j + 4], f[8 * j + 5]);
+            q.w = pack_bf16x2_relu(f[8 * j + 6], f[8 * j + 7]);
+            *reinterpret_cast<uint4*>(row + ((j ^ sw) << 4)) = q;
+        }
+    } else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        uint4 q;
-        q.x = pack_bf16x2(f[8 * j + 0], f[8 * j + 1]);
-        q.y = pack_bf16x2(f[8 * j + 2], f[8 * j + 3]);
-        q.z = pack_bf16x2(f[8 * j + 4], f[8 * j + 5]);
-        q.w = pack_bf16x2(f[8 * j + 6], f[8 * j + 7]);
-        *reinterpret_cast<uint4*>(row + (((4 * half + j) ^ sw) << 4)) = q;
+        for (int j = 0; j < 4; ++j) {
+            uint4 q;
+            q.x = pack_bf16x2(f[8 * j + 0], f[8 * j + 1]);
+            q.y = pack_bf16x2(f[8 * j + 2], f[8 * j + 3]);
+            q.z = pack_bf16x2(f[8 * j + 4], f[8 * j + 5]);
+            q.w = pack_bf16x2(f[8 * j + 6], f[8 * j + 7]);
+            *reinterpret_cast<uint4*>(row + ((j ^ sw) << 4)) = q;
+        }
     }
 }
 

@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                     if (lane == 0) bulk_wait_read_le1();
                     __syncwarp();
                     uint8_t* dst = stg + sbuf * kSkOutBytes;
-                    stage_row32(v, p.bias ? sm.bias + c : nullptr, p.relu, dst, lane);
+                    stage_row32<true>(v, p.bias ? sm.bias + c : nullptr, p.relu, dst, lane);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0 && rows_exist) {  // columns past W_out fall outside the map: not written
