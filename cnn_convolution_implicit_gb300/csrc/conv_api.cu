@@ -107,10 +107,15 @@ bool configure_tc(conv_plan* pl, bool one_by_one) {
         n_tile = mma_n = 256;
         gpc = 1;
     } else {
+        // groups packed per tile: the MMA issuer holds one ring stage per group at
+        // once, so gpc is also bounded by the stages that fit
         mma_n = g.cout_g;
+        const int stage_bytes = kTcBlockM * kTcBlockK * 2 + mma_n * 128;
+        const int max_gpc_stages = (pl->smem_optin - (1024 + 256 + 8 * 2 * 32 * 64)) / stage_bytes;
         gpc = 0;
         for (int c = g.G; c >= 1; --c)
-            if (g.G % c == 0 && c * g.cout_g <= 256 && (c * g.cout_g) % 32 == 0) {
+            if (g.G % c == 0 && c * g.cout_g <= 256 && (c * g.cout_g) % 32 == 0 && c <= kTcMaxGroupsPerTile &&
+                c <= max_gpc_stages) {
                 gpc = c;
                 break;
             }
@@ -168,7 +173,7 @@ bool configure_tc(conv_plan* pl, bool one_by_one) {
     const int fixed = 1024 + 256 + 8 * 2 * 32 * 64;  // alignment, barriers, epilogue store tiles
     int stages = (pl->smem_optin - fixed) / stage_bytes;
     if (stages > 8) stages = 8;
-    if (stages < 2) return false;
+    if (stages < 2 || stages < gpc) return false;
     t.stages = stages;
     t.smem_bytes = fixed + stages * stage_bytes;
     t.tmem_cols = pow2_at_least(2 * n_tile);

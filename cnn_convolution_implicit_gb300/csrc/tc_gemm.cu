@@ -210,10 +210,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int m = PAIR ? 2 * mu + static_cast<int>(rank) : mu;
                 PixTile t = pix_tile(p, m);
                 if (!t.exists) t = pix_tile(p, p.num_m_tiles - 1);  // a valid tile whose result is never stored
-                for (int j = 0; j < p.gpc && ok; ++j) {
-                    int grp, brow;
-                    sub_gemm(p, nt, j, grp, brow);
-                    for (int ks = 0; ks < p.ksteps; ++ks) {
+                // K-steps tap-major, group-minor: the MMA issuer interleaves the groups'
+                // independent accumulators instead of running one dependent chain per group
+                for (int ks = 0; ks < p.ksteps && ok; ++ks) {
+                    for (int j = 0; j < p.gpc; ++j) {
+                        int grp, brow;
+                        sub_gemm(p, nt, j, grp, brow);
                         if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
                             record_status(p.status, kStatusTimeoutProducer, abort);
                             ok = false;
@@ -272,33 +274,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_base = tmem_base + static_cast<uint32_t>(buf * p.n_tile);
-                for (int j = 0; j < p.gpc && ok; ++j) {
-                    const uint32_t d = d_base + static_cast<uint32_t>(j * p.mma_n);
-                    for (int ks = 0; ks < p.ksteps; ++ks) {
+                for (int ks = 0; ks < p.ksteps && ok; ++ks) {
+                    // the gpc stages of this K-step (one per group; gpc <= stages): stage0 + j mod stages
+                    const int stage0 = stage;
+                    for (int j = 0; j < p.gpc; ++j) {
                         if (!mbar_wait(&sm.full[stage], phase, abort)) {
                             record_status(p.status, kStatusTimeoutMma, abort);
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
-                        const uint64_t adesc = sdesc_sw128(smem_addr(sm.a + stage * kABytes));
-                        const uint64_t bdesc = sdesc_sw128(smem_addr(sm.b + stage * b_bytes));
-#pragma unroll
-                        for (int k = 0; k < kTcBlockK / 16; ++k) {
-                            // +32 bytes along K inside the swizzle row = +2 in the >>4 address field
-                            if constexpr (PAIR)
-                                mma_bf16_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
-                            else
-                                mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
-                        }
-                        if constexpr (PAIR)
-                            mma_commit_pair(&sm.empty[stage], 0x3);
-                        else
-                            mma_commit(&sm.empty[stage]);
                         if (++stage == p.stages) {
                             stage = 0;
                             phase ^= 1u;
                         }
+                    }
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < kTcBlockK / 16; ++k) {
+                        // +32 bytes along K inside the swizzle row = +2 in the >>4 address field
+                        for (int j = 0, sj = stage0; j < p.gpc; ++j, sj = sj + 1 == p.stages ? 0 : sj + 1) {
+                            const uint32_t d = d_base + static_cast<uint32_t>(j * p.mma_n);
+                            const uint64_t adesc = sdesc_sw128(smem_addr(sm.a + sj * kABytes)) + 2 * k;
+                            const uint64_t bdesc = sdesc_sw128(smem_addr(sm.b + sj * b_bytes)) + 2 * k;
+                            if constexpr (PAIR)
+                                mma_bf16_pair(d, adesc, bdesc, idesc, (ks | k) != 0 ? 1u : 0u);
+                            else
+                                mma_bf16(d, adesc, bdesc, idesc, (ks | k) != 0 ? 1u : 0u);
+                        }
+                    }
+                    for (int j = 0, sj = stage0; j < p.gpc; ++j, sj = sj + 1 == p.stages ? 0 : sj + 1) {
+                        if constexpr (PAIR)
+                            mma_commit_pair(&sm.empty[sj], 0x3);
+                        else
+                            mma_commit(&sm.empty[sj]);
                     }
                 }
                 if (ok) {

@@ -279,12 +279,13 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 }
                 tc_fence_after();
                 const int rows = min(R, p.num_segments - tile * R);
-                for (int j = 0; j < rows; ++j) {
-                    const uint64_t adesc = a_desc(p, smem_addr(sm.a + (stage * R + j) * a_tile_bytes(p)));
-                    const uint32_t d = tmem_base + static_cast<uint32_t>((buf * R + j) * n_tile);
-                    for (int k = 0; k < p.kmma; ++k)
+                // K slices outer, segments inner: consecutive MMAs go to independent accumulators
+                for (int k = 0; k < p.kmma; ++k)
+                    for (int j = 0; j < rows; ++j) {
+                        const uint64_t adesc = a_desc(p, smem_addr(sm.a + (stage * R + j) * a_tile_bytes(p)));
+                        const uint32_t d = tmem_base + static_cast<uint32_t>((buf * R + j) * n_tile);
                         mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, k != 0 ? 1u : 0u);
-                }
+                    }
                 mma_commit(&sm.empty[stage]);
                 mma_commit(&sm.tfull[buf]);
                 if (++stage == p.stages) {
