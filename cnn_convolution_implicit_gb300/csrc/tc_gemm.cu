@@ -274,40 +274,80 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_base = tmem_base + static_cast<uint32_t>(buf * p.n_tile);
-                for (int ks = 0; ks < p.ksteps && ok; ++ks) {
-                    // the gpc stages of this K-step (one per group; gpc <= stages): stage0 + j mod stages
-                    const int stage0 = stage;
-                    for (int j = 0; j < p.gpc; ++j) {
+                if (p.gpc == 1) {
+                    for (int ks = 0; ks < p.ksteps; ++ks) {
                         if (!mbar_wait(&sm.full[stage], phase, abort)) {
                             record_status(p.status, kStatusTimeoutMma, abort);
                             ok = false;
                             break;
                         }
+                        tc_fence_after();
+                        const uint64_t adesc = sdesc_sw128(smem_addr(sm.a + stage * kABytes));
+                        const uint64_t bdesc = sdesc_sw128(smem_addr(sm.b + stage * b_bytes));
+#pragma unroll
+                        for (int k = 0; k < kTcBlockK / 16; ++k) {
+                            // +32 bytes along K inside the swizzle row = +2 in the >>4 address field
+                            if constexpr (PAIR)
+                                mma_bf16_pair(d_base, adesc + 2 * k, bdesc + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
+                            else
+                                mma_bf16(d_base, adesc + 2 * k, bdesc + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
+                        }
+                        if constexpr (PAIR)
+                            mma_commit_pair(&sm.empty[stage], 0x3);
+                        else
+                            mma_commit(&sm.empty[stage]);
                         if (++stage == p.stages) {
                             stage = 0;
                             phase ^= 1u;
                         }
                     }
-                    if (!ok) break;
-                    tc_fence_after();
+                } else {
+                    // packed groups: one ring stage per group for this K-step, MMAs
+                    // interleaved over the groups' independent accumulators; all
+                    // descriptors computed before the first MMA
+                    for (int ks = 0; ks < p.ksteps && ok; ++ks) {
+                        uint64_t ad[kTcMaxGroupsPerTile], bd[kTcMaxGroupsPerTile];
+                        int sj[kTcMaxGroupsPerTile];
 #pragma unroll
-                    for (int k = 0; k < kTcBlockK / 16; ++k) {
-                        // +32 bytes along K inside the swizzle row = +2 in the >>4 address field
-                        for (int j = 0, sj = stage0; j < p.gpc; ++j, sj = sj + 1 == p.stages ? 0 : sj + 1) {
-                            const uint32_t d = d_base + static_cast<uint32_t>(j * p.mma_n);
-                            const uint64_t adesc = sdesc_sw128(smem_addr(sm.a + sj * kABytes)) + 2 * k;
-                            const uint64_t bdesc = sdesc_sw128(smem_addr(sm.b + sj * b_bytes)) + 2 * k;
-                            if constexpr (PAIR)
-                                mma_bf16_pair(d, adesc, bdesc, idesc, (ks | k) != 0 ? 1u : 0u);
-                            else
-                                mma_bf16(d, adesc, bdesc, idesc, (ks | k) != 0 ? 1u : 0u);
+                        for (int j = 0; j < kTcMaxGroupsPerTile; ++j) {
+                            if (j < p.gpc && ok) {
+                                sj[j] = stage;
+                                if (!mbar_wait(&sm.full[stage], phase, abort)) {
+                                    record_status(p.status, kStatusTimeoutMma, abort);
+                                    ok = false;
+                                }
+                                ad[j] = sdesc_sw128(smem_addr(sm.a + stage * kABytes));
+                                bd[j] = sdesc_sw128(smem_addr(sm.b + stage * b_bytes));
+                                if (++stage == p.stages) {
+                                    stage = 0;
+                                    phase ^= 1u;
+                                }
+                            }
                         }
-                    }
-                    for (int j = 0, sj = stage0; j < p.gpc; ++j, sj = sj + 1 == p.stages ? 0 : sj + 1) {
-                        if constexpr (PAIR)
-                            mma_commit_pair(&sm.empty[sj], 0x3);
-                        else
-                            mma_commit(&sm.empty[sj]);
+                        if (!ok) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int k = 0; k < kTcBlockK / 16; ++k) {
+#pragma unroll
+                            for (int j = 0; j < kTcMaxGroupsPerTile; ++j) {
+                                if (j < p.gpc) {
+                                    const uint32_t d = d_base + static_cast<uint32_t>(j * p.mma_n);
+                                    if constexpr (PAIR)
+                                        mma_bf16_pair(d, ad[j] + 2 * k, bd[j] + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
+                                    else
+                                        mma_bf16(d, ad[j] + 2 * k, bd[j] + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < kTcMaxGroupsPerTile; ++j) {
+                            if (j < p.gpc) {
+                                if constexpr (PAIR)
+                                    mma_commit_pair(&sm.empty[sj[j]], 0x3);
+                                else
+                                    mma_commit(&sm.empty[sj[j]]);
+                            }
+                        }
                     }
                 }
                 if (ok) {
