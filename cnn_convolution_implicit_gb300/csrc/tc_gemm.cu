@@ -210,12 +210,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int m = PAIR ? 2 * mu + static_cast<int>(rank) : mu;
                 PixTile t = pix_tile(p, m);
                 if (!t.exists) t = pix_tile(p, p.num_m_tiles - 1);  // a valid tile whose result is never stored
-                // K-steps tap-major, group-minor: the MMA issuer interleaves the groups'
-                // independent accumulators instead of running one dependent chain per group
-                for (int ks = 0; ks < p.ksteps && ok; ++ks) {
-                    for (int j = 0; j < p.gpc; ++j) {
-                        int grp, brow;
-                        sub_gemm(p, nt, j, grp, brow);
+                for (int j = 0; j < p.gpc && ok; ++j) {
+                    int grp, brow;
+                    sub_gemm(p, nt, j, grp, brow);
+                    for (int ks = 0; ks < p.ksteps; ++ks) {
                         if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
                             record_status(p.status, kStatusTimeoutProducer, abort);
                             ok = false;
@@ -274,7 +272,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_base = tmem_base + static_cast<uint32_t>(buf * p.n_tile);
-                if (p.gpc == 1) {
+                for (int j = 0; j < p.gpc && ok; ++j) {
+                    const uint32_t d = d_base + static_cast<uint32_t>(j * p.mma_n);
                     for (int ks = 0; ks < p.ksteps; ++ks) {
                         if (!mbar_wait(&sm.full[stage], phase, abort)) {
                             record_status(p.status, kStatusTimeoutMma, abort);
@@ -288,9 +287,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         for (int k = 0; k < kTcBlockK / 16; ++k) {
                             // +32 bytes along K inside the swizzle row = +2 in the >>4 address field
                             if constexpr (PAIR)
-                                mma_bf16_pair(d_base, adesc + 2 * k, bdesc + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
+                                mma_bf16_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
                             else
-                                mma_bf16(d_base, adesc + 2 * k, bdesc + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
+                                mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
                         }
                         if constexpr (PAIR)
                             mma_commit_pair(&sm.empty[stage], 0x3);
@@ -299,54 +298,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         if (++stage == p.stages) {
                             stage = 0;
                             phase ^= 1u;
-                        }
-                    }
-                } else {
-                    // packed groups: one ring stage per group for this K-step, MMAs
-                    // interleaved over the groups' independent accumulators; all
-                    // descriptors computed before the first MMA
-                    for (int ks = 0; ks < p.ksteps && ok; ++ks) {
-                        uint64_t ad[kTcMaxGroupsPerTile], bd[kTcMaxGroupsPerTile];
-                        int sj[kTcMaxGroupsPerTile];
-#pragma unroll
-                        for (int j = 0; j < kTcMaxGroupsPerTile; ++j) {
-                            if (j < p.gpc && ok) {
-                                sj[j] = stage;
-                                if (!mbar_wait(&sm.full[stage], phase, abort)) {
-                                    record_status(p.status, kStatusTimeoutMma, abort);
-                                    ok = false;
-                                }
-                                ad[j] = sdesc_sw128(smem_addr(sm.a + stage * kABytes));
-                                bd[j] = sdesc_sw128(smem_addr(sm.b + stage * b_bytes));
-                                if (++stage == p.stages) {
-                                    stage = 0;
-                                    phase ^= 1u;
-                                }
-                            }
-                        }
-                        if (!ok) break;
-                        tc_fence_after();
-#pragma unroll
-                        for (int k = 0; k < kTcBlockK / 16; ++k) {
-#pragma unroll
-                            for (int j = 0; j < kTcMaxGroupsPerTile; ++j) {
-                                if (j < p.gpc) {
-                                    const uint32_t d = d_base + static_cast<uint32_t>(j * p.mma_n);
-                                    if constexpr (PAIR)
-                                        mma_bf16_pair(d, ad[j] + 2 * k, bd[j] + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
-                                    else
-                                        mma_bf16(d, ad[j] + 2 * k, bd[j] + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
-                                }
-                            }
-                        }
-#pragma unroll
-                        for (int j = 0; j < kTcMaxGroupsPerTile; ++j) {
-                            if (j < p.gpc) {
-                                if constexpr (PAIR)
-                                    mma_commit_pair(&sm.empty[sj[j]], 0x3);
-                                else
-                                    mma_commit(&sm.empty[sj[j]]);
-                            }
                         }
                     }
                 }
