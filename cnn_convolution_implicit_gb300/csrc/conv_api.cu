@@ -191,9 +191,6 @@ bool configure_smallk(conv_plan* pl) {
     if (g.C_out % 32 != 0 || g.C_out > 256) return false;
     const long long row_bytes = static_cast<long long>(g.W) * g.C_in * 2;
     if (row_bytes % 16 != 0) return false;
-    const int rows = 256 / g.C_out < 4 ? 256 / g.C_out : 4;  // row segments per stage; 2*rows*C_out TMEM columns
-    const long long raw = (static_cast<long long>(rows) * g.Kh * row_bytes + 1023) / 1024 * 1024;
-    if (raw > 48 * 1024) return false;
     const long long segs = (g.W_out + 127) / 128;
     const long long segments = static_cast<long long>(g.N) * g.H_out * segs;
     if (segments > 0x7fffffffLL) return false;
@@ -202,19 +199,29 @@ bool configure_smallk(conv_plan* pl) {
     s.kmma = (ktot + 15) / 16;
     s.a_row_bytes = s.kmma * 16 <= 32 ? 64 : 128;
     s.segs = static_cast<int>(segs);
-    s.rows_per_tile = rows;
     s.num_segments = static_cast<int>(segments);
-    s.num_tiles = static_cast<int>((segments + rows - 1) / rows);
     s.row_bytes = static_cast<int>(row_bytes);
-    s.raw_bytes = static_cast<int>(raw);
     const int b_bytes = (g.C_out * s.a_row_bytes + 1023) / 1024 * 1024;
-    const int fixed = 1024 + b_bytes + 4 * 2 * 32 * 64 + 1024 + 3 * 64 * 4 + 16 + g.C_out * 4;
-    const int stage_bytes = rows * 128 * s.a_row_bytes + s.raw_bytes;
-    int stages = (pl->smem_optin - fixed) / stage_bytes;
+    const int fixed = 1024 + b_bytes + 8 * 2 * 32 * 64 + 1024 + 3 * 64 * 4 + 16 + g.C_out * 4;
+    // row segments per stage (2 * rows * C_out TMEM columns): as many as allow a two-stage ring
+    int rows = 256 / g.C_out < 4 ? 256 / g.C_out : 4;
+    int stages = 0;
+    for (; rows >= 1; --rows) {
+        const long long raw = (static_cast<long long>(rows) * g.Kh * row_bytes + 1023) / 1024 * 1024;
+        if (raw > 48 * 1024) continue;
+        const long long stage_bytes = static_cast<long long>(rows) * 128 * s.a_row_bytes + raw;
+        stages = static_cast<int>((pl->smem_optin - fixed) / stage_bytes);
+        if (stages >= 2) {
+            s.raw_bytes = static_cast<int>(raw);
+            break;
+        }
+    }
+    if (rows < 1 || stages < 2) return false;
     if (stages > 8) stages = 8;
-    if (stages < 2) return false;
+    s.rows_per_tile = rows;
+    s.num_tiles = static_cast<int>((segments + rows - 1) / rows);
     s.stages = stages;
-    s.smem_bytes = fixed + stages * stage_bytes;
+    s.smem_bytes = fixed + stages * (rows * 128 * s.a_row_bytes + s.raw_bytes);
     s.tmem_cols = pow2_at_least(2 * rows * g.C_out);
     s.relu = (pl->flags & CONV_FLAG_RELU) ? 1 : 0;
     s.status = pl->status;

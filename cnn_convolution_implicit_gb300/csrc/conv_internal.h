@@ -92,7 +92,8 @@ cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, c
 int tc_gemm_pair_max_clusters(const TcGemmParams& p);
 
 // ---------------------------------------------------------------- tcgen05 small-K (stem)
-constexpr int kSkThreads = 448;   // producer, MMA, 4 epilogue, 8 transform warps
+constexpr int kSkTransformThreads = 192;  // 6 transform warps
+constexpr int kSkThreads = 320 + kSkTransformThreads;  // producer, MMA, 2 x 4 epilogue, transform warps
 
 struct SmallKParams {
     ConvGeom g;

@@ -20,11 +20,12 @@
 // shared by several rows.  The whole weight matrix (C_out x K) stays in shared
 // memory.
 //
-// Warp roles (448 threads, persistent):
+// Warp roles (512 threads, persistent):
 //   warp 0       bulk-copy producer (one lane)
 //   warp 1       TMEM allocator; one lane issues tcgen05.mma
-//   warps 2..5   epilogue (tcgen05.ld -> +bias -> ReLU -> BF16 -> smem -> TMA store)
-//   warps 6..13  transform: raw rows -> swizzled A tiles
+//   warps 2..9   epilogue, two groups of four (one per TMEM accumulator buffer):
+//                tcgen05.ld -> +bias -> ReLU -> BF16 -> smem -> TMA store
+//   warps 10..15 transform: raw rows -> swizzled A tiles
 // The 3-channel 3x3 case is compiled with its K decomposition as constants;
 // other shapes read it from a per-CTA table.
 #include "conv_internal.h"
@@ -65,7 +66,7 @@ __device__ __forceinline__ SkSmem carve(uint8_t* raw, const SmallKParams& p) {
     s.a = s.b + b_bytes;
     s.raw = s.a + p.stages * p.rows_per_tile * a_tile_bytes(p);
     s.out = s.raw + p.stages * p.raw_bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s.out + 4 * 2 * kSkOutBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s.out + 8 * 2 * kSkOutBytes);
     s.raw_full = bars;
     s.a_full = bars + p.stages;
     s.empty = bars + 2 * p.stages;
@@ -194,7 +195,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&sm.raw_full[s], 1);
-            mbar_init(&sm.a_full[s], 256);
+            mbar_init(&sm.a_full[s], kSkTransformThreads);
             mbar_init(&sm.empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -296,14 +297,20 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             mma_commit(sm.drain);
             if (!mbar_wait(sm.drain, 0, nullptr)) record_status(p.status, kStatusTimeoutDrain, abort);
         }
-    } else if (warp < 6) {
+    } else if (warp < 10) {
         // ------------------------------------------------------------ epilogue
+        // Two groups of four warps, one per TMEM accumulator buffer (so two
+        // stages drain at once); the next chunk's TMEM load is in flight while
+        // the current one is converted and staged.
         const int quarter = warp & 3;
+        const int group = (warp - 2) >> 2;
         uint8_t* stg = sm.out + (warp - 2) * 2 * kSkOutBytes;
+        const int chunks = n_tile / 32;
         int sbuf = 0;
         int local = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
             const int buf = local & 1;
+            if (buf != group) continue;
             const uint32_t use = static_cast<uint32_t>(local >> 1) & 1u;
             const bool ready = __all_sync(0xffffffffu, mbar_wait(&sm.tfull[buf], use, abort));
             if (!ready) {
@@ -312,28 +319,48 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             }
             tc_fence_after();
             const int rows = min(R, p.num_segments - tile * R);
-            for (int j = 0; j < rows; ++j) {
+            const int items = rows * chunks;  // (segment, 32-column chunk) pairs
+            const uint32_t t_q = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                 static_cast<uint32_t>(buf * R * n_tile);
+            auto t_addr = [&](int it) {
+                const int j = it / chunks;
+                return t_q + static_cast<uint32_t>(j * n_tile + (it - j * chunks) * 32);
+            };
+            auto process = [&](const uint32_t(&v)[32], int it) {
+                const int j = it / chunks;
+                const int c = (it - j * chunks) * 32;
                 const SkSeg t = segment(p, tile * R + j);
                 const int wo_row0 = t.wo0 + quarter * 32;  // first output column of this warp's rows
                 const bool rows_exist = quarter * 32 < t.npix;
-                const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                       static_cast<uint32_t>((buf * R + j) * n_tile);
-                for (int c = 0; c < n_tile; c += 32) {
-                    uint32_t v[32];
+                if (lane == 0) bulk_wait_read_le1();
+                __syncwarp();
+                uint8_t* dst = stg + sbuf * kSkOutBytes;
+                stage_row32<true>(v, p.bias ? sm.bias + c : nullptr, p.relu, dst, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && rows_exist) {  // columns past W_out fall outside the map: not written
+                    tma_store_3d(&y_map, dst, c, wo_row0, t.n * p.g.H_out + t.ho);
+                    bulk_commit();
+                }
+                sbuf ^= 1;
+            };
+            uint32_t va[32], vb[32];
+            __syncwarp();
+            tmem_ld32(t_addr(0), va);
+            for (int it = 0; it < items; it += 2) {
+                tmem_ld_wait(va);
+                if (it + 1 < items) {
                     __syncwarp();
-                    tmem_ld32(t_row + static_cast<uint32_t>(c), v);
-                    tmem_ld_wait(v);
-                    if (lane == 0) bulk_wait_read_le1();
-                    __syncwarp();
-                    uint8_t* dst = stg + sbuf * kSkOutBytes;
-                    stage_row32<true>(v, p.bias ? sm.bias + c : nullptr, p.relu, dst, lane);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0 && rows_exist) {  // columns past W_out fall outside the map: not written
-                        tma_store_3d(&y_map, dst, c, wo_row0, t.n * p.g.H_out + t.ho);
-                        bulk_commit();
+                    tmem_ld32(t_addr(it + 1), vb);
+                }
+                process(va, it);
+                if (it + 1 < items) {
+                    tmem_ld_wait(vb);
+                    if (it + 2 < items) {
+                        __syncwarp();
+                        tmem_ld32(t_addr(it + 2), va);
                     }
-                    sbuf ^= 1;
+                    process(vb, it + 1);
                 }
             }
             tc_fence_before();
@@ -342,7 +369,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         if (lane == 0) bulk_wait_all();
     } else {
         // ------------------------------------------------------------ transform (im2col in smem)
-        const int tid = threadIdx.x - 192;  // 0..255
+        const int tid = threadIdx.x - 320;  // 0..kSkTransformThreads-1
         const uint16_t* raw16 = reinterpret_cast<const uint16_t*>(sm.raw);
         const int raw_elems = p.raw_bytes >> 1;
         const int row_elems = p.row_bytes >> 1;
@@ -354,7 +381,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 record_status(p.status, kStatusTimeoutTransform, abort);
                 break;
             }
-            for (int idx = tid; idx < R * 128; idx += 256) {
+            for (int idx = tid; idx < R * 128; idx += kSkTransformThreads) {
                 const int j = idx >> 7;   // row segment within the stage
                 const int r = idx & 127;  // A row = pixel within the segment
                 const int u = tile * R + j;
