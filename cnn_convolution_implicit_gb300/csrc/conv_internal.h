@@ -9,6 +9,21 @@
 
 namespace convgb {
 
+// Raise a kernel's dynamic shared-memory limit only when a launch needs more
+// than what was set before on this device (`limits` is the caller's per-kernel
+// table).  The limit is a per-function attribute, so a plan's later launches
+// cost no extra runtime call.  Concurrent first calls may both set it: harmless.
+inline cudaError_t ensure_smem_limit(const void* func, int bytes, int (&limits)[64]) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    }
+    if (limits[dev] >= bytes) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) limits[dev] = bytes;
+    return e;
+}
+
 // Geometry of one convolution (NHWC activations, [C_out][Kh][Kw][C_in/G] weights).
 struct ConvGeom {
     int N, C_in, H, W, C_out, Kh, Kw, S, P, D, G;

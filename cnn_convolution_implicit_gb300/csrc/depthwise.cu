@@ -324,8 +324,8 @@ int depthwise_config(const ConvGeom& g, int smem_per_sm, int num_sms, DepthwiseP
 
 template <int K, int TW>
 static cudaError_t launch_dw(const CUtensorMap& x_map, const DepthwiseParams& p, cudaStream_t stream) {
-    cudaError_t e =
-        cudaFuncSetAttribute(depthwise_kernel<K, TW>, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
+    static int limits[64] = {};
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(depthwise_kernel<K, TW>), p.smem_bytes, limits);
     if (e != cudaSuccess) return e;
     depthwise_kernel<K, TW><<<p.grid, kDwThreads, p.smem_bytes, stream>>>(x_map, p);
     return cudaGetLastError();

@@ -416,11 +416,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 }
 
+// per-device dynamic shared-memory limit already set on the pair kernel
+static int g_pair_smem_limits[64] = {};
+
 cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, const CUtensorMap& y_map,
                            const TcGemmParams& p, int grid, cudaStream_t stream) {
     if (p.pair) {
         cudaError_t e =
-            cudaFuncSetAttribute(tc_conv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
+            ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<true>), p.smem_bytes, g_pair_smem_limits);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid, 1, 1);
@@ -438,15 +441,15 @@ cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, c
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
-    cudaError_t e =
-        cudaFuncSetAttribute(tc_conv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
+    static int limits[64] = {};
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<false>), p.smem_bytes, limits);
     if (e != cudaSuccess) return e;
     tc_conv_kernel<false><<<grid, kTcThreads, p.smem_bytes, stream>>>(a_map, b_map, y_map, p);
     return cudaGetLastError();
 }
 
 int tc_gemm_pair_max_clusters(const TcGemmParams& p) {
-    if (cudaFuncSetAttribute(tc_conv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes) !=
+    if (ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<true>), p.smem_bytes, g_pair_smem_limits) !=
         cudaSuccess) {
         cudaGetLastError();
         return 0;

@@ -429,8 +429,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 
 template <int CIN, int KH, int KW>
 static cudaError_t launch_sk(const CUtensorMap& y_map, const SmallKParams& p, int grid, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(tc_smallk_kernel<CIN, KH, KW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         p.smem_bytes);
+    static int limits[64] = {};
+    cudaError_t e =
+        ensure_smem_limit(reinterpret_cast<const void*>(tc_smallk_kernel<CIN, KH, KW>), p.smem_bytes, limits);
     if (e != cudaSuccess) return e;
     tc_smallk_kernel<CIN, KH, KW><<<grid, kSkThreads, p.smem_bytes, stream>>>(y_map, p);
     return cudaGetLastError();
