@@ -15,7 +15,8 @@ follows, is stated at the top of ``conv_oracle.c``:
 * dilation, effective kernel, output size, groups: "Convolution variants and
   their matrix operations" (lpnh.cn/news/2674933), sections 2.2, 2.3, 4.2,
   4.3, 6.2;
-* bias after the sum, then ReLU: lesson 9, section 31.
+* bias after the sum, then ReLU: lesson 9, section 31 (with its per-channel
+  scale and shift, a folded batch norm: y = act(scale * sum + shift)).
 
 Every function here is pinned by ``tests/test_oracle.py`` against values the
 pages print, closed forms, and two independent restatements.
@@ -64,12 +65,12 @@ def _load():
         P = ctypes.POINTER
         lib.oracle_out_size.argtypes = [ctypes.c_int] * 5
         lib.oracle_out_size.restype = ctypes.c_int
-        lib.oracle_conv2d_f64.argtypes = [P(_Desc), ctypes.c_void_p, ctypes.c_void_p,
+        lib.oracle_conv2d_f64.argtypes = [P(_Desc), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         lib.oracle_conv2d_f64.restype = ctypes.c_int
         lib.oracle_conv2d_points_f64.argtypes = [P(_Desc), ctypes.c_void_p, ctypes.c_void_p,
-                                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
-                                                 ctypes.c_void_p, ctypes.c_int]
+                                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                 ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]
         lib.oracle_conv2d_points_f64.restype = ctypes.c_int
         lib.oracle_conv2d_macs_at.argtypes = [P(_Desc), ctypes.c_void_p, ctypes.c_void_p,
                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
@@ -126,8 +127,11 @@ def _f64(a):
 
 
 def conv2d(x, w, bias=None, stride=1, padding=0, dilation=1, groups=1, relu=False,
-           x_layout="NCHW", w_layout="OIHW", y_layout="NCHW", nthreads=0):
+           x_layout="NCHW", w_layout="OIHW", y_layout="NCHW", nthreads=0, scale=None):
     """Full FP64 output of the convolution (see module docstring).
+
+    ``scale`` ([C_out] or None) multiplies each channel's sum before the bias
+    is added: y = act(scale[co] * sum + bias[co]) (a folded batch norm).
 
     ``x`` is given in ``x_layout`` ("NCHW" or "NHWC"), ``w`` in ``w_layout``
     ("OIHW" = [C_out][C_in/G][Kh][Kw], or "OHWI" = [C_out][Kh][Kw][C_in/G]),
@@ -136,6 +140,7 @@ def conv2d(x, w, bias=None, stride=1, padding=0, dilation=1, groups=1, relu=Fals
     lib = _load()
     x, w = _f64(x), _f64(w)
     b = None if bias is None else _f64(bias)
+    sc = None if scale is None else _f64(scale)
     xl = _ACT_LAYOUTS[x_layout]
     N, C_in, H, W = _logical_shape(x, xl, "nchw")
     C_out, _, Kh, Kw = _logical_shape(w, _W_LAYOUTS[w_layout], "oihw")
@@ -147,6 +152,7 @@ def conv2d(x, w, bias=None, stride=1, padding=0, dilation=1, groups=1, relu=Fals
     y = np.empty(shape, dtype=np.float64)
     d = _desc(x, w, x_layout, w_layout, y_layout, stride, padding, dilation, groups, relu, y)
     rc = lib.oracle_conv2d_f64(ctypes.byref(d), x.ctypes.data, w.ctypes.data,
+                               None if sc is None else sc.ctypes.data,
                                None if b is None else b.ctypes.data, y.ctypes.data, int(nthreads))
     if rc != 0:
         raise ValueError("oracle rejected the convolution descriptor")
@@ -154,15 +160,17 @@ def conv2d(x, w, bias=None, stride=1, padding=0, dilation=1, groups=1, relu=Fals
 
 
 def conv2d_points(x, w, bias, pts, stride=1, padding=0, dilation=1, groups=1, relu=False,
-                  x_layout="NCHW", w_layout="OIHW", nthreads=0):
+                  x_layout="NCHW", w_layout="OIHW", nthreads=0, scale=None):
     """FP64 values at selected outputs; ``pts`` is an int array [npts, 4] of (n, co, ho, wo)."""
     lib = _load()
     x, w = _f64(x), _f64(w)
     b = None if bias is None else _f64(bias)
+    sc = None if scale is None else _f64(scale)
     pts = np.ascontiguousarray(pts, dtype=np.int64).reshape(-1, 4)
     out = np.empty(pts.shape[0], dtype=np.float64)
     d = _desc(x, w, x_layout, w_layout, "NCHW", stride, padding, dilation, groups, relu)
     rc = lib.oracle_conv2d_points_f64(ctypes.byref(d), x.ctypes.data, w.ctypes.data,
+                                      None if sc is None else sc.ctypes.data,
                                       None if b is None else b.ctypes.data, pts.ctypes.data,
                                       pts.shape[0], out.ctypes.data, int(nthreads))
     if rc != 0:

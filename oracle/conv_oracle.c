@@ -15,6 +15,10 @@
  *   with g = co / (C_out/G); taps whose input coordinate falls outside
  *   [0,H) x [0,W) contribute nothing; then ReLU if requested.
  *
+ *   With a per-channel scale (folded batch normalisation) the sum is first
+ *   multiplied by scale[co], then bias[co] is added, then the activation:
+ *   y = act(scale[co] * sum + bias[co]).
+ *
  * Sources:
  *   - the dot-product definition and the index map h_i = h_o*S_h + k_h - P_h:
  *     "GPU lesson 9: how a GPU executes neural-network convolution"
@@ -29,7 +33,9 @@
  *   - groups as G independent convolutions on contiguous channel blocks:
  *     variants page, sections 2.2 and 4.3; depthwise is G = C_in (lesson 9,
  *     section 23);
- *   - bias added after the sum, then the activation: lesson 9, section 31.
+ *   - bias added after the sum, then the activation: lesson 9, section 31;
+ *     the same section's per-channel scale and shift (a folded batch norm)
+ *     multiply the sum before the shift is added.
  *
  * Loop order follows the seven-loop nest of lesson 9, section 34
  * (n, co, ho, wo outer; ci, kh, kw inner), parallelised over (n, co) with
@@ -64,7 +70,7 @@ int oracle_out_size(int in, int k, int s, int p, int d)
 /* One output element, summed in the definition's order.  When macs is
  * non-NULL it receives the number of multiply terms actually taken. */
 static double one_output(const oracle_conv_desc *c, const double *x,
-                         const double *w, const double *bias,
+                         const double *w, const double *scale, const double *bias,
                          int n, int co, int ho, int wo, long *macs)
 {
     const int cin_g = c->C_in / c->G;
@@ -87,6 +93,7 @@ static double one_output(const oracle_conv_desc *c, const double *x,
             }
         }
     }
+    if (scale) acc *= scale[co];
     if (bias) acc += bias[co];
     if (c->relu && acc < 0.0) acc = 0.0;
     if (macs) *macs = count;
@@ -101,9 +108,9 @@ static int check_desc(const oracle_conv_desc *c)
     return 0;
 }
 
-/* Full output.  Returns 0, or -1 on a bad descriptor. */
+/* Full output; scale may be NULL (no scaling).  Returns 0, or -1 on a bad descriptor. */
 int oracle_conv2d_f64(const oracle_conv_desc *c, const double *x, const double *w,
-                      const double *bias, double *y, int nthreads)
+                      const double *scale, const double *bias, double *y, int nthreads)
 {
     if (check_desc(c)) return -1;
     const int Ho = oracle_out_size(c->H, c->Kh, c->S, c->P, c->D);
@@ -122,7 +129,7 @@ int oracle_conv2d_f64(const oracle_conv_desc *c, const double *x, const double *
         for (int ho = 0; ho < Ho; ++ho)
             for (int wo = 0; wo < Wo; ++wo)
                 y[n * c->ys_n + co * c->ys_c + ho * c->ys_h + wo * c->ys_w] =
-                    one_output(c, x, w, bias, n, co, ho, wo, 0);
+                    one_output(c, x, w, scale, bias, n, co, ho, wo, 0);
     }
     return 0;
 }
@@ -130,8 +137,8 @@ int oracle_conv2d_f64(const oracle_conv_desc *c, const double *x, const double *
 /* Selected outputs: pts holds npts quadruples (n, co, ho, wo); out[i] gets
  * the value at pts[i].  Returns 0, or -1 on a bad descriptor or point. */
 int oracle_conv2d_points_f64(const oracle_conv_desc *c, const double *x, const double *w,
-                             const double *bias, const int64_t *pts, int64_t npts,
-                             double *out, int nthreads)
+                             const double *scale, const double *bias, const int64_t *pts,
+                             int64_t npts, double *out, int nthreads)
 {
     if (check_desc(c)) return -1;
     const int Ho = oracle_out_size(c->H, c->Kh, c->S, c->P, c->D);
@@ -149,7 +156,7 @@ int oracle_conv2d_points_f64(const oracle_conv_desc *c, const double *x, const d
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < npts; ++i) {
         const int64_t *q = pts + 4 * i;
-        out[i] = one_output(c, x, w, bias, (int)q[0], (int)q[1], (int)q[2], (int)q[3], 0);
+        out[i] = one_output(c, x, w, scale, bias, (int)q[0], (int)q[1], (int)q[2], (int)q[3], 0);
     }
     return 0;
 }
@@ -160,7 +167,7 @@ long oracle_conv2d_macs_at(const oracle_conv_desc *c, const double *x, const dou
 {
     if (check_desc(c)) return -1;
     long macs = 0;
-    (void)one_output(c, x, w, 0, n, co, ho, wo, &macs);
+    (void)one_output(c, x, w, 0, 0, n, co, ho, wo, &macs);
     return macs;
 }
 

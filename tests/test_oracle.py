@@ -315,3 +315,50 @@ def test_rejects_bad_descriptors():
         oracle.conv2d(np.zeros((1, 3, 4, 4)), np.zeros((2, 2, 3, 3)), groups=1)
     with pytest.raises(ValueError):
         oracle.conv2d(np.zeros((1, 2, 2, 2)), np.zeros((2, 2, 5, 5)))  # empty output
+
+
+# ----------------------------------------------------------------- folded batch norm (scale + shift)
+def test_scale_one_is_bit_identical():
+    rng = np.random.default_rng(20)
+    x = rng.standard_normal((2, 4, 7, 6))
+    w = rng.standard_normal((6, 2, 3, 3))
+    b = rng.standard_normal(6)
+    y = oracle.conv2d(x, w, b, 1, 1, 1, 2, True)
+    assert np.array_equal(y, oracle.conv2d(x, w, b, 1, 1, 1, 2, True, scale=np.ones(6)))
+
+
+def test_scale_folds_into_weights():
+    """scale[co] * (w * x) == (scale[co] * w) * x: folding the scale into the weights."""
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((2, 6, 9, 8))
+    w = rng.standard_normal((9, 2, 3, 3))
+    b = rng.standard_normal(9)
+    sc = rng.standard_normal(9)
+    y = oracle.conv2d(x, w, b, 2, 1, 2, 3, False, scale=sc)
+    y2 = oracle.conv2d(x, w * sc[:, None, None, None], b, 2, 1, 2, 3, False)
+    assert np.allclose(y, y2, rtol=1e-12, atol=1e-12)
+
+
+def test_folded_batch_norm_matches_batch_norm():
+    """Inference batch norm after the conv (torch's float64 batch_norm) equals the
+    conv with scale = gamma / sqrt(var + eps), shift = beta - mean * scale."""
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal((2, 3, 8, 8))
+    w = rng.standard_normal((5, 3, 3, 3))
+    mean, var = rng.standard_normal(5), rng.uniform(0.5, 2.0, 5)
+    gamma, beta, eps = rng.standard_normal(5), rng.standard_normal(5), 1e-5
+    conv = F.conv2d(torch.from_numpy(x), torch.from_numpy(w), padding=1)
+    ref = torch.relu(F.batch_norm(conv, torch.from_numpy(mean), torch.from_numpy(var),
+                                  torch.from_numpy(gamma), torch.from_numpy(beta), False, 0.0, eps)).numpy()
+    sc = gamma / np.sqrt(var + eps)
+    y = oracle.conv2d(x, w, beta - mean * sc, 1, 1, 1, 1, True, scale=sc)
+    assert np.allclose(y, ref, rtol=1e-11, atol=1e-11)
+
+
+def test_scale_all_ones_closed_form_and_points():
+    w = np.arange(1, 10, dtype=float).reshape(1, 1, 3, 3)
+    y = oracle.conv2d(np.ones((1, 1, 5, 5)), w, np.array([0.5]), padding=1, scale=np.array([-2.0]))[0, 0]
+    assert y[2, 2] == -2.0 * w.sum() + 0.5
+    pts = np.array([[0, 0, 2, 2], [0, 0, 0, 0]])
+    v = oracle.conv2d_points(np.ones((1, 1, 5, 5)), w, np.array([0.5]), pts, 1, 1, scale=np.array([-2.0]))
+    assert v[0] == y[2, 2] and v[1] == y[0, 0]
