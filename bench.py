@@ -234,11 +234,14 @@ def gpu_layer(name):
     return s, plan, (x, w, b), (xd, wd, bd, y)
 
 
-def measure_layer(name, steps, warmup, flush, peaks):
+def measure_layer(name, steps, warmup, flush, peaks, affine=False):
     s, plan, host, (xd, wd, bd, y) = gpu_layer(name)
+    scale = None
+    if affine:  # folded batch norm: per-channel scale before the shift
+        scale = torch.from_numpy(np.random.default_rng(5).uniform(0.5, 1.5, s.C_out).astype(np.float32)).cuda()
 
     def step():
-        plan.forward(xd, wd, bd, y)
+        plan.forward(xd, wd, bd, y, scale=scale)
 
     ms = time_steps(step, steps, warmup, flush)
     t = float(np.mean(ms)) * 1e-3
@@ -246,7 +249,8 @@ def measure_layer(name, steps, warmup, flush, peaks):
     gbs = s.algorithmic_bytes / t / 1e9
     bound = "hbm" if s.flops / s.algorithmic_bytes < peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9) \
         or s.dtype == "f32" else "tensor"
-    res = {"workload": name, "kernel": plan.path, "ms": t * 1e3, "tflops": tflops, "gbs": gbs,
+    res = {"workload": name + ("+affine" if affine else ""), "kernel": plan.path, "ms": t * 1e3,
+           "tflops": tflops, "gbs": gbs,
            "bound": bound, "flops": s.flops, "bytes": s.algorithmic_bytes, "launches": steps,
            "source_hash": kernel_source_hash(name), "launch": plan.launch}
     if bound == "tensor":
@@ -414,6 +418,8 @@ def main():
     for name in ("dw", "stem", "pw", "dilated"):
         r, _ = measure_layer(name, max(10, args.steps // 2), args.warmup, flush, peaks)
         others[name] = r
+    r, _ = measure_layer("body", max(10, args.steps // 2), args.warmup, flush, peaks, affine=True)
+    others["body+affine"] = r
 
     traffic = load_traffic()
     tr = traffic.get("body")

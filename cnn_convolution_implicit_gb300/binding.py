@@ -23,7 +23,7 @@ PATHS = {0: "direct", 1: "depthwise", 2: "gemm_1x1", 3: "implicit_gemm", 4: "sma
 # Every symbol include/conv.h declares.
 EXPORTS = ("conv_plan_create", "conv_plan_output_shape", "conv_plan_info", "conv_forward",
            "conv_plan_destroy", "conv_status_string", "conv_device_status", "conv_plan_num_sms",
-           "conv_plan_launch_info")
+           "conv_plan_launch_info", "conv_forward_affine")
 
 _lock = threading.Lock()
 _lib = None
@@ -61,6 +61,8 @@ def lib():
             L.conv_plan_info.restype = c_int
             L.conv_forward.argtypes = [vp, vp, vp, vp, vp, vp]
             L.conv_forward.restype = c_int
+            L.conv_forward_affine.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+            L.conv_forward_affine.restype = c_int
             L.conv_plan_destroy.argtypes = [vp]
             L.conv_plan_destroy.restype = c_int
             L.conv_status_string.argtypes = [c_int]
@@ -145,8 +147,11 @@ class ConvPlan:
         N, _, _, _, C_out = self.shape[:5]
         return torch.empty((N, self.H_out, self.W_out, C_out), dtype=self.out_dtype(), device=device)
 
-    def forward(self, x, w, bias=None, y=None, stream=None):
-        """Launch on ``stream`` (default: torch's current stream); returns y."""
+    def forward(self, x, w, bias=None, y=None, stream=None, scale=None):
+        """Launch on ``stream`` (default: torch's current stream); returns y.
+
+        ``scale`` (CUDA float32 [C_out], optional) multiplies each channel's sum
+        before the bias: y = act(scale * sum + bias), a folded batch norm."""
         import torch
         N, C_in, H, W, C_out, Kh, Kw, S, P, D, G = self.shape
         dt = torch.bfloat16 if self.dtype == "bf16" else torch.float32
@@ -169,11 +174,19 @@ class ConvPlan:
             raise ValueError("y has the wrong shape, dtype or layout")
         if stream is None:
             stream = torch.cuda.current_stream(x.device)
-        st = lib().conv_forward(self._plan, x.data_ptr(), w.data_ptr(),
-                                bias.data_ptr() if (self.bias and bias is not None) else None,
-                                y.data_ptr(), stream.cuda_stream)
-        if st != 0:
-            raise ConvError(st, "conv_forward")
+        bptr = bias.data_ptr() if (self.bias and bias is not None) else None
+        if scale is None:
+            st = lib().conv_forward(self._plan, x.data_ptr(), w.data_ptr(), bptr, y.data_ptr(), stream.cuda_stream)
+            if st != 0:
+                raise ConvError(st, "conv_forward")
+        else:
+            if scale.dtype != torch.float32 or tuple(scale.shape) != (C_out,) or not scale.is_contiguous() or \
+                    not scale.is_cuda:
+                raise ValueError("scale must be a contiguous CUDA float32 tensor of shape (%d,)" % C_out)
+            st = lib().conv_forward_affine(self._plan, x.data_ptr(), w.data_ptr(), scale.data_ptr(), bptr,
+                                           y.data_ptr(), stream.cuda_stream)
+            if st != 0:
+                raise ConvError(st, "conv_forward_affine")
         return y
 
     __call__ = forward

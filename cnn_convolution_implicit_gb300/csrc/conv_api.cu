@@ -202,7 +202,7 @@ bool configure_smallk(conv_plan* pl) {
     s.num_segments = static_cast<int>(segments);
     s.row_bytes = static_cast<int>(row_bytes);
     const int b_bytes = (g.C_out * s.a_row_bytes + 1023) / 1024 * 1024;
-    const int fixed = 1024 + b_bytes + 8 * 2 * 32 * 64 + 1024 + 3 * 64 * 4 + 16 + g.C_out * 4;
+    const int fixed = 1024 + b_bytes + 8 * 2 * 32 * 64 + 1024 + 3 * 64 * 4 + 16 + 2 * (g.C_out + 4) * 4;
     // row segments per stage (2 * rows * C_out TMEM columns): as many as allow a two-stage ring
     int rows = 256 / g.C_out < 4 ? 256 / g.C_out : 4;
     int stages = 0;
@@ -496,7 +496,27 @@ conv_status conv_plan_launch_info(const conv_plan* p, int* grid, int* block, int
     return CONV_OK;
 }
 
+namespace {
+conv_status forward_impl(conv_plan* p, const void* x, const void* w, const float* scale, const void* bias, void* y,
+                         void* stream);
+}  // namespace
+
 conv_status conv_forward(conv_plan* p, const void* x, const void* w, const void* bias, void* y, void* stream) {
+    return forward_impl(p, x, w, nullptr, bias, y, stream);
+}
+
+conv_status conv_forward_affine(conv_plan* p, const void* x, const void* w, const void* scale, const void* bias,
+                                void* y, void* stream) {
+    if (scale == nullptr) return CONV_ERR_INVALID_ARG;
+    if (!aligned16(scale)) return CONV_ERR_MISALIGNED;
+    return forward_impl(p, x, w, static_cast<const float*>(scale), bias, y, stream);
+}
+
+}  // extern "C"
+
+namespace {
+conv_status forward_impl(conv_plan* p, const void* x, const void* w, const float* scale, const void* bias, void* y,
+                         void* stream) {
     if (p == nullptr || x == nullptr || w == nullptr || y == nullptr) return CONV_ERR_INVALID_ARG;
     if (p->device < 0) return CONV_ERR_CUDA;  // host-only plan: no device to run on
     const bool has_bias = (p->flags & CONV_FLAG_BIAS) != 0;
@@ -513,6 +533,7 @@ conv_status conv_forward(conv_plan* p, const void* x, const void* w, const void*
             if (s != CONV_OK) return s;
             TcGemmParams t = p->tc;
             t.bias = b;
+            t.scale = scale;
             t.y = static_cast<__nv_bfloat16*>(y);
             int grid = 0;
             conv_plan_launch_info(p, &grid, nullptr, nullptr, nullptr, nullptr);
@@ -526,6 +547,7 @@ conv_status conv_forward(conv_plan* p, const void* x, const void* w, const void*
             s.x = static_cast<const __nv_bfloat16*>(x);
             s.w = static_cast<const __nv_bfloat16*>(w);
             s.bias = b;
+            s.scale = scale;
             s.y = static_cast<__nv_bfloat16*>(y);
             const int grid = s.num_tiles < p->num_sms ? s.num_tiles : p->num_sms;
             e = launch_tc_smallk(p->map_y, s, grid, st);
@@ -537,6 +559,7 @@ conv_status conv_forward(conv_plan* p, const void* x, const void* w, const void*
             DepthwiseParams d = p->dw;
             d.w = static_cast<const float*>(w);
             d.bias = b;
+            d.scale = scale;
             d.y = y;
             e = launch_depthwise(p->map_a, d, st);
             break;
@@ -547,6 +570,7 @@ conv_status conv_forward(conv_plan* p, const void* x, const void* w, const void*
             d.x = x;
             d.w = w;
             d.bias = b;
+            d.scale = scale;
             d.y = y;
             d.relu = (p->flags & CONV_FLAG_RELU) ? 1 : 0;
             d.in_bf16 = p->dtype == CONV_BF16 ? 1 : 0;
@@ -561,6 +585,10 @@ conv_status conv_forward(conv_plan* p, const void* x, const void* w, const void*
     }
     return CONV_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 conv_status conv_plan_destroy(conv_plan* p) {
     delete p;

@@ -37,7 +37,8 @@ struct DirectParams {
     ConvGeom g;
     const void* x;
     const void* w;
-    const float* bias;  // nullptr when no bias
+    const float* bias;   // nullptr when no bias
+    const float* scale;  // nullptr when no per-channel scale
     void* y;
     int relu;
     int in_bf16;   // x, w are BF16 (else FP32)
@@ -48,8 +49,9 @@ cudaError_t launch_direct(const DirectParams& p, cudaStream_t stream);
 // ---------------------------------------------------------------- depthwise (FP32, TMA halo tile)
 struct DepthwiseParams {
     ConvGeom g;
-    const float* w;     // [C][Kh][Kw]
-    const float* bias;  // nullptr when no bias
+    const float* w;      // [C][Kh][Kw]
+    const float* bias;   // nullptr when no bias
+    const float* scale;  // nullptr when no per-channel scale
     void* y;
     int relu;
     int out_bf16;
@@ -92,6 +94,7 @@ struct TcGemmParams {
     int pair;          // 1: CTA-pair kernel (B rows split across the two CTAs)
     int relu;
     const float* bias;
+    const float* scale;  // nullptr when no per-channel scale
     __nv_bfloat16* y;
     unsigned* status;
 };
@@ -115,6 +118,7 @@ struct SmallKParams {
     const __nv_bfloat16* x;
     const __nv_bfloat16* w;   // [C_out][Ktot]
     const float* bias;
+    const float* scale;       // nullptr when no per-channel scale
     __nv_bfloat16* y;
     int relu;
     int ktot;          // C_in * Kh * Kw  (<= 64)

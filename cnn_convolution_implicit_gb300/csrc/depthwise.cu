@@ -85,9 +85,17 @@ struct DwOut {
     __nv_bfloat16* yb;
     long long stride;  // elements between consecutive output rows
     int relu, out_bf16;
+    int affine;         // per-channel scale: acc * scale + shift (the sum then started at 0)
+    float4 scale, shift;
 };
 
 __device__ __forceinline__ void dw_emit(DwOut& o, float4 acc, bool ok) {
+    if (o.affine) {
+        acc.x = fmaf(acc.x, o.scale.x, o.shift.x);
+        acc.y = fmaf(acc.y, o.scale.y, o.shift.y);
+        acc.z = fmaf(acc.z, o.scale.z, o.shift.z);
+        acc.w = fmaf(acc.w, o.scale.w, o.shift.w);
+    }
     if (o.relu) {
         acc.x = fmaxf(acc.x, 0.f);
         acc.y = fmaxf(acc.y, 0.f);
@@ -175,7 +183,8 @@ __global__ void __launch_bounds__(kDwThreads, kDwCtasPerSm)
     const int in_row4 = p.in_w * (kDwChannels / 4);  // float4 per input row
 
     float4 wreg[kTaps];
-    float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);   // the sum's starting value
+    float4 scale = make_float4(1.f, 1.f, 1.f, 1.f), shift = bias;
     int cur_cb = -1;
 
     for (int i = 0; i < my_count; ++i) {
@@ -190,6 +199,11 @@ __global__ void __launch_bounds__(kDwThreads, kDwCtasPerSm)
                                           __ldg(p.w + (c + 2) * kTaps + k), __ldg(p.w + (c + 3) * kTaps + k));
             }
             if (p.bias) bias = __ldg(reinterpret_cast<const float4*>(p.bias + c));
+            if (p.scale) {  // scaled sum + shift: start the sum at zero
+                scale = __ldg(reinterpret_cast<const float4*>(p.scale + c));
+                shift = bias;
+                bias = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
 
         const int slot = i % p.stages;
@@ -212,6 +226,9 @@ __global__ void __launch_bounds__(kDwThreads, kDwCtasPerSm)
         o.stride = static_cast<long long>(p.g.W_out) * p.g.C_out;
         o.relu = p.relu;
         o.out_bf16 = p.out_bf16;
+        o.affine = p.scale != nullptr;
+        o.scale = scale;
+        o.shift = shift;
 
         bool done = false;
         if constexpr (K == 3) {

@@ -53,6 +53,7 @@ __global__ void __launch_bounds__(256) direct_kernel(const DirectParams p) {
                 for (int ci = 0; ci < g.cin_g; ++ci) acc = fmaf(to_f32(xp[ci]), to_f32(wp[ci]), acc);
             }
         }
+        if (p.scale) acc *= p.scale[co];
         if (p.bias) acc += p.bias[co];
         if (p.relu) acc = fmaxf(acc, 0.f);
         if constexpr (sizeof(Tout) == 2) {

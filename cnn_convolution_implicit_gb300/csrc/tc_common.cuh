@@ -15,14 +15,26 @@ namespace convgb {
 // out in the 64-byte swizzle pattern (16-byte chunk j of row r at chunk
 // j ^ ((r >> 1) & 3)), which the Y tensor map (box 32 x 32, SWIZZLE_64B) reads.
 // Eight consecutive rows hit eight distinct bank groups, so the warp's stores
-// are conflict-free.  SMEM_BIAS: `bias` points to shared memory (else global,
-// read through the read-only path).
+// are conflict-free.  SMEM_BIAS: `bias` and `scale` point to shared memory
+// (else global, read through the read-only path).  `scale` (optional) multiplies
+// the accumulator before the bias is added.
 template <bool SMEM_BIAS = false>
 __device__ __forceinline__ void stage_row32(const uint32_t (&v)[32], const float* bias, int relu, uint8_t* stg,
-                                            int r) {
+                                            int r, const float* scale = nullptr) {
     float f[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+    if (scale != nullptr) {  // per-channel scale first (a folded batch norm), then the shift
+        const float4* s4 = reinterpret_cast<const float4*>(scale);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 s = SMEM_BIAS ? s4[i] : __ldg(s4 + i);
+            f[4 * i + 0] *= s.x;
+            f[4 * i + 1] *= s.y;
+            f[4 * i + 2] *= s.z;
+            f[4 * i + 3] *= s.w;
+        }
+    }
     if (bias != nullptr) {
         const float4* b4 = reinterpret_cast<const float4*>(bias);
 #pragma unroll

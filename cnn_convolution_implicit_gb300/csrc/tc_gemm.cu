@@ -378,7 +378,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (lane == 0) bulk_wait_read_le1();  // the tile written two chunks ago is free
                     __syncwarp();
                     uint8_t* dst = stg + sbuf * kOutTileBytes;
-                    stage_row32(cur, p.bias ? p.bias + co0 + cc : nullptr, p.relu, dst, lane);
+                    stage_row32(cur, p.bias ? p.bias + co0 + cc : nullptr, p.relu, dst, lane,
+                                p.scale ? p.scale + co0 + cc : nullptr);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0 && rows_exist) {

@@ -54,6 +54,7 @@ struct SkSmem {
     int* tab_kwd;    // per K index: kw*D
     int* tab_kh;     // per K index: kh, or -1 beyond the reduction (zero padding of K)
     float* bias;     // [C_out] copy of the bias
+    float* scale;    // [C_out] copy of the per-channel scale (when given)
 };
 
 __device__ __forceinline__ uint32_t a_tile_bytes(const SmallKParams& p) { return 128u * p.a_row_bytes; }
@@ -80,6 +81,7 @@ __device__ __forceinline__ SkSmem carve(uint8_t* raw, const SmallKParams& p) {
     s.tab_kh = s.tab_kwd + 64;
     // 16-byte aligned: the epilogue reads it as float4 (the barrier count above varies with `stages`)
     s.bias = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(s.tab_kh + 64) + 15) & ~uintptr_t(15));
+    s.scale = s.bias + ((p.g.C_out + 3) & ~3);
     return s;
 }
 
@@ -190,7 +192,10 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 sm.tab_kh[k] = -1;
             }
         }
-        for (int c = threadIdx.x; c < p.g.C_out; c += blockDim.x) sm.bias[c] = p.bias ? p.bias[c] : 0.f;
+        for (int c = threadIdx.x; c < p.g.C_out; c += blockDim.x) {
+            sm.bias[c] = p.bias ? p.bias[c] : 0.f;
+            sm.scale[c] = p.scale ? p.scale[c] : 1.f;
+        }
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -335,7 +340,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 if (lane == 0) bulk_wait_read_le1();
                 __syncwarp();
                 uint8_t* dst = stg + sbuf * kSkOutBytes;
-                stage_row32<true>(v, p.bias ? sm.bias + c : nullptr, p.relu, dst, lane);
+                stage_row32<true>(v, p.bias ? sm.bias + c : nullptr, p.relu, dst, lane,
+                                  p.scale ? sm.scale + c : nullptr);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0 && rows_exist) {  // columns past W_out fall outside the map: not written

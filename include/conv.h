@@ -116,6 +116,21 @@ conv_status conv_plan_info(const conv_plan *p, int *path, long long *gemm_m,
 conv_status conv_forward(conv_plan *p, const void *x, const void *w, const void *bias,
                          void *y, void *stream);
 
+/*
+ * conv_forward with a per-channel scale applied to the sum before the bias:
+ *
+ *   y[n][ho][wo][co] = act( scale[co] * sum + bias[co] )
+ *
+ * i.e. a batch normalisation folded into the epilogue (scale = gamma /
+ * sqrt(var + eps), bias = beta - mean * scale): the per-channel "scale and
+ * shift" step of lesson 9, section 31, fused with the bias and activation.
+ * scale is a device pointer to C_out FP32 values, non-NULL and 16-byte
+ * aligned; bias follows the plan's CONV_FLAG_BIAS as in conv_forward (without
+ * it the shift is zero).  Same layouts, errors and asynchrony as conv_forward.
+ */
+conv_status conv_forward_affine(conv_plan *p, const void *x, const void *w, const void *scale,
+                                const void *bias, void *y, void *stream);
+
 /* Free the plan (host memory only).  NULL is accepted. */
 conv_status conv_plan_destroy(conv_plan *p);
 

@@ -66,7 +66,11 @@ def test_create_null_out_and_null_plan_calls():
     a, b = ctypes.c_int(), ctypes.c_int()
     assert L.conv_plan_output_shape(None, ctypes.byref(a), ctypes.byref(b)) == 1
     assert L.conv_forward(None, 16, 16, None, 16, None) == 1
+    assert L.conv_forward_affine(None, 16, 16, 16, None, 16, None) == 1
     assert L.conv_device_status(None) == 1
+    p = cg.ConvPlan(1, 8, 8, 8, 8, 3, 3, 1, 1, 1, 1, "f32")
+    assert L.conv_forward_affine(p._plan, 256, 256, None, None, 256, None) == 1   # scale required
+    assert L.conv_forward_affine(p._plan, 256, 256, 260, None, 256, None) == 3    # misaligned scale
 
 
 @pytest.mark.parametrize("shape,path", [
