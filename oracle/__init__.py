@@ -16,7 +16,10 @@ follows, is stated at the top of ``conv_oracle.c``:
   their matrix operations" (lpnh.cn/news/2674933), sections 2.2, 2.3, 4.2,
   4.3, 6.2;
 * bias after the sum, then ReLU: lesson 9, section 31 (with its per-channel
-  scale and shift, a folded batch norm: y = act(scale * sum + shift)).
+  scale and shift, a folded batch norm: y = act(scale * sum + shift));
+* the depthwise-separable block, depthwise 3x3 then pointwise 1x1 (lesson 9,
+  section 25), with its intermediate rounded to BF16 (``round_bf16``, the
+  pointwise GEMM's operand type).
 
 Every function here is pinned by ``tests/test_oracle.py`` against values the
 pages print, closed forms, and two independent restatements.
@@ -186,3 +189,32 @@ def macs_at(x, w, n, co, ho, wo, stride=1, padding=0, dilation=1, groups=1,
     d = _desc(x, w, x_layout, w_layout, "NCHW", stride, padding, dilation, groups, False)
     return int(lib.oracle_conv2d_macs_at(ctypes.byref(d), x.ctypes.data, w.ctypes.data,
                                          n, co, ho, wo))
+
+
+def round_bf16(a):
+    """Round to the nearest BF16 value (8 significant bits, ties to even), returned as float64.
+
+    BF16 keeps FP32's exponent range with a 7-bit stored mantissa; below the normal
+    range its spacing stays 2**-133.  Written from that definition: scale each value
+    by its own ulp, round half-to-even, scale back."""
+    a = np.asarray(a, dtype=np.float64)
+    _, e = np.frexp(a)                        # a = m * 2**e, 0.5 <= |m| < 1
+    ulp = np.ldexp(1.0, np.maximum(e - 8, -133))
+    r = np.rint(a / ulp) * ulp                # np.rint rounds halves to even
+    big = np.abs(r) > np.ldexp(255.0, 120)    # beyond the largest finite BF16 (0x7f7f)
+    return np.where(big, np.copysign(np.inf, a), r)
+
+
+def dwpw_block(x, w_dw, w_pw, padding=1, dw_scale=None, dw_bias=None, dw_relu=False,
+               pw_scale=None, pw_bias=None, pw_relu=False, round_mid=True, nthreads=0):
+    """Depthwise-separable block (lesson 9, section 25): depthwise KxK, stride 1, then 1x1.
+
+    x NCHW [N][C][H][W]; w_dw [C][1][K][K] (groups = C); w_pw [C_out][C][1][1].
+    Intermediate t = act_dw(dw_scale * dw(x) + dw_bias), rounded to BF16 when
+    ``round_mid`` (the pointwise GEMM's operand type), then
+    y = act_pw(pw_scale * pw(t) + pw_bias).  Returns y (NCHW, float64)."""
+    C = np.asarray(x).shape[1]
+    mid = conv2d(x, w_dw, dw_bias, 1, padding, 1, C, dw_relu, nthreads=nthreads, scale=dw_scale)
+    if round_mid:
+        mid = round_bf16(mid)
+    return conv2d(mid, w_pw, pw_bias, 1, 0, 1, 1, pw_relu, nthreads=nthreads, scale=pw_scale)

@@ -362,3 +362,60 @@ def test_scale_all_ones_closed_form_and_points():
     pts = np.array([[0, 0, 2, 2], [0, 0, 0, 0]])
     v = oracle.conv2d_points(np.ones((1, 1, 5, 5)), w, np.array([0.5]), pts, 1, 1, scale=np.array([-2.0]))
     assert v[0] == y[2, 2] and v[1] == y[0, 0]
+
+
+# ----------------------------------------------------------------- BF16 rounding and the block
+def test_round_bf16_matches_torch_on_float32_values():
+    """Nearest-even rounding to BF16 agrees with torch's float32 -> bfloat16 conversion
+    on random values, exact ties, signed zeros, subnormals and the largest finite values."""
+    rng = np.random.default_rng(11)
+    bits = rng.integers(0, 2**32, 200000, dtype=np.uint64).astype(np.uint32)
+    vals = bits.view(np.float32)
+    vals = vals[np.isfinite(vals)]
+    ties = (rng.integers(0, 2**16, 4000, dtype=np.uint32) << 16 | 0x8000).view(np.float32)  # exact halves
+    ties = ties[np.isfinite(ties)]
+    special = np.array([0.0, -0.0, 1.0, -1.0, 1.00390625, 1.01171875, 1e-40, -3e-39, 3.3e38, -3.38e38,
+                        np.float32(2**-126), np.float32(2**-133) * 3], dtype=np.float32)
+    for v in (vals, ties, special, rng.standard_normal(100000).astype(np.float32)):
+        ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+        got = oracle.round_bf16(v.astype(np.float64))
+        assert np.array_equal(got, ref), v[np.argmax(got != ref)]
+
+
+def test_round_bf16_ties_go_to_even():
+    # 1 + 2**-8 lies halfway between 1 and 1 + 2**-7: even mantissa is 1.0
+    assert oracle.round_bf16(1 + 2.0**-8) == 1.0
+    assert oracle.round_bf16(1 + 3 * 2.0**-8) == 1 + 2 * 2.0**-7
+    assert oracle.round_bf16(-(1 + 2.0**-8)) == -1.0
+
+
+def test_block_identity_depthwise_is_pointwise_of_rounded_input():
+    """With a centre-tap depthwise kernel (no scale, shift, ReLU) the block is the 1x1
+    conv of bf16(x): a numpy GEMM over channels."""
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((2, 64, 5, 6))
+    wdw = np.zeros((64, 1, 3, 3))
+    wdw[:, 0, 1, 1] = 1.0
+    wpw = rng.standard_normal((32, 64, 1, 1))
+    b = rng.standard_normal(32)
+    y = oracle.dwpw_block(x, wdw, wpw, 1, pw_bias=b)
+    xr = oracle.round_bf16(x)
+    ref = np.einsum("oc,nchw->nohw", wpw[:, :, 0, 0], xr) + b[None, :, None, None]
+    assert np.allclose(y, ref, rtol=1e-13, atol=1e-12)
+
+
+def test_block_stages_apply_in_order():
+    """The depthwise stage's scale, shift and ReLU act before the rounding and the
+    pointwise sum: a negative depthwise shift under dw ReLU zeroes the pointwise input."""
+    x = np.ones((1, 64, 4, 4))
+    wdw = np.ones((64, 1, 3, 3))
+    wpw = np.ones((32, 64, 1, 1))
+    y = oracle.dwpw_block(x, wdw, wpw, 1, dw_scale=np.full(64, 0.5), dw_bias=np.full(64, -10.0),
+                          dw_relu=True, pw_bias=np.full(32, 0.25))
+    assert np.all(y == 0.25)
+    # without the ReLU: interior depthwise sum 9 * 0.5 - 10 = -5.5, pointwise 64 * -5.5 + 0.25
+    y = oracle.dwpw_block(x, wdw, wpw, 1, dw_scale=np.full(64, 0.5), dw_bias=np.full(64, -10.0),
+                          pw_bias=np.full(32, 0.25))
+    assert y[0, 0, 1, 1] == 64 * -5.5 + 0.25
+    # a corner sees 4 taps: 4 * 0.5 - 10 = -8
+    assert y[0, 3, 0, 0] == 64 * -8.0 + 0.25
