@@ -69,6 +69,7 @@ KERNEL_SOURCES = {
     "stem": ["tc_smallk.cu", "tc_common.cuh", "ptx.cuh", "conv_internal.h"],
     "dw": ["depthwise.cu", "ptx.cuh", "conv_internal.h"],
     "tiny_f32": ["direct.cu", "conv_internal.h"],
+    "block": ["dwpw_block.cu", "tc_common.cuh", "ptx.cuh", "conv_internal.h"],
 }
 
 
@@ -260,6 +261,47 @@ def measure_layer(name, steps, warmup, flush, peaks, affine=False):
     return res, (s, plan, host, (xd, wd, bd, y))
 
 
+def measure_block(steps, warmup, flush, peaks):
+    """The depthwise-separable block (depthwise 3x3 FP32 on N64 C256 56x56, then the
+    256 -> 512 pointwise with bias + ReLU): the fused kernel, and for comparison the
+    two-launch path (depthwise writing a BF16 intermediate, then the 1x1 GEMM)."""
+    from cnn_convolution_implicit_gb300 import BlockPlan, ConvPlan
+    sd, x, wd, _ = inputs("dw")
+    sp, _, wp, bp = inputs("pw")
+    plan = BlockPlan(sd.N, sd.C_in, sd.H, sd.W, sp.C_out, 3, 1, dw_relu=False, pw_relu=True)
+    xd = x_device(x, "f32")
+    wdd = torch.from_numpy(np.ascontiguousarray(wd[:, 0], np.float32)).cuda()
+    wpd = w_device(wp, "bf16").reshape(sp.C_out, sp.C_in)
+    bd = b_device(bp)
+    y = plan.empty_output()
+    ms = time_steps(lambda: plan.forward(xd, wdd, wpd, pw_bias=bd, y=y), steps, warmup, flush)
+    t = float(np.mean(ms)) * 1e-3
+    # algorithmic bytes: FP32 input and BF16 output once, weights and bias once
+    nbytes = x.size * 4 + sp.pixels * sp.C_out * 2 + wd.size * 4 + wp.size * 2 + bp.size * 4
+    flops = sd.flops + sp.flops
+    res = {"workload": "block (fused dw3x3 + pw1x1)", "kernel": "dwpw_block", "ms": t * 1e3,
+           "tflops": flops / t / 1e12, "gbs": nbytes / t / 1e9, "bound": "hbm", "flops": flops, "bytes": nbytes,
+           "frac": nbytes / t / 1e9 / peaks["hbm_gbs"], "launches": steps,
+           "source_hash": kernel_source_hash("block"), "launch": plan.launch}
+    dw_plan = ConvPlan(sd.N, sd.C_in, sd.H, sd.W, sd.C_out, 3, 3, 1, 1, 1, sd.G, "f32", False, False,
+                       out_bf16=True)
+    pw_plan = ConvPlan.for_shape(sp)
+    wdd4, wpd4 = w_device(wd, "f32"), w_device(wp, "bf16")
+    mid = dw_plan.empty_output()
+    y2 = pw_plan.empty_output()
+
+    def two():
+        dw_plan.forward(xd, wdd4, None, mid)
+        pw_plan.forward(mid, wpd4, bd, y2)
+
+    ms2 = time_steps(two, steps, warmup, flush)
+    t2 = float(np.mean(ms2)) * 1e-3
+    two_res = {"workload": "block (two launches: dw -> bf16 -> pw)", "kernel": "depthwise + gemm_1x1",
+               "ms": t2 * 1e3, "gbs": nbytes / t2 / 1e9, "frac": nbytes / t2 / 1e9 / peaks["hbm_gbs"],
+               "launches": 2 * steps}
+    return res, two_res
+
+
 class OracleSampler:
     """Times the FP64 oracle (as it stands, never tuned) on bounded seeded samples
     of a workload's outputs, on this host's cores.  Inputs are drawn once."""
@@ -315,7 +357,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=sorted(WORKLOADS), default=None,
+    ap.add_argument("--only", choices=sorted(WORKLOADS) + ["block"], default=None,
                     help="time one layer alone (no oracle, no e2e); used for ncu captures")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -323,7 +365,10 @@ def main():
     if args.only:
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-        r, _ = measure_layer(args.only, args.steps, args.warmup, flush, load_peaks())
+        if args.only == "block":
+            r, _ = measure_block(args.steps, args.warmup, flush, load_peaks())
+        else:
+            r, _ = measure_layer(args.only, args.steps, args.warmup, flush, load_peaks())
         print(json.dumps(r))
         return
 
@@ -420,6 +465,8 @@ def main():
         others[name] = r
     r, _ = measure_layer("body", max(10, args.steps // 2), args.warmup, flush, peaks, affine=True)
     others["body+affine"] = r
+    others["block"], others["block_two_launches"] = measure_block(max(10, args.steps // 2), args.warmup, flush,
+                                                                  peaks)
 
     traffic = load_traffic()
     tr = traffic.get("body")

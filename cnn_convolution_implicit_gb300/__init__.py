@@ -4,8 +4,8 @@ direct fallback kernel, behind the C ABI of include/conv.h.
 
     from cnn_convolution_implicit_gb300 import ConvPlan, conv2d
 """
-from .binding import (CONV_BF16, CONV_F32, EXPORTS, PATHS, ConvError, ConvPlan, conv2d,
-                      device_status, lib)
+from .binding import (CONV_BF16, CONV_F32, EXPORTS, PATHS, BlockPlan, ConvError, ConvPlan,
+                      conv2d, device_status, lib)
 
-__all__ = ["ConvPlan", "conv2d", "ConvError", "device_status", "lib", "PATHS", "EXPORTS",
-           "CONV_BF16", "CONV_F32"]
+__all__ = ["ConvPlan", "BlockPlan", "conv2d", "ConvError", "device_status", "lib", "PATHS",
+           "EXPORTS", "CONV_BF16", "CONV_F32"]

@@ -23,7 +23,10 @@ PATHS = {0: "direct", 1: "depthwise", 2: "gemm_1x1", 3: "implicit_gemm", 4: "sma
 # Every symbol include/conv.h declares.
 EXPORTS = ("conv_plan_create", "conv_plan_output_shape", "conv_plan_info", "conv_forward",
            "conv_plan_destroy", "conv_status_string", "conv_device_status", "conv_plan_num_sms",
-           "conv_plan_launch_info", "conv_forward_affine")
+           "conv_plan_launch_info", "conv_forward_affine", "conv_block_plan_create",
+           "conv_block_plan_output_shape", "conv_block_forward", "conv_block_plan_launch_info",
+           "conv_block_plan_destroy")
+CONV_BLOCK_DW_RELU, CONV_BLOCK_PW_RELU = 1, 2
 
 _lock = threading.Lock()
 _lib = None
@@ -73,6 +76,16 @@ def lib():
             L.conv_plan_num_sms.restype = c_int
             L.conv_plan_launch_info.argtypes = [vp] + [ctypes.POINTER(c_int)] * 5
             L.conv_plan_launch_info.restype = c_int
+            L.conv_block_plan_create.argtypes = [ctypes.POINTER(vp)] + [c_int] * 7 + [ctypes.c_uint]
+            L.conv_block_plan_create.restype = c_int
+            L.conv_block_plan_output_shape.argtypes = [vp, ctypes.POINTER(c_int), ctypes.POINTER(c_int)]
+            L.conv_block_plan_output_shape.restype = c_int
+            L.conv_block_forward.argtypes = [vp] * 10
+            L.conv_block_forward.restype = c_int
+            L.conv_block_plan_launch_info.argtypes = [vp] + [ctypes.POINTER(c_int)] * 5
+            L.conv_block_plan_launch_info.restype = c_int
+            L.conv_block_plan_destroy.argtypes = [vp]
+            L.conv_block_plan_destroy.restype = c_int
             _lib = L
         return _lib
 
@@ -187,6 +200,83 @@ class ConvPlan:
                                            y.data_ptr(), stream.cuda_stream)
             if st != 0:
                 raise ConvError(st, "conv_forward_affine")
+        return y
+
+    __call__ = forward
+
+
+class BlockPlan:
+    """Fused depthwise-separable block: depthwise 3x3 (FP32) -> BF16 -> pointwise 1x1
+    (BF16 tensor cores), one kernel (include/conv.h, conv_block_forward).
+
+    x NHWC FP32 [N][H][W][C]; w_dw FP32 [C][3][3]; w_pw BF16 [C_out][C]; optional
+    FP32 per-channel scale / shift for each stage; y NHWC BF16 [N][H_out][W_out][C_out].
+    """
+
+    def __init__(self, N, C, H, W, C_out, K=3, P=1, dw_relu=False, pw_relu=True):
+        L = lib()
+        self._plan = None
+        flags = (CONV_BLOCK_DW_RELU if dw_relu else 0) | (CONV_BLOCK_PW_RELU if pw_relu else 0)
+        h = ctypes.c_void_p()
+        st = L.conv_block_plan_create(ctypes.byref(h), N, C, H, W, C_out, K, P, flags)
+        if st != 0:
+            raise ConvError(st, "conv_block_plan_create")
+        self._plan = h
+        self.shape = (N, C, H, W, C_out, K, P)
+        self.dw_relu, self.pw_relu = dw_relu, pw_relu
+        ho, wo = ctypes.c_int(), ctypes.c_int()
+        L.conv_block_plan_output_shape(h, ctypes.byref(ho), ctypes.byref(wo))
+        self.H_out, self.W_out = ho.value, wo.value
+        li = [ctypes.c_int() for _ in range(5)]
+        L.conv_block_plan_launch_info(h, *[ctypes.byref(v) for v in li])
+        self.launch = dict(zip(("grid", "block", "smem_bytes", "halo_stages", "weight_stages"),
+                               [v.value for v in li]))
+
+    def close(self):
+        if self._plan is not None and _lib is not None:
+            _lib.conv_block_plan_destroy(self._plan)
+        self._plan = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def empty_output(self, device="cuda"):
+        import torch
+        N, C_out = self.shape[0], self.shape[4]
+        return torch.empty((N, self.H_out, self.W_out, C_out), dtype=torch.bfloat16, device=device)
+
+    def forward(self, x, w_dw, w_pw, dw_scale=None, dw_bias=None, pw_scale=None, pw_bias=None, y=None,
+                stream=None):
+        """Launch on ``stream`` (default: torch's current stream); returns y."""
+        import torch
+        N, C, H, W, C_out, K, P = self.shape
+
+        def need(t, name, shape, dtype):
+            if t is None or not t.is_cuda or t.dtype != dtype or tuple(t.shape) != shape or not t.is_contiguous():
+                raise ValueError("%s must be a contiguous CUDA %s tensor of shape %s" % (name, dtype, shape))
+
+        need(x, "x", (N, H, W, C), torch.float32)
+        need(w_dw, "w_dw", (C, K, K), torch.float32)
+        need(w_pw, "w_pw", (C_out, C), torch.bfloat16)
+        for t, name, n in ((dw_scale, "dw_scale", C), (dw_bias, "dw_bias", C), (pw_scale, "pw_scale", C_out),
+                           (pw_bias, "pw_bias", C_out)):
+            if t is not None:
+                need(t, name, (n,), torch.float32)
+        if y is None:
+            y = self.empty_output(x.device)
+        else:
+            need(y, "y", (N, self.H_out, self.W_out, C_out), torch.bfloat16)
+        if stream is None:
+            stream = torch.cuda.current_stream(x.device)
+        ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+        st = lib().conv_block_forward(self._plan, x.data_ptr(), w_dw.data_ptr(), ptr(dw_scale), ptr(dw_bias),
+                                      w_pw.data_ptr(), ptr(pw_scale), ptr(pw_bias), y.data_ptr(),
+                                      stream.cuda_stream)
+        if st != 0:
+            raise ConvError(st, "conv_block_forward")
         return y
 
     __call__ = forward

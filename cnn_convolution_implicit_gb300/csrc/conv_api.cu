@@ -356,6 +356,24 @@ conv_status encode_maps(conv_plan* pl, const void* x, const void* w, void* y) {
 
 }  // namespace
 
+namespace convgb {
+
+bool tensor_map_encoder_ready() { return load_entry_points(); }
+
+CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t rank, void* base, const cuuint64_t* dims,
+                      const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle) {
+    if (!load_entry_points()) return CUDA_ERROR_NOT_INITIALIZED;
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return g_encode_tiled(map, type, rank, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+cudaError_t device_status_word(unsigned** word) {
+    return cudaGetSymbolAddress(reinterpret_cast<void**>(word), g_conv_status_word);
+}
+
+}  // namespace convgb
+
 extern "C" {
 
 conv_status conv_plan_create(conv_plan** out, int N, int C_in, int H, int W, int C_out, int Kh, int Kw, int S,

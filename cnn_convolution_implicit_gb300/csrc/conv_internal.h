@@ -138,4 +138,44 @@ struct SmallKParams {
 // y_map: 3-D {C_out, W_out, N*H_out} BF16, box {32, 32, 1}, 64-byte swizzle.
 cudaError_t launch_tc_smallk(const CUtensorMap& y_map, const SmallKParams& p, int grid, cudaStream_t stream);
 
+// ---------------------------------------------------------------- fused depthwise 3x3 + pointwise 1x1 block
+constexpr int kBkTileH = 16;          // output tile: 16 rows x 8 columns = 128 pixels (TMEM lanes)
+constexpr int kBkTileW = 8;
+constexpr int kBkChunk = 32;          // depthwise channels per halo copy (one 128-byte FP32 row)
+constexpr int kBkHaloBytes = (kBkTileH + 2) * (kBkTileW + 2) * kBkChunk * 4;  // 23,040
+constexpr int kBkThreads = 480;       // halo producer, MMA, 2 x 4 epilogue, 4 depthwise, weight producer
+constexpr int kBkMaxKblk = 4;         // C <= 256: the whole BF16 A tile (128 x C) stays in shared memory
+
+struct BlockParams {
+    int N, C, H, W, C_out, P;
+    int H_out, W_out;
+    int tiles_w, tiles_h, num_tiles;  // 16 x 8 output tiles
+    int kblk;                         // C / 64 (A k-blocks)
+    int chunks;                       // C / 32 (halo copies per tile)
+    int slices, slice_n;              // pointwise GEMM N slices (slice_n <= 256, multiple of 32)
+    int halo_stages, b_stages;
+    int tmem_cols;
+    int smem_bytes;
+    int dw_relu, pw_relu;
+    const float* w_dw;      // [C][3][3]
+    const float* dw_scale;  // nullptr: 1
+    const float* dw_bias;   // nullptr: 0
+    const float* pw_scale;  // nullptr: none
+    const float* pw_bias;   // nullptr: none
+    unsigned* status;
+};
+// x_map: FP32 4-D {C, W, H, N}, box {32, 10, 18, 1}, no swizzle.  w_map: BF16
+// 2-D {C, C_out}, box {64, slice_n}, 128-byte swizzle.  y_map: BF16 4-D
+// {C_out, W_out, H_out, N}, box {32, 8, 4, 1}, 64-byte swizzle.
+cudaError_t launch_dwpw_block(const CUtensorMap& x_map, const CUtensorMap& w_map, const CUtensorMap& y_map,
+                              const BlockParams& p, int grid, cudaStream_t stream);
+// Shared memory the block kernel needs for a configuration.
+int dwpw_block_smem_bytes(int C, int slice_n, int halo_stages, int b_stages);
+
+// Helpers of the plan code, shared with the block plan (conv_api.cu).
+bool tensor_map_encoder_ready();
+CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t rank, void* base, const cuuint64_t* dims,
+                      const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle);
+cudaError_t device_status_word(unsigned** word);
+
 }  // namespace convgb

@@ -159,6 +159,76 @@ int conv_plan_num_sms(const conv_plan *p);
 conv_status conv_plan_launch_info(const conv_plan *p, int *grid, int *block, int *smem_bytes,
                                   int *stages, int *cluster);
 
+/* ------------------------------------------------------------------------
+ * Depthwise-separable block in one kernel: depthwise 3x3 (FP32) followed by
+ * pointwise 1x1 (BF16 tensor cores), the two stages of "GPU lesson 9"
+ * section 25, fused so the depthwise feature map never goes to memory (the
+ * kernel fusion that section names to save its write and re-read):
+ *
+ *   t[n][ho][wo][c]  = bf16( act_dw( dw_scale[c] * sum_{kh,kw<3}
+ *                        x[n][ho+kh-P][wo+kw-P][c] * w_dw[c][kh][kw] + dw_bias[c] ) )
+ *   y[n][ho][wo][co] = act_pw( pw_scale[co] * sum_{c<C} t[n][ho][wo][c] * w_pw[co][c]
+ *                        + pw_bias[co] )
+ *
+ * with H_out = H + 2P - 2, W_out = W + 2P - 2 (stride 1, dilation 1), input
+ * pixels outside the image read as zero, bf16() round-to-nearest-even (the
+ * pointwise GEMM's BF16 operand; the sum stays FP32), act_dw / act_pw ReLU when
+ * CONV_BLOCK_DW_RELU / CONV_BLOCK_PW_RELU is set.
+ *
+ * Layouts (dense, caller-owned device memory, 16-byte aligned):
+ *   x        [N][H][W][C]        FP32 (NHWC)
+ *   w_dw     [C][3][3]           FP32
+ *   dw_scale, dw_bias [C]        FP32, each may be NULL (scale 1, shift 0)
+ *   w_pw     [C_out][C]          BF16
+ *   pw_scale, pw_bias [C_out]    FP32, each may be NULL (scale 1, shift 0)
+ *   y        [N][H_out][W_out][C_out]  BF16 (NHWC)
+ * Supported: K = 3, 0 <= P <= 2, C % 64 == 0 and C <= 256, C_out % 32 == 0
+ * (the output channels run as equal slices of at most 256, each a multiple
+ * of 32, two slices in flight in tensor memory).  Other blocks get CONV_ERR_UNSUPPORTED from the create call
+ * and run as two conv_forward calls (a depthwise plan with CONV_FLAG_OUT_BF16,
+ * then a 1x1 plan).  The plan owns no device memory.
+ * ------------------------------------------------------------------------ */
+typedef struct conv_block_plan conv_block_plan; /* opaque, host-owned */
+
+#define CONV_BLOCK_DW_RELU 1u
+#define CONV_BLOCK_PW_RELU 2u
+
+/*
+ * Check the block's shape and choose its launch configuration.  *plan gets a
+ * new plan, or NULL on error.  Returns CONV_ERR_INVALID_ARG for non-positive
+ * sizes, an empty output or unknown flags, CONV_ERR_UNSUPPORTED for a valid
+ * block outside the supported family above, CONV_ERR_CUDA if the device
+ * cannot be queried.  Without a device a host-only plan is made (shape checks
+ * only); its forward returns CONV_ERR_CUDA.
+ */
+conv_status conv_block_plan_create(conv_block_plan **plan, int N, int C, int H, int W, int C_out,
+                                   int K, int P, unsigned flags);
+
+/* Output extents of the block (H_out = H + 2P - 2, W_out = W + 2P - 2). */
+conv_status conv_block_plan_output_shape(const conv_block_plan *p, int *H_out, int *W_out);
+
+/*
+ * Run the block on `stream` (a cudaStream_t; NULL = the legacy default
+ * stream).  x, w_dw, w_pw, y must be non-NULL; every non-NULL pointer must be
+ * 16-byte aligned (else CONV_ERR_MISALIGNED); y must not overlap any input.
+ * Asynchronous like conv_forward; wait timeouts are latched for
+ * conv_device_status.
+ */
+conv_status conv_block_forward(conv_block_plan *p, const void *x, const void *w_dw,
+                               const void *dw_scale, const void *dw_bias, const void *w_pw,
+                               const void *pw_scale, const void *pw_bias, void *y, void *stream);
+
+/*
+ * Launch configuration of conv_block_forward: grid and block size, dynamic
+ * shared memory per CTA, halo-copy and weight-ring stages.  Any output
+ * pointer may be NULL.
+ */
+conv_status conv_block_plan_launch_info(const conv_block_plan *p, int *grid, int *block,
+                                        int *smem_bytes, int *halo_stages, int *weight_stages);
+
+/* Free the block plan (host memory only).  NULL is accepted. */
+conv_status conv_block_plan_destroy(conv_block_plan *p);
+
 #ifdef __cplusplus
 }
 #endif

@@ -114,3 +114,66 @@ def test_forward_without_device_fails_loudly():
     p = cg.ConvPlan(1, 8, 8, 8, 8, 3, 3, 1, 1, 1, 1, "f32")
     L = cg.lib()
     assert L.conv_forward(p._plan, 256, 256, 256, 256, None) == 4  # CONV_ERR_CUDA, nothing launched
+
+
+# ----------------------------------------------------------------- fused depthwise-separable block
+def _block_create(*args):
+    L = cg.lib()
+    h = ctypes.c_void_p(1234)
+    st = L.conv_block_plan_create(ctypes.byref(h), *args)
+    return st, h
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, 64, 8, 8, 32, 3, 1, 0), 1),       # N = 0
+    ((1, 64, 8, 8, 32, 3, -1, 0), 1),      # P < 0
+    ((1, 64, 1, 1, 32, 3, 0, 0), 1),       # empty output
+    ((1, 64, 8, 8, 32, 3, 1, 4), 1),       # unknown flag
+    ((1, 64, 8, 8, 32, 5, 2, 0), 2),       # 5x5 depthwise: not fused
+    ((1, 64, 8, 8, 32, 3, 3, 0), 2),       # P > 2
+    ((1, 96, 8, 8, 32, 3, 1, 0), 2),       # C % 64 != 0
+    ((1, 320, 8, 8, 32, 3, 1, 0), 2),      # C > 256
+    ((1, 64, 8, 8, 48, 3, 1, 0), 2),       # C_out % 32 != 0
+])
+def test_block_create_rejects(args, status):
+    st, h = _block_create(*args)
+    assert st == status and h.value is None
+
+
+@pytest.mark.parametrize("C_out,slices", [(32, 1), (256, 1), (320, 2), (384, 2), (512, 2), (352, 11), (768, 3)])
+def test_block_output_slices_and_stages(C_out, slices):
+    p = cg.BlockPlan(2, 128, 12, 12, C_out, 3, 1)
+    assert (p.H_out, p.W_out) == (12, 12)
+    assert p.launch["block"] == 480
+    assert p.launch["halo_stages"] >= 2 and p.launch["weight_stages"] >= 2
+    assert p.launch["smem_bytes"] <= 232448
+
+
+def test_block_full_size_launch():
+    p = cg.BlockPlan(64, 256, 56, 56, 512, 3, 1)
+    assert (p.H_out, p.W_out) == (56, 56)
+    tiles = 64 * 4 * 7  # 16 x 8 output tiles: 56 / 16 -> 4 rows of tiles, 56 / 8 -> 7 columns
+    assert 1 <= p.launch["grid"] <= tiles
+    if not torch.cuda.is_available():
+        assert p.launch["grid"] == 152  # host-only plan: one persistent CTA per SM of a 152-SM part
+
+
+def test_block_null_and_misaligned_calls():
+    L = cg.lib()
+    assert L.conv_block_plan_create(None, 1, 64, 8, 8, 32, 3, 1, 0) == 1
+    assert L.conv_block_plan_destroy(None) == 0
+    a, b = ctypes.c_int(), ctypes.c_int()
+    assert L.conv_block_plan_output_shape(None, ctypes.byref(a), ctypes.byref(b)) == 1
+    assert L.conv_block_plan_launch_info(None, None, None, None, None, None) == 1
+    assert L.conv_block_forward(None, 16, 16, None, None, 16, None, None, 16, None) == 1
+    p = cg.BlockPlan(1, 64, 8, 8, 32, 3, 1)
+    assert L.conv_block_forward(p._plan, None, 256, None, None, 256, None, None, 256, None) == 1
+    assert L.conv_block_forward(p._plan, 256, 256, 260, None, 256, None, None, 256, None) == 3
+    assert L.conv_block_forward(p._plan, 256, 256, None, None, 256, None, 264, 256, None) == 3
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device behaviour")
+def test_block_forward_without_device_fails_loudly():
+    p = cg.BlockPlan(1, 64, 8, 8, 32, 3, 1)
+    L = cg.lib()
+    assert L.conv_block_forward(p._plan, 256, 256, None, None, 256, None, None, 256, None) == 4
