@@ -133,7 +133,7 @@ conv_status conv_block_plan_create(conv_block_plan** out, int N, int C, int H, i
     b.halo_stages = b.b_stages = 0;
     for (int hs = 4; hs >= 2 && b.halo_stages == 0; --hs)
         for (int bs = 4; bs >= 2; --bs)
-            if (dwpw_block_smem_bytes(C, b.slice_n, hs, bs) <= smem_optin) {
+            if (dwpw_block_smem_bytes(C, C_out, b.slice_n, hs, bs) <= smem_optin) {
                 b.halo_stages = hs;
                 b.b_stages = bs;
                 break;
@@ -142,7 +142,7 @@ conv_status conv_block_plan_create(conv_block_plan** out, int N, int C, int H, i
         delete pl;
         return CONV_ERR_UNSUPPORTED;
     }
-    b.smem_bytes = dwpw_block_smem_bytes(C, b.slice_n, b.halo_stages, b.b_stages);
+    b.smem_bytes = dwpw_block_smem_bytes(C, C_out, b.slice_n, b.halo_stages, b.b_stages);
     pl->grid = b.num_tiles < pl->num_sms ? b.num_tiles : pl->num_sms;
     *out = pl;
     return CONV_OK;

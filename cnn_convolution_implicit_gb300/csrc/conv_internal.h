@@ -170,7 +170,7 @@ struct BlockParams {
 cudaError_t launch_dwpw_block(const CUtensorMap& x_map, const CUtensorMap& w_map, const CUtensorMap& y_map,
                               const BlockParams& p, int grid, cudaStream_t stream);
 // Shared memory the block kernel needs for a configuration.
-int dwpw_block_smem_bytes(int C, int slice_n, int halo_stages, int b_stages);
+int dwpw_block_smem_bytes(int C, int C_out, int slice_n, int halo_stages, int b_stages);
 
 // Helpers of the plan code, shared with the block plan (conv_api.cu).
 bool tensor_map_encoder_ready();

@@ -53,6 +53,8 @@ struct BkSmem {
     float* wdw;  // [chunk][tap][32]
     float* dsc;  // [C]
     float* dbi;  // [C]
+    float* pbi;  // [C_out] pointwise shift
+    float* psc;  // [C_out] pointwise scale
     uint64_t* hfull;
     uint64_t* hempty;
     uint64_t* bfull;
@@ -76,7 +78,9 @@ __device__ __forceinline__ BkSmem bk_carve(uint8_t* raw, const BlockParams& p) {
     s.wdw = reinterpret_cast<float*>(s.halo + p.halo_stages * kBkHaloBytes);
     s.dsc = s.wdw + p.C * 9;
     s.dbi = s.dsc + p.C;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s.dbi + p.C);
+    s.pbi = s.dbi + p.C;
+    s.psc = s.pbi + p.C_out;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s.psc + p.C_out);
     s.hfull = bars;
     s.hempty = s.hfull + p.halo_stages;
     s.bfull = s.hempty + p.halo_stages;
@@ -167,6 +171,10 @@ __global__ void __launch_bounds__(kBkThreads, 1)
     for (int c = threadIdx.x; c < p.C; c += blockDim.x) {
         sm.dsc[c] = p.dw_scale ? __ldg(p.dw_scale + c) : 1.f;
         sm.dbi[c] = p.dw_bias ? __ldg(p.dw_bias + c) : 0.f;
+    }
+    for (int c = threadIdx.x; c < p.C_out; c += blockDim.x) {  // read by the epilogue from shared memory
+        sm.psc[c] = p.pw_scale ? __ldg(p.pw_scale + c) : 1.f;
+        sm.pbi[c] = p.pw_bias ? __ldg(p.pw_bias + c) : 0.f;
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.halo_stages; ++s) {
@@ -407,34 +415,25 @@ __global__ void __launch_bounds__(kBkThreads, 1)
                 const int co0 = sl * p.slice_n;
                 const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        static_cast<uint32_t>(buf * p.slice_n);
-                uint32_t va[32], vb[32];
-                __syncwarp();
-                tmem_ld32(t_row, va);
-                for (int c = 0; c < p.slice_n; c += 64) {
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int cc = c + 32 * hh;
-                        if (cc >= p.slice_n) break;
-                        uint32_t(&cur)[32] = hh == 0 ? va : vb;
-                        uint32_t(&nxt)[32] = hh == 0 ? vb : va;
-                        tmem_ld_wait(cur);
-                        if (cc + 32 < p.slice_n) {
-                            __syncwarp();
-                            tmem_ld32(t_row + static_cast<uint32_t>(cc + 32), nxt);
-                        }
-                        if (lane == 0) bulk_wait_read_le1();
-                        __syncwarp();
-                        uint8_t* dst = stg + sbuf * kBkStoreTile;
-                        stage_row32(cur, p.pw_bias ? p.pw_bias + co0 + cc : nullptr, p.pw_relu, dst, lane,
-                                    p.pw_scale ? p.pw_scale + co0 + cc : nullptr);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0 && rows_exist) {
-                            tma_store_4d(&y_map, dst, co0 + cc, t.wo0, h, t.n);
-                            bulk_commit();
-                        }
-                        sbuf ^= 1;
+                // one 32-column chunk at a time: the TMEM load latency is short next to
+                // the staging and store work, and a second register buffer would spill
+                for (int cc = 0; cc < p.slice_n; cc += 32) {
+                    uint32_t v[32];
+                    __syncwarp();
+                    tmem_ld32(t_row + static_cast<uint32_t>(cc), v);
+                    tmem_ld_wait(v);
+                    if (lane == 0) bulk_wait_read_le1();  // the tile written two chunks ago is free
+                    __syncwarp();
+                    uint8_t* dst = stg + sbuf * kBkStoreTile;
+                    stage_row32<true>(v, p.pw_bias ? sm.pbi + co0 + cc : nullptr, p.pw_relu, dst, lane,
+                                      p.pw_scale ? sm.psc + co0 + cc : nullptr);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && rows_exist) {
+                        tma_store_4d(&y_map, dst, co0 + cc, t.wo0, h, t.n);
+                        bulk_commit();
                     }
+                    sbuf ^= 1;
                 }
                 tmem_ld_wait();
                 tc_fence_before();
@@ -454,10 +453,10 @@ __global__ void __launch_bounds__(kBkThreads, 1)
     }
 }
 
-int dwpw_block_smem_bytes(int C, int slice_n, int halo_stages, int b_stages) {
+int dwpw_block_smem_bytes(int C, int C_out, int slice_n, int halo_stages, int b_stages) {
     const int bars = (2 * halo_stages + 2 * b_stages + 2 * kBkMaxKblk + 5) * 8 + 16;
     return 1024 + (C / 64) * static_cast<int>(kBkKblkBytes) + b_stages * slice_n * 128 +
-           8 * 2 * static_cast<int>(kBkStoreTile) + halo_stages * kBkHaloBytes + C * 11 * 4 + bars;
+           8 * 2 * static_cast<int>(kBkStoreTile) + halo_stages * kBkHaloBytes + C * 11 * 4 + C_out * 2 * 4 + bars;
 }
 
 cudaError_t launch_dwpw_block(const CUtensorMap& x_map, const CUtensorMap& w_map, const CUtensorMap& y_map,
