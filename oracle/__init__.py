@@ -17,6 +17,10 @@ follows, is stated at the top of ``conv_oracle.c``:
   4.3, 6.2;
 * bias after the sum, then ReLU: lesson 9, section 31 (with its per-channel
   scale and shift, a folded batch norm: y = act(scale * sum + shift));
+* transposed convolution, the adjoint of the convolution (variants page,
+  sections 2.3 and 4.2: zero insertion between input pixels, then a stride-1
+  convolution; in matrix form the weight enters transposed), output extent
+  (H - 1)*S - 2P + D*(K - 1) + 1;
 * the depthwise-separable block, depthwise 3x3 then pointwise 1x1 (lesson 9,
   section 25), with its intermediate rounded to BF16 (``round_bf16``, the
   pointwise GEMM's operand type).
@@ -78,6 +82,12 @@ def _load():
         lib.oracle_conv2d_macs_at.argtypes = [P(_Desc), ctypes.c_void_p, ctypes.c_void_p,
                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
         lib.oracle_conv2d_macs_at.restype = ctypes.c_long
+        lib.oracle_out_size_transposed.argtypes = [ctypes.c_int] * 5
+        lib.oracle_out_size_transposed.restype = ctypes.c_int
+        lib.oracle_conv_transpose2d_f64.argtypes = lib.oracle_conv2d_f64.argtypes
+        lib.oracle_conv_transpose2d_f64.restype = ctypes.c_int
+        lib.oracle_conv_transpose2d_points_f64.argtypes = lib.oracle_conv2d_points_f64.argtypes
+        lib.oracle_conv_transpose2d_points_f64.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -218,3 +228,72 @@ def dwpw_block(x, w_dw, w_pw, padding=1, dw_scale=None, dw_bias=None, dw_relu=Fa
     if round_mid:
         mid = round_bf16(mid)
     return conv2d(mid, w_pw, pw_bias, 1, 0, 1, 1, pw_relu, nthreads=nthreads, scale=pw_scale)
+
+
+def out_size_transposed(size: int, k: int, s: int, p: int, d: int) -> int:
+    """Transposed-convolution output extent (size - 1)*s - 2p + d(k - 1) + 1, or 0 if not positive."""
+    return int(_load().oracle_out_size_transposed(size, k, s, p, d))
+
+
+def _tdesc(x, w, x_layout, w_layout, y_layout, stride, padding, dilation, groups, relu, y=None):
+    """Descriptor of a transposed convolution; w is logical [C_in][C_out/G][Kh][Kw]
+    ("IOHW", torch's ConvTranspose2d layout) or "IHWO" = [C_in][Kh][Kw][C_out/G]."""
+    xl = _ACT_LAYOUTS[x_layout]
+    N, C_in, H, W = _logical_shape(x, xl, "nchw")
+    wl = {"IOHW": "iohw", "IHWO": "ihwo"}[w_layout]
+    Cin_w, Cout_g, Kh, Kw = _logical_shape(w, wl, "iohw")
+    if Cin_w != C_in:
+        raise ValueError("weight input-channel extent %d != C_in %d" % (Cin_w, C_in))
+    d = _Desc()
+    d.N, d.C_in, d.H, d.W, d.C_out = N, C_in, H, W, Cout_g * groups
+    d.Kh, d.Kw, d.S, d.P, d.D, d.G = Kh, Kw, stride, padding, dilation, groups
+    d.relu = 1 if relu else 0
+    d.xs_n, d.xs_c, d.xs_h, d.xs_w = _strides(x, xl, "nchw")
+    d.ws_o, d.ws_i, d.ws_h, d.ws_w = _strides(w, wl, "iohw")
+    if y is not None:
+        d.ys_n, d.ys_c, d.ys_h, d.ys_w = _strides(y, _ACT_LAYOUTS[y_layout], "nchw")
+    return d
+
+
+def conv_transpose2d(x, w, bias=None, stride=1, padding=0, dilation=1, groups=1, relu=False,
+                     x_layout="NCHW", w_layout="IOHW", y_layout="NCHW", nthreads=0, scale=None):
+    """Full FP64 transposed convolution (scatter order).  x [N][C_in][H][W] (NCHW) or
+    NHWC; w [C_in][C_out/G][Kh][Kw] ("IOHW") or [C_in][Kh][Kw][C_out/G] ("IHWO");
+    optional per-channel scale, then bias, then ReLU."""
+    lib = _load()
+    x, w = _f64(x), _f64(w)
+    b = None if bias is None else _f64(bias)
+    sc = None if scale is None else _f64(scale)
+    d0 = _tdesc(x, w, x_layout, w_layout, y_layout, stride, padding, dilation, groups, relu)
+    Ho = out_size_transposed(d0.H, d0.Kh, stride, padding, dilation)
+    Wo = out_size_transposed(d0.W, d0.Kw, stride, padding, dilation)
+    if Ho <= 0 or Wo <= 0:
+        raise ValueError("empty output (H_out=%d, W_out=%d)" % (Ho, Wo))
+    shape = {"NCHW": (d0.N, d0.C_out, Ho, Wo), "NHWC": (d0.N, Ho, Wo, d0.C_out)}[y_layout]
+    y = np.empty(shape, dtype=np.float64)
+    d = _tdesc(x, w, x_layout, w_layout, y_layout, stride, padding, dilation, groups, relu, y)
+    rc = lib.oracle_conv_transpose2d_f64(ctypes.byref(d), x.ctypes.data, w.ctypes.data,
+                                         None if sc is None else sc.ctypes.data,
+                                         None if b is None else b.ctypes.data, y.ctypes.data, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected the transposed-convolution descriptor")
+    return y
+
+
+def conv_transpose2d_points(x, w, bias, pts, stride=1, padding=0, dilation=1, groups=1, relu=False,
+                            x_layout="NCHW", w_layout="IOHW", nthreads=0, scale=None):
+    """FP64 transposed-convolution values at (n, co, h, w) points, gather order."""
+    lib = _load()
+    x, w = _f64(x), _f64(w)
+    b = None if bias is None else _f64(bias)
+    sc = None if scale is None else _f64(scale)
+    pts = np.ascontiguousarray(pts, dtype=np.int64).reshape(-1, 4)
+    out = np.empty(pts.shape[0], dtype=np.float64)
+    d = _tdesc(x, w, x_layout, w_layout, "NCHW", stride, padding, dilation, groups, relu)
+    rc = lib.oracle_conv_transpose2d_points_f64(ctypes.byref(d), x.ctypes.data, w.ctypes.data,
+                                                None if sc is None else sc.ctypes.data,
+                                                None if b is None else b.ctypes.data, pts.ctypes.data,
+                                                pts.shape[0], out.ctypes.data, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected the descriptor or a point")
+    return out

@@ -171,6 +171,131 @@ long oracle_conv2d_macs_at(const oracle_conv_desc *c, const double *x, const dou
     return macs;
 }
 
+/* ------------------------------------------------------------------------
+ * Transposed convolution: the adjoint (matrix transpose) of the convolution
+ * with the same S, P, D, G.  "Convolution variants and their matrix
+ * operations" (lpnh.cn/news/2674933), sections 2.3 and 4.2: it upsamples, it
+ * is still a convolution, and in matrix form the weight matrix enters
+ * transposed (Y_col = W^T X); equivalently s-1 zeros are inserted between
+ * neighbouring input pixels before a stride-1 convolution.  Each input pixel
+ * (i, j) of channel ci = g*C_in/G + ci' adds x * w[ci][co'][kh][kw] to output
+ * (i*S + kh*D - P, j*S + kw*D - P) of channel co = g*C_out/G + co'; positions
+ * outside the output are dropped.  The weight is indexed [C_in][C_out/G][Kh][Kw]
+ * here: the desc's ws_o strides ci, ws_i strides co'.  Output extent
+ * (H - 1)*S - 2P + D*(Kh - 1) + 1 (section 6.2 says only that it differs from
+ * the convolution's; this is the adjoint's size, with no output padding).
+ * ------------------------------------------------------------------------ */
+int oracle_out_size_transposed(int in, int k, int s, int p, int d)
+{
+    if (in <= 0 || k <= 0 || s <= 0 || p < 0 || d <= 0) return 0;
+    long v = (long)(in - 1) * s - 2L * p + (long)d * (k - 1) + 1;
+    return v > 0 ? (int)v : 0;
+}
+
+/* Full output, scatter order (each input pixel stamps its weighted kernel). */
+int oracle_conv_transpose2d_f64(const oracle_conv_desc *c, const double *x, const double *w,
+                                const double *scale, const double *bias, double *y, int nthreads)
+{
+    if (check_desc(c)) return -1;
+    const int Ho = oracle_out_size_transposed(c->H, c->Kh, c->S, c->P, c->D);
+    const int Wo = oracle_out_size_transposed(c->W, c->Kw, c->S, c->P, c->D);
+    if (Ho <= 0 || Wo <= 0) return -1;
+    const int cin_g = c->C_in / c->G, cout_g = c->C_out / c->G;
+    const long total = (long)c->N * c->C_out;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long nc = 0; nc < total; ++nc) {
+        const int n = (int)(nc / c->C_out);
+        const int co = (int)(nc % c->C_out);
+        const int g = co / cout_g, cop = co % cout_g;
+        double *yp = y + n * c->ys_n + co * c->ys_c;
+        for (int h = 0; h < Ho; ++h)
+            for (int v = 0; v < Wo; ++v) yp[h * c->ys_h + v * c->ys_w] = 0.0;
+        for (int cp = 0; cp < cin_g; ++cp) {
+            const int ci = g * cin_g + cp;
+            for (int i = 0; i < c->H; ++i)
+                for (int j = 0; j < c->W; ++j) {
+                    const double xv = x[n * c->xs_n + ci * c->xs_c + i * c->xs_h + j * c->xs_w];
+                    for (int kh = 0; kh < c->Kh; ++kh) {
+                        const int h = i * c->S + kh * c->D - c->P;
+                        if (h < 0 || h >= Ho) continue;
+                        for (int kw = 0; kw < c->Kw; ++kw) {
+                            const int v = j * c->S + kw * c->D - c->P;
+                            if (v < 0 || v >= Wo) continue;
+                            yp[h * c->ys_h + v * c->ys_w] +=
+                                xv * w[ci * c->ws_o + cop * c->ws_i + kh * c->ws_h + kw * c->ws_w];
+                        }
+                    }
+                }
+        }
+        for (int h = 0; h < Ho; ++h)
+            for (int v = 0; v < Wo; ++v) {
+                double a = yp[h * c->ys_h + v * c->ys_w];
+                if (scale) a *= scale[co];
+                if (bias) a += bias[co];
+                if (c->relu && a < 0.0) a = 0.0;
+                yp[h * c->ys_h + v * c->ys_w] = a;
+            }
+    }
+    return 0;
+}
+
+/* Selected outputs, gather order: output (h, v) takes input row i = (h + P - kh*D)/S
+ * for every kh where that division is exact and i is inside the input (same for
+ * columns).  pts holds (n, co, h, v) quadruples. */
+int oracle_conv_transpose2d_points_f64(const oracle_conv_desc *c, const double *x, const double *w,
+                                       const double *scale, const double *bias, const int64_t *pts,
+                                       int64_t npts, double *out, int nthreads)
+{
+    if (check_desc(c)) return -1;
+    const int Ho = oracle_out_size_transposed(c->H, c->Kh, c->S, c->P, c->D);
+    const int Wo = oracle_out_size_transposed(c->W, c->Kw, c->S, c->P, c->D);
+    for (int64_t i = 0; i < npts; ++i) {
+        const int64_t *q = pts + 4 * i;
+        if (q[0] < 0 || q[0] >= c->N || q[1] < 0 || q[1] >= c->C_out ||
+            q[2] < 0 || q[2] >= Ho || q[3] < 0 || q[3] >= Wo) return -1;
+    }
+    const int cin_g = c->C_in / c->G, cout_g = c->C_out / c->G;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < npts; ++t) {
+        const int64_t *q = pts + 4 * t;
+        const int n = (int)q[0], co = (int)q[1], h = (int)q[2], v = (int)q[3];
+        const int g = co / cout_g, cop = co % cout_g;
+        double acc = 0.0;
+        for (int cp = 0; cp < cin_g; ++cp) {
+            const int ci = g * cin_g + cp;
+            for (int kh = 0; kh < c->Kh; ++kh) {
+                const int nh = h + c->P - kh * c->D;
+                if (nh < 0 || nh % c->S) continue;
+                const int i = nh / c->S;
+                if (i >= c->H) continue;
+                for (int kw = 0; kw < c->Kw; ++kw) {
+                    const int nv = v + c->P - kw * c->D;
+                    if (nv < 0 || nv % c->S) continue;
+                    const int j = nv / c->S;
+                    if (j >= c->W) continue;
+                    acc += x[n * c->xs_n + ci * c->xs_c + i * c->xs_h + j * c->xs_w] *
+                           w[ci * c->ws_o + cop * c->ws_i + kh * c->ws_h + kw * c->ws_w];
+                }
+            }
+        }
+        if (scale) acc *= scale[co];
+        if (bias) acc += bias[co];
+        if (c->relu && acc < 0.0) acc = 0.0;
+        out[t] = acc;
+    }
+    return 0;
+}
+
 /* Threads the OpenMP runtime would use (1 when built without OpenMP). */
 int oracle_max_threads(void)
 {

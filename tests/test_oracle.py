@@ -419,3 +419,114 @@ def test_block_stages_apply_in_order():
     assert y[0, 0, 1, 1] == 64 * -5.5 + 0.25
     # a corner sees 4 taps: 4 * 0.5 - 10 = -8
     assert y[0, 3, 0, 0] == 64 * -8.0 + 0.25
+
+
+# ----------------------------------------------------------------- transposed convolution
+def _adjoint_shapes():
+    rng = np.random.default_rng(21)
+    out = []
+    while len(out) < 40:
+        G = int(rng.choice([1, 1, 2]))
+        A, B = G * int(rng.integers(1, 4)), G * int(rng.integers(1, 4))
+        K, S, D = int(rng.choice([1, 2, 3, 4])), int(rng.choice([1, 2, 3])), int(rng.choice([1, 2]))
+        P = int(rng.integers(0, D * (K - 1) + 1))
+        Hy, Wy = int(rng.integers(1, 5)), int(rng.integers(1, 5))
+        H = (Hy - 1) * S - 2 * P + D * (K - 1) + 1
+        W = (Wy - 1) * S - 2 * P + D * (K - 1) + 1
+        if H >= 1 and W >= 1:
+            out.append((int(rng.integers(1, 3)), A, B, H, W, Hy, Wy, K, S, P, D, G))
+    return out
+
+
+@pytest.mark.parametrize("shape", _adjoint_shapes())
+def test_transposed_is_the_adjoint_of_the_convolution(shape):
+    """<conv(x), y> == <x, conv_transpose(y)> with the same weight array: the transposed
+    convolution is the convolution's matrix transpose (variants page, section 4.2)."""
+    N, A, B, H, W, Hy, Wy, K, S, P, D, G = shape
+    rng = np.random.default_rng(abs(hash(shape)) % 2**32)
+    w = rng.standard_normal((A, B // G, K, K))      # conv: [C_out=A][C_in/G]; transposed: [C_in=A][C_out/G]
+    x = rng.standard_normal((N, B, H, W))
+    y = rng.standard_normal((N, A, Hy, Wy))
+    cx = oracle.conv2d(x, w, None, S, P, D, G)
+    assert cx.shape == y.shape
+    ty = oracle.conv_transpose2d(y, w, None, S, P, D, G)
+    assert ty.shape == x.shape
+    lhs, rhs = float(np.sum(cx * y)), float(np.sum(x * ty))
+    assert abs(lhs - rhs) <= 1e-11 * (1 + abs(lhs)), (lhs, rhs)
+
+
+@pytest.mark.parametrize("K,S,P,D,G", [(3, 2, 1, 1, 1), (4, 2, 1, 1, 1), (2, 2, 0, 1, 2), (3, 3, 2, 1, 1),
+                                       (3, 2, 0, 2, 1), (5, 1, 2, 1, 1), (1, 2, 0, 1, 1)])
+def test_transposed_equals_zero_insertion_then_stride1_conv(K, S, P, D, G):
+    """The construction of the variants page, section 4.2: insert S-1 zeros between
+    neighbouring input pixels, pad by D(K-1)-P, run a stride-1 convolution with the
+    kernel flipped and its in/out channel roles swapped."""
+    rng = np.random.default_rng(22 + K + S)
+    C_in, C_out, H, W = 2 * G, 3 * G, 4, 5
+    x = rng.standard_normal((2, C_in, H, W))
+    w = rng.standard_normal((C_in, C_out // G, K, K))
+    b = rng.standard_normal(C_out)
+    y = oracle.conv_transpose2d(x, w, b, S, P, D, G)
+    z = np.zeros((2, C_in, (H - 1) * S + 1, (W - 1) * S + 1))
+    z[:, :, ::S, ::S] = x
+    cin_g, cout_g = C_in // G, C_out // G
+    wf = np.zeros((C_out, cin_g, K, K))
+    for g in range(G):
+        for co in range(cout_g):
+            for ci in range(cin_g):
+                wf[g * cout_g + co, ci] = w[g * cin_g + ci, co, ::-1, ::-1]
+    ref = oracle.conv2d(z, wf, b, 1, D * (K - 1) - P, D, G)
+    assert y.shape == ref.shape
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_transposed_stride_equals_kernel_stamps_blocks():
+    """K = S = 2, P = 0: every input pixel stamps a copy of the kernel scaled by its value
+    into its own 2x2 output block (no overlap)."""
+    x = np.array([[[[1.0, 2.0], [3.0, 4.0]]]])
+    w = np.array([[[[1.0, 10.0], [100.0, 1000.0]]]])
+    y = oracle.conv_transpose2d(x, w, None, 2, 0)[0, 0]
+    ref = np.block([[1 * w[0, 0], 2 * w[0, 0]], [3 * w[0, 0], 4 * w[0, 0]]])
+    assert np.array_equal(y, ref)
+    # K = 3, S = 2: neighbouring stamps overlap on one shared row / column and add
+    w3 = np.ones((1, 1, 3, 3))
+    y3 = oracle.conv_transpose2d(np.ones((1, 1, 2, 2)), w3, None, 2, 0)[0, 0]
+    assert y3.shape == (5, 5)
+    assert y3[2, 2] == 4.0 and y3[0, 2] == 2.0 and y3[2, 0] == 2.0 and y3[0, 0] == 1.0
+
+
+def test_transposed_points_match_full_output():
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal((2, 4, 6, 5))
+    w = rng.standard_normal((4, 3, 4, 4))
+    b = rng.standard_normal(6)
+    full = oracle.conv_transpose2d(x, w, b, 2, 1, 1, 2, True)
+    pts = np.stack([rng.integers(0, 2, 300), rng.integers(0, 6, 300), rng.integers(0, full.shape[2], 300),
+                    rng.integers(0, full.shape[3], 300)], 1)
+    got = oracle.conv_transpose2d_points(x, w, b, pts, 2, 1, 1, 2, True)
+    ref = full[pts[:, 0], pts[:, 1], pts[:, 2], pts[:, 3]]
+    assert np.allclose(got, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_transposed_matches_torch_and_size_formula():
+    rng = np.random.default_rng(24)
+    for _ in range(60):
+        G = int(rng.choice([1, 2]))
+        C_in, C_out = G * int(rng.integers(1, 4)), G * int(rng.integers(1, 4))
+        K, S, D = int(rng.choice([1, 2, 3, 4])), int(rng.choice([1, 2, 3])), int(rng.choice([1, 2]))
+        P = int(rng.integers(0, 3))
+        H, W = int(rng.integers(1, 7)), int(rng.integers(1, 7))
+        Ho = (H - 1) * S - 2 * P + D * (K - 1) + 1
+        Wo = (W - 1) * S - 2 * P + D * (K - 1) + 1
+        assert oracle.out_size_transposed(H, K, S, P, D) == max(Ho, 0)
+        if Ho < 1 or Wo < 1:
+            continue
+        x = rng.standard_normal((2, C_in, H, W))
+        w = rng.standard_normal((C_in, C_out // G, K, K))
+        b = rng.standard_normal(C_out)
+        y = oracle.conv_transpose2d(x, w, b, S, P, D, G)
+        t = torch.nn.functional.conv_transpose2d(torch.from_numpy(x), torch.from_numpy(w), torch.from_numpy(b),
+                                                 S, P, 0, G, D).numpy()
+        assert y.shape == t.shape and np.allclose(y, t, rtol=1e-12, atol=1e-12)
+    # the upsampling layer the pages describe: 56 -> 112 with K = 4, S = 2, P = 1
+    assert oracle.out_size_transposed(56, 4, 2, 1, 1) == 112
