@@ -29,7 +29,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from workloads import WORKLOADS, b_device, inputs, w_device, x_device  # noqa: E402
+from workloads import WORKLOADS, b_device, inputs, w_device, w_device_transposed, x_device  # noqa: E402
 
 L2_FLUSH_BYTES = 256 << 20   # twice the 129 MB L2
 
@@ -66,6 +66,7 @@ KERNEL_SOURCES = {
     "body": ["tc_gemm.cu", "tc_common.cuh", "ptx.cuh", "conv_internal.h"],
     "pw": ["tc_gemm.cu", "tc_common.cuh", "ptx.cuh", "conv_internal.h"],
     "dilated": ["tc_gemm.cu", "tc_common.cuh", "ptx.cuh", "conv_internal.h"],
+    "upsample": ["tc_gemm.cu", "tc_common.cuh", "ptx.cuh", "conv_internal.h"],
     "stem": ["tc_smallk.cu", "tc_common.cuh", "ptx.cuh", "conv_internal.h"],
     "dw": ["depthwise.cu", "ptx.cuh", "conv_internal.h"],
     "tiny_f32": ["direct.cu", "conv_internal.h"],
@@ -229,7 +230,8 @@ def gpu_layer(name):
     from cnn_convolution_implicit_gb300 import ConvPlan
     s, x, w, b = inputs(name)
     plan = ConvPlan.for_shape(s)
-    xd, wd = x_device(x, s.dtype), w_device(w, s.dtype)
+    xd = x_device(x, s.dtype)
+    wd = w_device_transposed(w, s.dtype, s.G) if s.transposed else w_device(w, s.dtype)
     bd = b_device(b) if s.bias else None
     y = plan.empty_output()
     return s, plan, (x, w, b), (xd, wd, bd, y)
@@ -460,7 +462,7 @@ def main():
 
     # ---- the other layers of the metric (depthwise GB/s first)
     others = {}
-    for name in ("dw", "stem", "pw", "dilated"):
+    for name in ("dw", "stem", "pw", "dilated", "upsample"):
         r, _ = measure_layer(name, max(10, args.steps // 2), args.warmup, flush, peaks)
         others[name] = r
     r, _ = measure_layer("body", max(10, args.steps // 2), args.warmup, flush, peaks, affine=True)

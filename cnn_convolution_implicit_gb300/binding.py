@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libconv.so")
 
 CONV_F32, CONV_BF16 = 0, 1
-CONV_FLAG_BIAS, CONV_FLAG_RELU, CONV_FLAG_OUT_BF16, CONV_FLAG_SM_PAIRS = 1, 2, 4, 8
+CONV_FLAG_BIAS, CONV_FLAG_RELU, CONV_FLAG_OUT_BF16, CONV_FLAG_SM_PAIRS, CONV_FLAG_TRANSPOSED = 1, 2, 4, 8, 16
 STATUS = {0: "CONV_OK", 1: "CONV_ERR_INVALID_ARG", 2: "CONV_ERR_UNSUPPORTED", 3: "CONV_ERR_MISALIGNED",
           4: "CONV_ERR_CUDA", 5: "CONV_ERR_NO_MEMORY", 6: "CONV_ERR_TIMEOUT"}
 PATHS = {0: "direct", 1: "depthwise", 2: "gemm_1x1", 3: "implicit_gemm", 4: "small_k_gemm"}
@@ -104,15 +104,18 @@ class ConvPlan:
 
     Tensors are NHWC activations [N][H][W][C], weights [C_out][Kh][Kw][C_in/G]
     and an FP32 bias [C_out].  dtype "bf16": BF16 x, w, y.  dtype "f32": FP32
-    x, w and FP32 y (BF16 y with out_bf16=True).
+    x, w and FP32 y (BF16 y with out_bf16=True).  transposed=True plans the
+    transposed convolution (the adjoint of the convolution with the same S, P,
+    D, G; output (H - 1)*S - 2P + D(Kh - 1) + 1 rows), same weight layout.
     """
 
     def __init__(self, N, C_in, H, W, C_out, Kh, Kw, S=1, P=0, D=1, G=1, dtype="bf16",
-                 bias=True, relu=False, out_bf16=False, sm_pairs=False):
+                 bias=True, relu=False, out_bf16=False, sm_pairs=False, transposed=False):
         L = lib()
         self._plan = None
         flags = (CONV_FLAG_BIAS if bias else 0) | (CONV_FLAG_RELU if relu else 0) | \
-                (CONV_FLAG_OUT_BF16 if out_bf16 else 0) | (CONV_FLAG_SM_PAIRS if sm_pairs else 0)
+                (CONV_FLAG_OUT_BF16 if out_bf16 else 0) | (CONV_FLAG_SM_PAIRS if sm_pairs else 0) | \
+                (CONV_FLAG_TRANSPOSED if transposed else 0)
         dt = {"bf16": CONV_BF16, "f32": CONV_F32}[dtype]
         h = ctypes.c_void_p()
         st = L.conv_plan_create(ctypes.byref(h), N, C_in, H, W, C_out, Kh, Kw, S, P, D, G, dt, flags)
@@ -121,6 +124,7 @@ class ConvPlan:
         self._plan = h
         self.shape = (N, C_in, H, W, C_out, Kh, Kw, S, P, D, G)
         self.dtype, self.bias, self.relu, self.out_bf16 = dtype, bias, relu, out_bf16
+        self.transposed = transposed
         ho, wo = ctypes.c_int(), ctypes.c_int()
         L.conv_plan_output_shape(h, ctypes.byref(ho), ctypes.byref(wo))
         self.H_out, self.W_out = ho.value, wo.value
@@ -137,7 +141,7 @@ class ConvPlan:
     def for_shape(cls, s, sm_pairs=False):
         """Plan from a workloads.ConvShape-like object."""
         return cls(s.N, s.C_in, s.H, s.W, s.C_out, s.Kh, s.Kw, s.S, s.P, s.D, s.G, s.dtype,
-                   s.bias, s.relu, s.out_bf16, sm_pairs)
+                   s.bias, s.relu, s.out_bf16, sm_pairs, getattr(s, "transposed", False))
 
     def close(self):
         if self._plan is not None and _lib is not None:

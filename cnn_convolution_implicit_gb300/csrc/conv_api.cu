@@ -14,6 +14,7 @@
 //   BF16, 1x1, S=1, P=0, G=1, aligned      -> tcgen05 GEMM with tiled TMA
 //   BF16, (C_in/G) % 64 == 0, aligned      -> tcgen05 implicit GEMM, TMA im2col
 //   BF16, G=1, C_in*Kh*Kw <= 64            -> tcgen05 small-K kernel (stem)
+//   BF16 transposed, aligned, S | H_out    -> tcgen05 implicit GEMM, phase mode
 //   anything else                          -> direct CUDA-core kernel
 #include <mutex>
 #include <new>
@@ -85,6 +86,12 @@ int out_extent(int in, int k, int s, int p, int d) {
     return static_cast<int>(num / s + 1);
 }
 
+// Transposed convolution: (in - 1)*s - 2p + d(k - 1) + 1, or 0 when not positive.
+int out_extent_transposed(int in, int k, int s, int p, int d) {
+    const long long v = static_cast<long long>(in - 1) * s - 2LL * p + static_cast<long long>(d) * (k - 1) + 1;
+    return v > 0 && v <= 0x7fffffffLL ? static_cast<int>(v) : 0;
+}
+
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
 int pow2_at_least(int v) {
@@ -93,8 +100,29 @@ int pow2_at_least(int v) {
     return r;
 }
 
+// Taps of one axis of a transposed convolution, per output phase residue r:
+// kernel index k with (r + P - k*D) divisible by S, input offset (r + P - k*D)/S.
+// False if a residue has no tap or an offset does not fit the table.
+bool phase_axis(int K, int S, int P, int D, TcPhaseAxis& a) {
+    for (int r = 0; r < S; ++r) {
+        int n = 0;
+        for (int k = 0; k < K; ++k) {
+            const int num = r + P - k * D;
+            if (((num % S) + S) % S != 0) continue;
+            const int off = num / S;
+            if (off < -128 || off > 127 || n >= kTcMaxPhaseTaps) return false;
+            a.k[r][n] = static_cast<int8_t>(k);
+            a.off[r][n] = static_cast<int8_t>(off);
+            ++n;
+        }
+        if (n == 0) return false;
+        a.cnt[r] = static_cast<int8_t>(n);
+    }
+    return true;
+}
+
 // tcgen05 GEMM configuration; false when the shape does not fit it.
-bool configure_tc(conv_plan* pl, bool one_by_one) {
+bool configure_tc(conv_plan* pl, bool one_by_one, bool transposed = false) {
     const ConvGeom& g = pl->g;
     TcGemmParams& t = pl->tc;
     if (g.cin_g % kTcBlockK != 0) return false;
@@ -122,7 +150,15 @@ bool configure_tc(conv_plan* pl, bool one_by_one) {
         if (gpc == 0) return false;
         n_tile = gpc * g.cout_g;
     }
-    if (!one_by_one) {
+    if (transposed) {
+        // phase mode: S x S output phases, each a stride-1 gather over the input
+        if (g.S > kTcMaxPhaseStride || g.Kh > kTcMaxPhaseTaps || g.Kw > kTcMaxPhaseTaps) return false;
+        if (g.H_out % g.S != 0 || g.W_out % g.S != 0) return false;
+        if (!phase_axis(g.Kh, g.S, g.P, g.D, t.ph) || !phase_axis(g.Kw, g.S, g.P, g.D, t.pw)) return false;
+        t.ps = g.S;
+        t.hq = g.H_out / g.S;
+        t.wq = g.W_out / g.S;
+    } else if (!one_by_one) {
         // im2col bounding box corners must fit the 4-D map's signed 8-bit range
         const int lo = -g.P;
         const int up_w = g.P - (g.Kw - 1) * g.D, up_h = g.P - (g.Kh - 1) * g.D;
@@ -132,30 +168,37 @@ bool configure_tc(conv_plan* pl, bool one_by_one) {
     }
     if (g.pixels > 0x7fffffffLL) return false;
     t.g = g;
-    t.mode = one_by_one ? kTcMode1x1 : (g.S == 1 ? kTcModeRect : kTcModeIm2col);
+    t.mode = transposed ? kTcModePhase : one_by_one ? kTcMode1x1 : (g.S == 1 ? kTcModeRect : kTcModeIm2col);
     t.n_tile = n_tile;
     t.mma_n = mma_n;
     t.gpc = gpc;
     t.kblk = g.cin_g / kTcBlockK;
     t.ksteps = g.Kh * g.Kw * t.kblk;
-    if (t.mode == kTcModeRect) {
-        // 128-pixel rectangle, 8 / 16 / 32 wide: the one that pads the image least
-        // (ties go to 16 x 8).  A warp's 32 TMEM lanes are 32/TW whole rows of it.
+    if (t.mode == kTcModeRect || t.mode == kTcModePhase) {
+        // 128-pixel rectangle (of the output, or of one phase's output grid), 8 /
+        // 16 / 32 wide: the one that pads least (ties go to 16 x 8).  A warp's 32
+        // TMEM lanes are 32/TW whole rows of it; in phase mode a warp's rows must
+        // not cross the end of the phase grid (its store view runs on into the
+        // next image), so the grid height must be a multiple of 32/TW.
+        const bool phase = t.mode == kTcModePhase;
+        const int eh = phase ? t.hq : g.H_out, ew = phase ? t.wq : g.W_out;
         auto padded = [](int extent, int t) { return static_cast<long long>((extent + t - 1) / t) * t; };
-        int best = 16;
-        long long best_area = padded(g.W_out, 16) * padded(g.H_out, 8);
-        for (int tw : {8, 32}) {
-            const long long area = padded(g.W_out, tw) * padded(g.H_out, kTcBlockM / tw);
-            if (area < best_area) {
+        int best = 0;
+        long long best_area = 0;
+        for (int tw : {16, 8, 32}) {
+            if (phase && eh % (32 / tw) != 0) continue;
+            const long long area = padded(ew, tw) * padded(eh, kTcBlockM / tw);
+            if (best == 0 || area < best_area) {
                 best = tw;
                 best_area = area;
             }
         }
         t.rect_w = best;
         t.rect_h = kTcBlockM / best;
-        t.rect_tiles_w = (g.W_out + t.rect_w - 1) / t.rect_w;
-        t.rect_tiles_h = (g.H_out + t.rect_h - 1) / t.rect_h;
-        const long long m_tiles = static_cast<long long>(g.N) * t.rect_tiles_w * t.rect_tiles_h;
+        t.rect_tiles_w = (ew + t.rect_w - 1) / t.rect_w;
+        t.rect_tiles_h = (eh + t.rect_h - 1) / t.rect_h;
+        const long long m_tiles =
+            static_cast<long long>(g.N) * t.rect_tiles_w * t.rect_tiles_h * (phase ? t.ps * t.ps : 1);
         if (m_tiles > 0x3fffffffLL) return false;
         t.num_m_tiles = static_cast<int>(m_tiles);
     } else {
@@ -167,7 +210,7 @@ bool configure_tc(conv_plan* pl, bool one_by_one) {
     t.ychunk = 32;
     // SM pairs (one MMA over 2 x 128 pixels, weight rows split between the two
     // CTAs) on request, when there are at least two pixel tiles to pair up.
-    t.pair = (t.num_m_tiles >= 2 && (pl->flags & CONV_FLAG_SM_PAIRS)) ? 1 : 0;
+    t.pair = (t.num_m_tiles >= 2 && (pl->flags & CONV_FLAG_SM_PAIRS) && !transposed) ? 1 : 0;
     const int b_rows = t.pair ? mma_n / 2 : mma_n;
     const int stage_bytes = kTcBlockM * kTcBlockK * 2 + b_rows * 128;
     const int fixed = 1024 + 256 + 8 * 2 * 32 * 64;  // alignment, barriers, epilogue store tiles
@@ -258,6 +301,21 @@ CUresult encode_y_map(conv_plan* pl, void* y) {
     }
     const TcGemmParams& t = pl->tc;
     const CUtensorMapSwizzle sw = t.ychunk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (t.mode == kTcModePhase) {
+        // y viewed as {C_out, S (column phase), W_out/S, S (row phase), N*H_out/S}: one
+        // box is 32 channels x TW pixels of one phase x 32/TW phase rows
+        const cuuint64_t S = static_cast<cuuint64_t>(t.ps), Co = static_cast<cuuint64_t>(g.C_out);
+        const cuuint32_t box[5] = {static_cast<cuuint32_t>(t.ychunk), 1, static_cast<cuuint32_t>(t.rect_w), 1,
+                                   static_cast<cuuint32_t>(32 / t.rect_w)};
+        const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+        const cuuint64_t dims[5] = {Co, S, static_cast<cuuint64_t>(t.wq), S,
+                                    static_cast<cuuint64_t>(g.N) * static_cast<cuuint64_t>(t.hq)};
+        const cuuint64_t strides[4] = {Co * 2, S * Co * 2, static_cast<cuuint64_t>(g.W_out) * Co * 2,
+                                       S * static_cast<cuuint64_t>(g.W_out) * Co * 2};
+        return g_encode_tiled(&pl->map_y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, y, dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (t.mode == kTcModeRect) {  // {C_out, W_out, H_out, N}: 32/TW rows of TW pixels per store
         const cuuint32_t box[4] = {static_cast<cuuint32_t>(t.ychunk), static_cast<cuuint32_t>(t.rect_w),
                                    static_cast<cuuint32_t>(32 / t.rect_w), 1};
@@ -295,7 +353,7 @@ conv_status encode_maps(conv_plan* pl, const void* x, const void* w, void* y) {
             r = g_encode_tiled(&pl->map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides,
                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        } else if (pl->tc.mode == kTcModeRect) {
+        } else if (pl->tc.mode == kTcModeRect || pl->tc.mode == kTcModePhase) {
             const cuuint64_t dims[4] = {static_cast<cuuint64_t>(g.C_in), static_cast<cuuint64_t>(g.W),
                                         static_cast<cuuint64_t>(g.H), static_cast<cuuint64_t>(g.N)};
             const cuuint64_t strides[3] = {static_cast<cuuint64_t>(g.C_in) * 2,
@@ -385,10 +443,12 @@ conv_status conv_plan_create(conv_plan** out, int N, int C_in, int H, int W, int
         return CONV_ERR_INVALID_ARG;
     if (C_in % G != 0 || C_out % G != 0) return CONV_ERR_INVALID_ARG;
     if (dtype != CONV_F32 && dtype != CONV_BF16) return CONV_ERR_INVALID_ARG;
-    if (flags & ~(CONV_FLAG_BIAS | CONV_FLAG_RELU | CONV_FLAG_OUT_BF16 | CONV_FLAG_SM_PAIRS))
+    if (flags & ~(CONV_FLAG_BIAS | CONV_FLAG_RELU | CONV_FLAG_OUT_BF16 | CONV_FLAG_SM_PAIRS | CONV_FLAG_TRANSPOSED))
         return CONV_ERR_INVALID_ARG;
     if ((flags & CONV_FLAG_OUT_BF16) && dtype != CONV_F32) return CONV_ERR_INVALID_ARG;
-    const int Ho = out_extent(H, Kh, S, P, D), Wo = out_extent(W, Kw, S, P, D);
+    const bool transposed = (flags & CONV_FLAG_TRANSPOSED) != 0;
+    const int Ho = transposed ? out_extent_transposed(H, Kh, S, P, D) : out_extent(H, Kh, S, P, D);
+    const int Wo = transposed ? out_extent_transposed(W, Kw, S, P, D) : out_extent(W, Kw, S, P, D);
     if (Ho < 1 || Wo < 1) return CONV_ERR_INVALID_ARG;
 
     conv_plan* pl = new (std::nothrow) conv_plan();
@@ -428,7 +488,9 @@ conv_status conv_plan_create(conv_plan** out, int N, int C_in, int H, int W, int
 
     pl->path = CONV_PATH_DIRECT;
     pl->pair_clusters = 0;
-    if (dtype == CONV_F32) {
+    if (transposed) {
+        if (dtype == CONV_BF16 && configure_tc(pl, false, true)) pl->path = CONV_PATH_IMPLICIT_GEMM;
+    } else if (dtype == CONV_F32) {
         if (configure_depthwise(pl)) pl->path = CONV_PATH_DEPTHWISE;
     } else {
         const bool pointwise = Kh == 1 && Kw == 1 && S == 1 && P == 0 && G == 1;
@@ -456,6 +518,12 @@ conv_status conv_plan_output_shape(const conv_plan* p, int* H_out, int* W_out) {
 conv_status conv_plan_info(const conv_plan* p, int* path, long long* gemm_m, long long* gemm_n, long long* gemm_k) {
     if (p == nullptr) return CONV_ERR_INVALID_ARG;
     if (path) *path = p->path;
+    if (p->flags & CONV_FLAG_TRANSPOSED) {  // Y_col = W^T X
+        if (gemm_m) *gemm_m = static_cast<long long>(p->g.C_out) * p->g.Kh * p->g.Kw;
+        if (gemm_n) *gemm_n = static_cast<long long>(p->g.N) * p->g.H * p->g.W;
+        if (gemm_k) *gemm_k = p->g.cin_g;
+        return CONV_OK;
+    }
     if (gemm_m) *gemm_m = p->g.C_out;
     if (gemm_n) *gemm_n = p->g.pixels;
     if (gemm_k) *gemm_k = static_cast<long long>(p->g.cin_g) * p->g.Kh * p->g.Kw;
@@ -593,6 +661,7 @@ conv_status forward_impl(conv_plan* p, const void* x, const void* w, const float
             d.relu = (p->flags & CONV_FLAG_RELU) ? 1 : 0;
             d.in_bf16 = p->dtype == CONV_BF16 ? 1 : 0;
             d.out_bf16 = (p->dtype == CONV_BF16 || (p->flags & CONV_FLAG_OUT_BF16)) ? 1 : 0;
+            d.transposed = (p->flags & CONV_FLAG_TRANSPOSED) ? 1 : 0;
             e = launch_direct(d, st);
             break;
         }

@@ -41,8 +41,9 @@ struct DirectParams {
     const float* scale;  // nullptr when no per-channel scale
     void* y;
     int relu;
-    int in_bf16;   // x, w are BF16 (else FP32)
-    int out_bf16;  // y is BF16 (else FP32)
+    int in_bf16;     // x, w are BF16 (else FP32)
+    int out_bf16;    // y is BF16 (else FP32)
+    int transposed;  // transposed convolution (gather form): x is the H x W input, y the H_out x W_out output
 };
 cudaError_t launch_direct(const DirectParams& p, cudaStream_t stream);
 
@@ -74,7 +75,19 @@ constexpr int kTcBlockK = 64;     // BF16 elements per K-step (one 128-byte swiz
 constexpr int kTcThreads = 320;   // producer warp, MMA warp, 2 x 4 epilogue warps
 constexpr int kTcMaxGroupsPerTile = 8;  // groups packed side by side in one accumulator (<= ring stages)
 
-enum TcMode { kTcMode1x1 = 0, kTcModeIm2col = 1, kTcModeRect = 2 };
+enum TcMode { kTcMode1x1 = 0, kTcModeIm2col = 1, kTcModeRect = 2, kTcModePhase = 3 };
+
+// Transposed convolution (kTcModePhase, any stride S): output pixels split into
+// S x S phases by (h mod S, w mod S); phase residue r of one axis uses the kernel
+// taps k with (r + P - k*D) divisible by S, reading input row (q + off) for phase
+// row q, off = (r + P - k*D) / S.
+constexpr int kTcMaxPhaseStride = 4;
+constexpr int kTcMaxPhaseTaps = 8;
+struct TcPhaseAxis {
+    int8_t cnt[kTcMaxPhaseStride];                    // taps per residue
+    int8_t k[kTcMaxPhaseStride][kTcMaxPhaseTaps];     // kernel index of each tap
+    int8_t off[kTcMaxPhaseStride][kTcMaxPhaseTaps];   // input offset of each tap
+};
 
 struct TcGemmParams {
     ConvGeom g;
@@ -92,16 +105,21 @@ struct TcGemmParams {
     int tmem_cols;     // power of two >= 2 * n_tile
     int smem_bytes;
     int pair;          // 1: CTA-pair kernel (B rows split across the two CTAs)
+    int ps;            // kTcModePhase: the transposed convolution's stride S (phases = S*S)
+    int hq, wq;        // kTcModePhase: output rows / columns per phase (H_out / S, W_out / S)
+    TcPhaseAxis ph, pw;
     int relu;
     const float* bias;
     const float* scale;  // nullptr when no per-channel scale
     __nv_bfloat16* y;
     unsigned* status;
 };
-// a_map: rect mode 4-D tiled {C_in, W, H, N} box {64, rect_w, rect_h, 1}; im2col
+// a_map: rect and phase modes 4-D tiled {C_in, W, H, N} box {64, rect_w, rect_h, 1}; im2col
 // mode 4-D im2col; 1x1 mode 2-D {C_in, pixels} box {64, 128}; all 128-byte swizzle.
 // y_map: rect mode 4-D {C_out, W_out, H_out, N} box {32, rect_w, 32/rect_w, 1},
-// else 2-D {C_out, pixels} box {32, 32}; 64-byte swizzle.  p.pair selects the
+// phase mode 5-D {C_out, S, W_out/S, S, N*H_out/S} box {32, 1, rect_w, 1, 32/rect_w}
+// (one phase's pixels of 32/rect_w rows), else 2-D {C_out, pixels} box {32, 32};
+// 64-byte swizzle.  p.pair selects the
 // CTA-pair kernel (grid even, clusters of 2).
 cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, const CUtensorMap& y_map,
                            const TcGemmParams& p, int grid, cudaStream_t stream);

@@ -8,6 +8,13 @@
 // (odd channel counts, groups not aligned to the MMA tile, BF16 with
 // C_out % 16 != 0, ...).  Threads are ordered with the output channel fastest
 // so a warp writes a contiguous NHWC run and reads the same input pixels.
+//
+// Transposed convolution ("Convolution variants and their matrix operations",
+// lpnh.cn/news/2674933, sections 2.3 and 4.2: the adjoint of the convolution,
+// each input pixel (i, j) contributing to output (i*S + kh*D - P,
+// j*S + kw*D - P)) runs here in gather form: output (ho, wo) takes input row
+// i = (ho + P - kh*D) / S for every kernel row kh where the division is exact
+// and i is inside the input, likewise for columns.
 #include "conv_internal.h"
 #include "ptx.cuh"
 
@@ -42,7 +49,22 @@ __global__ void __launch_bounds__(256) direct_kernel(const DirectParams p) {
         const int grp = co / g.cout_g;
         const Tin* wco = w + static_cast<long long>(co) * g.Kh * g.Kw * g.cin_g;
         float acc = 0.f;
-        for (int kh = 0; kh < g.Kh; ++kh) {
+        if (p.transposed) {
+            for (int kh = 0; kh < g.Kh; ++kh) {
+                const int nh = ho + g.P - kh * g.D;
+                if (nh < 0 || nh % g.S != 0 || nh / g.S >= g.H) continue;
+                const int hi = nh / g.S;
+                for (int kw = 0; kw < g.Kw; ++kw) {
+                    const int nw = wo + g.P - kw * g.D;
+                    if (nw < 0 || nw % g.S != 0 || nw / g.S >= g.W) continue;
+                    const int wi = nw / g.S;
+                    const Tin* xp = x + ((static_cast<long long>(n) * g.H + hi) * g.W + wi) * g.C_in + grp * g.cin_g;
+                    const Tin* wp = wco + (kh * g.Kw + kw) * g.cin_g;
+                    for (int ci = 0; ci < g.cin_g; ++ci) acc = fmaf(to_f32(xp[ci]), to_f32(wp[ci]), acc);
+                }
+            }
+        }
+        for (int kh = 0; kh < g.Kh && !p.transposed; ++kh) {
             const int hi = ho * g.S + kh * g.D - g.P;
             if (hi < 0 || hi >= g.H) continue;
             for (int kw = 0; kw < g.Kw; ++kw) {

@@ -95,13 +95,29 @@ __device__ __forceinline__ void sub_gemm(const TcGemmParams& p, int nt, int j, i
 struct PixTile {
     long long pix0;
     int n, ho0, wo0;
+    int rh, rw;   // phase mode: the tile's output phase (h mod S, w mod S); ho0, wo0 are phase-grid coordinates
     bool exists;  // m is a real tile (the pair kernel may run one past the end)
 };
 
+template <bool PHASE>
 __device__ __forceinline__ PixTile pix_tile(const TcGemmParams& p, int m) {
     PixTile t;
     t.exists = m < p.num_m_tiles;
-    if (p.mode == kTcModeRect) {
+    t.rh = t.rw = 0;
+    if constexpr (PHASE) {  // phases fastest: neighbouring tiles read the same input rectangle
+        const int nph = p.ps * p.ps;
+        const int ph = m % nph;
+        t.rh = ph / p.ps;
+        t.rw = ph - t.rh * p.ps;
+        const int per_img = p.rect_tiles_h * p.rect_tiles_w;
+        const int q = m / nph;
+        t.n = q / per_img;
+        const int r = q - t.n * per_img;
+        const int th = r / p.rect_tiles_w;
+        t.ho0 = th * p.rect_h;
+        t.wo0 = (r - th * p.rect_tiles_w) * p.rect_w;
+        t.pix0 = 0;
+    } else if (p.mode == kTcModeRect) {
         const int per_img = p.rect_tiles_h * p.rect_tiles_w;
         t.n = m / per_img;
         const int r = m - t.n * per_img;
@@ -120,17 +136,53 @@ __device__ __forceinline__ PixTile pix_tile(const TcGemmParams& p, int m) {
     return t;
 }
 
+// K-steps of one sub-GEMM of a tile: taps x 64-channel blocks (phase mode: the
+// taps of the tile's phase only).
+template <bool PHASE>
+__device__ __forceinline__ int tile_ksteps(const TcGemmParams& p, int rh, int rw) {
+    if constexpr (PHASE) return p.ph.cnt[rh] * p.pw.cnt[rw] * p.kblk;
+    return p.ksteps;
+}
+
+// Tap `tap` of a tile: kernel indices, input offsets (rect / phase modes) and
+// the weight tap it multiplies.
+struct Tap {
+    int kh, kw, dh, dw, wtap;
+};
+
+template <bool PHASE>
+__device__ __forceinline__ Tap tile_tap(const TcGemmParams& p, const PixTile& t, int tap) {
+    Tap r;
+    if constexpr (PHASE) {
+        const int cw = p.pw.cnt[t.rw];
+        const int a = tap / cw, b = tap - a * cw;
+        r.kh = p.ph.k[t.rh][a];
+        r.kw = p.pw.k[t.rw][b];
+        r.dh = p.ph.off[t.rh][a];
+        r.dw = p.pw.off[t.rw][b];
+        r.wtap = r.kh * p.g.Kw + r.kw;
+    } else {
+        r.kh = tap / p.g.Kw;
+        r.kw = tap - r.kh * p.g.Kw;
+        r.dh = r.kh * p.g.D - p.g.P;
+        r.dw = r.kw * p.g.D - p.g.P;
+        r.wtap = tap;
+    }
+    return r;
+}
+
 // A operand of one K-step: 128 pixels x 64 channels of tap (kh, kw).
-template <bool PAIR>
+template <bool PAIR, bool PHASE>
 __device__ __forceinline__ void load_a(const TcGemmParams& p, const CUtensorMap* map, uint8_t* dst, uint64_t* bar,
-                                       uint32_t bar_cluster, const PixTile& t, int c, int kh, int kw) {
-    if (p.mode == kTcMode1x1) {
+                                       uint32_t bar_cluster, const PixTile& t, int c, const Tap& tp) {
+    const int kh = tp.kh, kw = tp.kw;
+    if (!PHASE && p.mode == kTcMode1x1) {
         if constexpr (PAIR)
             tma_load_2d_pair(dst, map, bar_cluster, c, static_cast<int>(t.pix0));
         else
             tma_load_2d(dst, map, bar, c, static_cast<int>(t.pix0));
-    } else if (p.mode == kTcModeRect) {
-        const int w = t.wo0 + kw * p.g.D - p.g.P, h = t.ho0 + kh * p.g.D - p.g.P;
+    } else if (PHASE || p.mode == kTcModeRect) {
+        const int w = t.wo0 + tp.dw, h = t.ho0 + tp.dh;
         if constexpr (PAIR)
             tma_load_4d_pair(dst, map, bar_cluster, c, w, h, t.n);
         else
@@ -147,7 +199,9 @@ __device__ __forceinline__ void load_a(const TcGemmParams& p, const CUtensorMap*
 
 }  // namespace
 
-template <bool PAIR>
+// PHASE: the transposed-convolution phase mode (kTcModePhase), compiled
+// separately so the convolution modes keep their own loops.
+template <bool PAIR, bool PHASE>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_conv_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
                    const __grid_constant__ CUtensorMap y_map, const TcGemmParams p) {
@@ -208,12 +262,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int mu = u / p.num_n_tiles;
                 const int nt = u - mu * p.num_n_tiles;
                 const int m = PAIR ? 2 * mu + static_cast<int>(rank) : mu;
-                PixTile t = pix_tile(p, m);
-                if (!t.exists) t = pix_tile(p, p.num_m_tiles - 1);  // a valid tile whose result is never stored
+                PixTile t = pix_tile<PHASE>(p, m);
+                if (!t.exists) t = pix_tile<PHASE>(p, p.num_m_tiles - 1);  // a valid tile whose result is never stored
+                const int ksteps = tile_ksteps<PHASE>(p, t.rh, t.rw);
                 for (int j = 0; j < p.gpc && ok; ++j) {
                     int grp, brow;
                     sub_gemm(p, nt, j, grp, brow);
-                    for (int ks = 0; ks < p.ksteps; ++ks) {
+                    for (int ks = 0; ks < ksteps; ++ks) {
                         if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
                             record_status(p.status, kStatusTimeoutProducer, abort);
                             ok = false;
@@ -221,15 +276,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                         const int tap = ks / p.kblk;
                         const int kb = ks - tap * p.kblk;
-                        const int kh = tap / p.g.Kw;
-                        const int kw = tap - kh * p.g.Kw;
+                        const Tap tp = tile_tap<PHASE>(p, t, tap);
                         const int c = grp * p.g.cin_g + kb * kTcBlockK;
                         uint8_t* a_dst = sm.a + stage * kABytes;
                         uint8_t* b_dst = sm.b + stage * b_bytes;
                         const uint32_t full_leader = PAIR ? mapa_shared(smem_addr(&sm.full[stage]), 0) : 0u;
                         if (leader) mbar_arrive_expect_tx(&sm.full[stage], a_b_bytes);
-                        load_a<PAIR>(p, &a_map, a_dst, &sm.full[stage], full_leader, t, c, kh, kw);
-                        const int kcol = tap * p.g.cin_g + kb * kTcBlockK;
+                        load_a<PAIR, PHASE>(p, &a_map, a_dst, &sm.full[stage], full_leader, t, c, tp);
+                        const int kcol = tp.wtap * p.g.cin_g + kb * kTcBlockK;
                         if constexpr (PAIR)
                             tma_load_2d_pair(b_dst, &b_map, full_leader, kcol, brow + static_cast<int>(rank) * b_rows);
                         else
@@ -272,9 +326,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_base = tmem_base + static_cast<uint32_t>(buf * p.n_tile);
+                int ksteps = p.ksteps;
+                if constexpr (PHASE) {  // the phase of tile m (no pairs in this mode)
+                    const int ph = (u / p.num_n_tiles) % (p.ps * p.ps);
+                    ksteps = tile_ksteps<PHASE>(p, ph / p.ps, ph % p.ps);
+                }
                 for (int j = 0; j < p.gpc && ok; ++j) {
                     const uint32_t d = d_base + static_cast<uint32_t>(j * p.mma_n);
-                    for (int ks = 0; ks < p.ksteps; ++ks) {
+                    for (int ks = 0; ks < ksteps; ++ks) {
                         if (!mbar_wait(&sm.full[stage], phase, abort)) {
                             record_status(p.status, kStatusTimeoutMma, abort);
                             ok = false;
@@ -341,11 +400,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int mu = u / p.num_n_tiles;
             const int nt = u - mu * p.num_n_tiles;
             const int m = PAIR ? 2 * mu + static_cast<int>(rank) : mu;
-            const PixTile t = pix_tile(p, m);
+            const PixTile t = pix_tile<PHASE>(p, m);
             // this warp's 32 pixels: rect mode = 32/TW rows of the rectangle, else 32 linear pixels
             bool rows_exist;
             int yc1, yc2, yc3;
-            if (p.mode == kTcModeRect) {
+            if (PHASE) {
+                const int h = t.ho0 + quarter * 32 / p.rect_w;  // phase-grid row
+                rows_exist = t.exists && h < p.hq && t.wo0 < p.wq;
+                yc1 = t.wo0;
+                yc2 = h;
+                yc3 = t.n;
+            } else if (p.mode == kTcModeRect) {
                 const int h = t.ho0 + quarter * 32 / p.rect_w;
                 rows_exist = t.exists && h < p.g.H_out && t.wo0 < p.g.W_out;
                 yc1 = t.wo0;
@@ -383,7 +448,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0 && rows_exist) {
-                        if (p.mode == kTcModeRect)
+                        if (PHASE)
+                            tma_store_5d(&y_map, dst, co0 + cc, t.rw, yc1, t.rh, yc3 * p.hq + yc2);
+                        else if (p.mode == kTcModeRect)
                             tma_store_4d(&y_map, dst, co0 + cc, yc1, yc2, yc3);
                         else
                             tma_store_2d(&y_map, dst, co0 + cc, yc1);
@@ -423,8 +490,8 @@ static int g_pair_smem_limits[64] = {};
 cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, const CUtensorMap& y_map,
                            const TcGemmParams& p, int grid, cudaStream_t stream) {
     if (p.pair) {
-        cudaError_t e =
-            ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<true>), p.smem_bytes, g_pair_smem_limits);
+        cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<true, false>), p.smem_bytes,
+                                          g_pair_smem_limits);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid, 1, 1);
@@ -438,20 +505,29 @@ cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, c
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, tc_conv_kernel<true>, a_map, b_map, y_map, p);
+        e = cudaLaunchKernelEx(&cfg, tc_conv_kernel<true, false>, a_map, b_map, y_map, p);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
+    if (p.mode == kTcModePhase) {
+        static int phase_limits[64] = {};
+        cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<false, true>), p.smem_bytes,
+                                          phase_limits);
+        if (e != cudaSuccess) return e;
+        tc_conv_kernel<false, true><<<grid, kTcThreads, p.smem_bytes, stream>>>(a_map, b_map, y_map, p);
+        return cudaGetLastError();
+    }
     static int limits[64] = {};
-    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<false>), p.smem_bytes, limits);
+    cudaError_t e =
+        ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<false, false>), p.smem_bytes, limits);
     if (e != cudaSuccess) return e;
-    tc_conv_kernel<false><<<grid, kTcThreads, p.smem_bytes, stream>>>(a_map, b_map, y_map, p);
+    tc_conv_kernel<false, false><<<grid, kTcThreads, p.smem_bytes, stream>>>(a_map, b_map, y_map, p);
     return cudaGetLastError();
 }
 
 int tc_gemm_pair_max_clusters(const TcGemmParams& p) {
-    if (ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<true>), p.smem_bytes, g_pair_smem_limits) !=
-        cudaSuccess) {
+    if (ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<true, false>), p.smem_bytes,
+                          g_pair_smem_limits) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -467,7 +543,7 @@ int tc_gemm_pair_max_clusters(const TcGemmParams& p) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_conv_kernel<true>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, tc_conv_kernel<true, false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }

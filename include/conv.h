@@ -54,10 +54,31 @@ enum {
     CONV_FLAG_BIAS = 1u,       /* add bias[co] after the sum                          */
     CONV_FLAG_RELU = 2u,       /* max(., 0) after the bias                            */
     CONV_FLAG_OUT_BF16 = 4u,   /* CONV_F32 only: write y as BF16 (round to nearest even) */
-    CONV_FLAG_SM_PAIRS = 8u    /* tensor-core GEMM paths: run each MMA on an SM pair
+    CONV_FLAG_SM_PAIRS = 8u,   /* tensor-core GEMM paths: run each MMA on an SM pair
                                   (clusters of 2, 256 pixels per MMA, weight rows split
                                   between the two SMs) instead of one SM per 128 pixels */
+    CONV_FLAG_TRANSPOSED = 16u /* transposed convolution (see below)                  */
 };
+
+/*
+ * Transposed convolution (CONV_FLAG_TRANSPOSED): the adjoint (matrix
+ * transpose) of the convolution with the same S, P, D, G ("Convolution
+ * variants and their matrix operations", sections 2.3 and 4.2: it upsamples;
+ * S-1 zeros between neighbouring input pixels, then a stride-1 convolution;
+ * in matrix form Y_col = W^T X).  Input pixel (i, j) of x [N][H][W][C_in]
+ * adds x * w[co][kh][kw][ci'] to output (i*S + kh*D - P, j*S + kw*D - P) of
+ * y [N][H_out][W_out][C_out]; positions outside the output are dropped:
+ *
+ *   y[n][ho][wo][co] = act( bias[co] + sum over ci' < C_in/G, kh, kw with
+ *        i = (ho + P - kh*D)/S and j = (wo + P - kw*D)/S exact and inside the
+ *        input of x[n][i][j][g*C_in/G + ci'] * w[co][kh][kw][ci'] ),
+ *
+ *   H_out = (H - 1)*S - 2P + D(Kh - 1) + 1, W_out likewise (no output padding;
+ *   the pages give no formula, this is the adjoint's size).
+ *
+ * The weight keeps this library's layout [C_out][Kh][Kw][C_in/G] (a framework
+ * weight [C_in][C_out/G][Kh][Kw] is permuted to it, not flipped).
+ */
 
 typedef enum {
     CONV_OK = 0,
@@ -69,7 +90,10 @@ typedef enum {
     CONV_ERR_TIMEOUT = 6       /* a device-side wait gave up (reported by conv_device_status) */
 } conv_status;
 
-/* Which kernel a plan runs (conv_plan_info). */
+/* Which kernel a plan runs (conv_plan_info).  A BF16 transposed plan runs the
+ * implicit-GEMM kernel in its phase mode when C_in/G % 64 == 0, C_out/G % 16 == 0,
+ * S <= 4, Kh, Kw <= 8, every output phase has at least one tap and S divides
+ * H_out and W_out; other transposed plans run the direct kernel. */
 typedef enum {
     CONV_PATH_DIRECT = 0,         /* CUDA-core direct loop, any shape                      */
     CONV_PATH_DEPTHWISE = 1,      /* FP32 depthwise, TMA halo tile in shared memory        */
@@ -98,7 +122,9 @@ conv_status conv_plan_output_shape(const conv_plan *p, int *H_out, int *W_out);
 
 /*
  * The chosen kernel (conv_path) and the logical GEMM extents of section 19 of
- * lesson 9: M = C_out, N = N*H_out*W_out, K = (C_in/G)*Kh*Kw (per group).
+ * lesson 9: M = C_out, N = N*H_out*W_out, K = (C_in/G)*Kh*Kw (per group).  For
+ * a transposed plan, the extents of its matrix form Y_col = W^T X (variants
+ * page, section 4.2): M = C_out*Kh*Kw, N = N*H*W, K = C_in/G.
  * Any output pointer may be NULL.
  */
 conv_status conv_plan_info(const conv_plan *p, int *path, long long *gemm_m,

@@ -52,7 +52,8 @@ def _create(*args):
     (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 1, 4),        # OUT_BF16 with BF16 input
     (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 2, 0),        # bad dtype
     (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 64),       # unknown flag
-    (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 16),       # unknown flag
+    (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 32),       # unknown flag
+    (1, 3, 2, 2, 4, 3, 3, 1, 3, 1, 1, 0, 16),       # transposed with an empty output: (2-1) - 6 + 2 + 1 < 1
 ])
 def test_create_rejects_bad_shapes(args):
     st, h = _create(*args)
@@ -177,3 +178,23 @@ def test_block_forward_without_device_fails_loudly():
     p = cg.BlockPlan(1, 64, 8, 8, 32, 3, 1)
     L = cg.lib()
     assert L.conv_block_forward(p._plan, 256, 256, None, None, 256, None, None, 256, None) == 4
+
+
+@pytest.mark.parametrize("shape,path", [
+    ((16, 256, 56, 56, 128, 4, 4, 2, 1, 1, 1, "bf16"), "implicit_gemm"),   # the upsampling layer
+    ((2, 64, 9, 7, 64, 3, 3, 1, 1, 1, 1, "bf16"), "implicit_gemm"),        # stride 1
+    ((2, 64, 6, 6, 32, 3, 3, 2, 1, 1, 1, "bf16"), "direct"),               # H_out = 11, not a multiple of S
+    ((2, 64, 6, 6, 32, 1, 1, 2, 0, 1, 1, "bf16"), "direct"),               # odd phases have no tap
+    ((2, 64, 6, 6, 32, 9, 9, 2, 4, 1, 1, "bf16"), "direct"),               # K > 8
+    ((2, 64, 6, 6, 32, 5, 5, 5, 0, 1, 1, "bf16"), "direct"),               # S > 4
+    ((2, 64, 8, 8, 64, 3, 3, 1, 1, 1, 64, "f32"), "direct"),               # FP32 depthwise-shaped: direct
+])
+def test_transposed_kernel_choice(shape, path):
+    *dims, dtype = shape
+    p = cg.ConvPlan(*dims, dtype=dtype, bias=True, relu=True, transposed=True)
+    assert p.path == path
+    N, C_in, H, W, C_out, Kh, Kw, S, P, D, G = dims
+    assert p.H_out == (H - 1) * S - 2 * P + D * (Kh - 1) + 1
+    assert p.W_out == (W - 1) * S - 2 * P + D * (Kw - 1) + 1
+    # matrix form Y_col = W^T X (variants page, section 4.2)
+    assert p.gemm_mnk == (C_out * Kh * Kw, N * H * W, C_in // G)

@@ -17,6 +17,14 @@ Shapes are the layer shapes the source pages discuss:
 * ``pw``         -- the block's pointwise 1x1, 256 -> 512, BF16, bias+ReLU.
 * ``dilated``    -- N=16, 256 -> 256, 64x64, 3x3 d2 p2 s1, groups 4, BF16,
   bias+ReLU (variants page, sections 2.2-2.3 and 4.2).
+* ``upsample``   -- N=16, 256 -> 128, 56x56 -> 112x112 transposed convolution,
+  4x4 s2 p1, BF16, bias+ReLU (the upsampling layer of the variants page,
+  sections 2.3 and 4.2, with the kernel size divisible by the stride as the
+  page advises against checkerboard overlap).
+
+Transposed shapes draw their weight as [C_in][C_out/G][Kh][Kw] (the matrix the
+operation transposes) with Kaiming fan-in = taps reaching one output,
+(C_in/G)*ceil(Kh/S)*ceil(Kw/S).
 
 Value recipe: X ~ N(0, 1) unless stated; W ~ N(0, 2/fan_in) with
 fan_in = (C_in/G)*Kh*Kw (Kaiming normal); bias ~ N(0, 0.01^2).  Config i
@@ -51,13 +59,18 @@ class ConvShape:
     bias: bool = True
     relu: bool = False
     out_bf16: bool = False       # FP32 depthwise writing a BF16 result (block mode)
+    transposed: bool = False     # transposed convolution (the adjoint of the convolution)
 
     @property
     def H_out(self) -> int:
+        if self.transposed:
+            return (self.H - 1) * self.S - 2 * self.P + self.D * (self.Kh - 1) + 1
         return (self.H + 2 * self.P - self.D * (self.Kh - 1) - 1) // self.S + 1
 
     @property
     def W_out(self) -> int:
+        if self.transposed:
+            return (self.W - 1) * self.S - 2 * self.P + self.D * (self.Kw - 1) + 1
         return (self.W + 2 * self.P - self.D * (self.Kw - 1) - 1) // self.S + 1
 
     @property
@@ -66,7 +79,14 @@ class ConvShape:
 
     @property
     def flops(self) -> int:
-        """Algorithmic FLOPs: 2 per multiply-add over live taps only."""
+        """Algorithmic FLOPs: 2 per multiply-add over live taps only.  Transposed:
+        2 per multiply-add of an (output pixel, tap) pair whose input pixel exists."""
+        if self.transposed:
+            def pairs(n_in, n_out, k):
+                ho = np.arange(n_out)[:, None] + self.P - self.D * np.arange(k)[None, :]
+                return int(np.sum((ho >= 0) & (ho % self.S == 0) & (ho // self.S < n_in)))
+            taps = pairs(self.H, self.H_out, self.Kh) * pairs(self.W, self.W_out, self.Kw)
+            return 2 * self.N * taps * self.C_out * (self.C_in // self.G)
         return 2 * self.pixels * self.C_out * (self.C_in // self.G) * self.Kh * self.Kw
 
     @property
@@ -112,6 +132,9 @@ WORKLOADS = {
     "dilated": Workload("dilated", 5,
                         ConvShape(16, 256, 64, 64, 256, 3, 3, 1, 2, 2, 4, "bf16", True, True),
                         description="dilated grouped conv bf16, N=16, 256->256, 64x64, 3x3 d2 p2 g4, bias+ReLU"),
+    "upsample": Workload("upsample", 6,
+                         ConvShape(16, 256, 56, 56, 128, 4, 4, 2, 1, 1, 1, "bf16", True, True, transposed=True),
+                         description="transposed conv bf16, N=16, 256->128, 56x56 -> 112x112, 4x4 s2 p1, bias+ReLU"),
 }
 
 
@@ -137,11 +160,16 @@ def draw(shape: ConvShape, seeds, x_dist="normal", w_dist="kaiming", b_dist="nor
         x = torch.rand(s.N, s.C_in, s.H, s.W, generator=_gen(seeds[0])) * 2 - 1
     else:
         x = torch.randn(s.N, s.C_in, s.H, s.W, generator=_gen(seeds[0]))
+    # conv: w [C_out][C_in/G][Kh][Kw]; transposed: w [C_in][C_out/G][Kh][Kw]
+    wshape = (s.C_in, s.C_out // s.G, s.Kh, s.Kw) if s.transposed else (s.C_out, cin_g, s.Kh, s.Kw)
     if w_dist == "uniform":
-        w = torch.rand(s.C_out, cin_g, s.Kh, s.Kw, generator=_gen(seeds[1])) * 2 - 1
+        w = torch.rand(*wshape, generator=_gen(seeds[1])) * 2 - 1
     else:
-        std = math.sqrt(2.0 / (cin_g * s.Kh * s.Kw))
-        w = torch.randn(s.C_out, cin_g, s.Kh, s.Kw, generator=_gen(seeds[1])) * std
+        fan_in = cin_g * s.Kh * s.Kw
+        if s.transposed:
+            fan_in = cin_g * (-(-s.Kh // s.S)) * (-(-s.Kw // s.S))
+        std = math.sqrt(2.0 / fan_in)
+        w = torch.randn(*wshape, generator=_gen(seeds[1])) * std
     b = None
     if s.bias:
         if b_dist == "uniform":
@@ -191,6 +219,17 @@ def x_device(x_nchw: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
     t = torch.from_numpy(np.ascontiguousarray(x_nchw, dtype=np.float32)).permute(0, 2, 3, 1).contiguous()
     t = t.to(torch.bfloat16 if dtype == "bf16" else torch.float32)
     return t.to(device)
+
+
+def w_device_transposed(w_iohw: np.ndarray, dtype: str, groups: int = 1, device="cuda") -> torch.Tensor:
+    """Transposed-convolution weights [C_in][C_out/G][Kh][Kw] -> the library's
+    [C_out][Kh][Kw][C_in/G] (a permutation per group, no flip)."""
+    C_in, cout_g, Kh, Kw = w_iohw.shape
+    cin_g = C_in // groups
+    w = np.asarray(w_iohw, dtype=np.float32).reshape(groups, cin_g, cout_g, Kh, Kw)
+    w = w.transpose(0, 2, 3, 4, 1).reshape(groups * cout_g, Kh, Kw, cin_g)
+    t = torch.from_numpy(np.ascontiguousarray(w))
+    return t.to(torch.bfloat16 if dtype == "bf16" else torch.float32).to(device)
 
 
 def w_device(w_oihw: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
