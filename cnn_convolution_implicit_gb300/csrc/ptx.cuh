@@ -170,6 +170,9 @@ __device__ __forceinline__ void bulk_wait_read_le1() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
+// Every committed bulk group of this thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 // Every committed bulk group of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 

@@ -28,7 +28,8 @@
 //   warp 0      TMA producer (one lane): A (pixels x 64 ch) and B (C_out x 64) per K-step
 //   warp 1      TMEM allocator; one lane issues tcgen05.mma and commits
 //   warps 2..9  epilogue, two groups of four (one per TMEM accumulator):
-//               tcgen05.ld -> +bias -> ReLU -> BF16 -> swizzled smem -> TMA store
+//               tcgen05.ld -> +bias -> ReLU -> BF16 -> swizzled smem -> TMA store,
+//               64 columns (two store tiles, one proxy fence) per step
 // Shared memory holds a ring of `stages` (A, B) buffers; TMEM holds two
 // accumulators so the epilogue of tile i overlaps the MMAs of tile i+1.
 //
@@ -377,14 +378,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         // Two groups of four warps, one per TMEM accumulator: group e takes the
-        // tiles that land in buffer e, so two tiles drain at once.  Per 32-column
-        // chunk: tcgen05.ld (the next chunk's load is in flight while this one
-        // is processed) -> +bias, ReLU, BF16 -> swizzled smem tile -> TMA store;
-        // two store tiles in flight per warp.
+        // tiles that land in buffer e, so two tiles drain at once.  Per 64
+        // columns: two tcgen05.ld -> scale, +bias, ReLU, BF16 -> two swizzled
+        // smem tiles -> two TMA stores in one bulk group.
         const int quarter = warp & 3;             // TMEM lane quarter this warp may access
         const int group = (warp - 2) >> 2;        // = the accumulator buffer it drains
         uint8_t* stg = sm.out + (warp - 2) * 2 * kOutTileBytes;
-        int sbuf = 0;
         int local = 0;
         for (int u = unit0; u < num_units; u += unit_step, ++local) {
             const int buf = local & 1;
@@ -425,38 +424,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int co0 = nt * p.n_tile;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(buf * p.n_tile);
-            uint32_t va[32], vb[32];
-            __syncwarp();
-            tmem_ld32(t_row, va);
+            // 64 columns per step: both 32-column TMEM loads in flight together, both
+            // chunks staged into this warp's 4 KB (the two staging tiles), then one
+            // proxy fence and one bulk group for the two TMA stores.
             for (int c = 0; c < p.n_tile; c += 64) {
+                const bool two = c + 32 < p.n_tile;
+                uint32_t va[32], vb[32];
+                __syncwarp();
+                tmem_ld32(t_row + static_cast<uint32_t>(c), va);
+                if (two) tmem_ld32(t_row + static_cast<uint32_t>(c + 32), vb);
+                tmem_ld_wait(va);
+                if (two) tmem_ld_wait(vb);
+                if (lane == 0) bulk_wait_read_all();  // the previous step's stores have read the staging tiles
+                __syncwarp();
+                stage_row32(va, p.bias ? p.bias + co0 + c : nullptr, p.relu, stg, lane,
+                            p.scale ? p.scale + co0 + c : nullptr);
+                if (two)
+                    stage_row32(vb, p.bias ? p.bias + co0 + c + 32 : nullptr, p.relu, stg + kOutTileBytes, lane,
+                                p.scale ? p.scale + co0 + c + 32 : nullptr);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && rows_exist) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int cc = c + 32 * h;
-                    if (cc >= p.n_tile) break;
-                    uint32_t(&cur)[32] = h == 0 ? va : vb;
-                    uint32_t(&nxt)[32] = h == 0 ? vb : va;
-                    tmem_ld_wait(cur);                 // chunk cc is in registers
-                    if (cc + 32 < p.n_tile) {          // start the next chunk's load
-                        __syncwarp();
-                        tmem_ld32(t_row + static_cast<uint32_t>(cc + 32), nxt);
-                    }
-                    if (lane == 0) bulk_wait_read_le1();  // the tile written two chunks ago is free
-                    __syncwarp();
-                    uint8_t* dst = stg + sbuf * kOutTileBytes;
-                    stage_row32(cur, p.bias ? p.bias + co0 + cc : nullptr, p.relu, dst, lane,
-                                p.scale ? p.scale + co0 + cc : nullptr);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0 && rows_exist) {
+                    for (int h = 0; h < 2; ++h) {
+                        if (h == 1 && !two) break;
+                        const uint8_t* src = stg + h * kOutTileBytes;
+                        const int cc = c + 32 * h;
                         if (PHASE)
-                            tma_store_5d(&y_map, dst, co0 + cc, t.rw, yc1, t.rh, yc3 * p.hq + yc2);
+                            tma_store_5d(&y_map, src, co0 + cc, t.rw, yc1, t.rh, yc3 * p.hq + yc2);
                         else if (p.mode == kTcModeRect)
-                            tma_store_4d(&y_map, dst, co0 + cc, yc1, yc2, yc3);
+                            tma_store_4d(&y_map, src, co0 + cc, yc1, yc2, yc3);
                         else
-                            tma_store_2d(&y_map, dst, co0 + cc, yc1);
-                        bulk_commit();
+                            tma_store_2d(&y_map, src, co0 + cc, yc1);
                     }
-                    sbuf ^= 1;
+                    bulk_commit();
                 }
             }
             tmem_ld_wait();
