@@ -530,3 +530,55 @@ def test_transposed_matches_torch_and_size_formula():
         assert y.shape == t.shape and np.allclose(y, t, rtol=1e-12, atol=1e-12)
     # the upsampling layer the pages describe: 56 -> 112 with K = 4, S = 2, P = 1
     assert oracle.out_size_transposed(56, 4, 2, 1, 1) == 112
+
+
+# ----------------------------------------------------------------- Winograd F(2x2, 3x3)
+def test_winograd_1d_minimal_filtering_is_exact():
+    """F(2, 3): y = A^T[(G g) * (B^T d)] equals the 2-output correlation exactly (integer
+    data, binary-exact halves): the transforms are right, not just close."""
+    BT, G, AT = oracle.WINO_BT, oracle.WINO_G, oracle.WINO_AT
+    d, g = np.array([1.0, 2.0, 3.0, 4.0]), np.array([1.0, 1.0, 1.0])
+    assert np.array_equal(AT @ ((G @ g) * (BT @ d)), [6.0, 9.0])
+    rng = np.random.default_rng(31)
+    for _ in range(200):
+        d = rng.integers(-50, 50, 4).astype(np.float64)
+        g = rng.integers(-50, 50, 3).astype(np.float64)
+        ref = np.array([d[0] * g[0] + d[1] * g[1] + d[2] * g[2], d[1] * g[0] + d[2] * g[1] + d[3] * g[2]])
+        assert np.array_equal(AT @ ((G @ g) * (BT @ d)), ref)
+
+
+@pytest.mark.parametrize("N,C,H,W,Co,P", [(2, 5, 7, 6, 4, 1), (1, 3, 8, 8, 8, 0), (2, 4, 5, 9, 3, 2),
+                                          (1, 16, 13, 11, 6, 1), (1, 2, 3, 3, 2, 0), (1, 1, 1, 1, 1, 1)])
+def test_winograd_equals_direct_convolution_in_fp64(N, C, H, W, Co, P):
+    """In exact arithmetic the method computes the convolution itself: in FP64 it matches the
+    direct oracle to rounding, for odd and even sizes (ragged last tiles) and P = 0, 1, 2."""
+    rng = np.random.default_rng(32 + H)
+    x = rng.standard_normal((N, C, H, W))
+    w = rng.standard_normal((Co, C, 3, 3))
+    b = rng.standard_normal(Co)
+    sc = rng.uniform(0.5, 2.0, Co)
+    y = oracle.winograd_conv2d(x, w, b, P, True, scale=sc)
+    r = oracle.conv2d(x, w, b, 1, P, 1, 1, True, scale=sc)
+    assert y.shape == r.shape
+    assert np.max(np.abs(y - r)) <= 1e-12 * (1 + np.max(np.abs(r)))
+
+
+def test_winograd_multiply_count_and_precision_cost():
+    """4 multiplies per output instead of 9 (16 per 2x2 tile): the pages' 2.25x; and in FP32
+    its error exceeds direct FP32 accumulation on the same data (the precision caveat), while
+    staying within the FP32 tolerance used for the library's FP32 paths."""
+    assert oracle.WINO_BT.shape[0] * oracle.WINO_BT.shape[0] / (oracle.WINO_AT.shape[0] ** 2) == 4.0
+    assert 9 / (16 / 4) == 2.25
+    rng = np.random.default_rng(33)
+    x = rng.standard_normal((2, 64, 16, 16))
+    w = rng.standard_normal((32, 64, 3, 3)) * np.sqrt(2.0 / 576)
+    ref = oracle.conv2d(x, w, None, 1, 1)
+    wino32 = oracle.winograd_conv2d(x.astype(np.float32), w.astype(np.float32), None, 1, dtype=np.float32)
+    # direct FP32 sums: explicit im2col columns times the weight matrix, in float32
+    xp = np.pad(x.astype(np.float32), ((0, 0), (0, 0), (1, 1), (1, 1)))
+    cols = np.lib.stride_tricks.sliding_window_view(xp, (3, 3), axis=(2, 3))      # N C H W 3 3
+    direct32 = np.einsum("nchwij,ocij->nohw", cols, w.astype(np.float32), optimize=True).astype(np.float64)
+    e_w = np.linalg.norm(wino32 - ref) / np.linalg.norm(ref)
+    e_d = np.linalg.norm(direct32 - ref) / np.linalg.norm(ref)
+    assert e_w > e_d
+    assert np.max(np.abs(wino32 - ref) / (1 + np.abs(ref))) <= 1e-5 and e_w <= 1e-5
