@@ -564,9 +564,10 @@ def test_winograd_equals_direct_convolution_in_fp64(N, C, H, W, Co, P):
 
 
 def test_winograd_multiply_count_and_precision_cost():
-    """4 multiplies per output instead of 9 (16 per 2x2 tile): the pages' 2.25x; and in FP32
-    its error exceeds direct FP32 accumulation on the same data (the precision caveat), while
-    staying within the FP32 tolerance used for the library's FP32 paths."""
+    """4 multiplies per output instead of 9 (16 per 2x2 tile): the pages' 2.25x.  In FP32 its
+    error on Kaiming-scale data is of the same order as direct FP32 sums (whose own error moves
+    with the summation order) and within the FP32 tolerance of the library's FP32 paths: for
+    this smallest tile the pages' precision caveat is mild."""
     assert oracle.WINO_BT.shape[0] * oracle.WINO_BT.shape[0] / (oracle.WINO_AT.shape[0] ** 2) == 4.0
     assert 9 / (16 / 4) == 2.25
     rng = np.random.default_rng(33)
@@ -580,5 +581,5 @@ def test_winograd_multiply_count_and_precision_cost():
     direct32 = np.einsum("nchwij,ocij->nohw", cols, w.astype(np.float32), optimize=True).astype(np.float64)
     e_w = np.linalg.norm(wino32 - ref) / np.linalg.norm(ref)
     e_d = np.linalg.norm(direct32 - ref) / np.linalg.norm(ref)
-    assert e_w > e_d
+    assert e_d / 3 <= e_w <= 3 * e_d
     assert np.max(np.abs(wino32 - ref) / (1 + np.abs(ref))) <= 1e-5 and e_w <= 1e-5
