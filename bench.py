@@ -32,6 +32,8 @@ sys.path.insert(0, ROOT)
 from workloads import WORKLOADS, b_device, inputs, w_device, w_device_transposed, x_device  # noqa: E402
 
 L2_FLUSH_BYTES = 256 << 20   # twice the 129 MB L2
+# FP32 FMA peak: 152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz (maximum SM clock)
+FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 def load_peaks():
@@ -71,6 +73,8 @@ KERNEL_SOURCES = {
     "dw": ["depthwise.cu", "ptx.cuh", "conv_internal.h"],
     "tiny_f32": ["direct.cu", "conv_internal.h"],
     "block": ["dwpw_block.cu", "tc_common.cuh", "ptx.cuh", "conv_internal.h"],
+    "winograd": ["winograd.cu", "conv_internal.h"],
+    "f32_3x3": ["direct.cu", "conv_internal.h"],
 }
 
 
@@ -225,11 +229,11 @@ def time_steps(fn, steps, warmup, flush):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
-def gpu_layer(name):
+def gpu_layer(name, winograd=False):
     """Device tensors + plan for a named workload."""
     from cnn_convolution_implicit_gb300 import ConvPlan
     s, x, w, b = inputs(name)
-    plan = ConvPlan.for_shape(s)
+    plan = ConvPlan.for_shape(s, winograd=winograd)
     xd = x_device(x, s.dtype)
     wd = w_device_transposed(w, s.dtype, s.G) if s.transposed else w_device(w, s.dtype)
     bd = b_device(b) if s.bias else None
@@ -237,8 +241,8 @@ def gpu_layer(name):
     return s, plan, (x, w, b), (xd, wd, bd, y)
 
 
-def measure_layer(name, steps, warmup, flush, peaks, affine=False):
-    s, plan, host, (xd, wd, bd, y) = gpu_layer(name)
+def measure_layer(name, steps, warmup, flush, peaks, affine=False, winograd=False):
+    s, plan, host, (xd, wd, bd, y) = gpu_layer(name, winograd)
     scale = None
     if affine:  # folded batch norm: per-channel scale before the shift
         scale = torch.from_numpy(np.random.default_rng(5).uniform(0.5, 1.5, s.C_out).astype(np.float32)).cuda()
@@ -250,14 +254,20 @@ def measure_layer(name, steps, warmup, flush, peaks, affine=False):
     t = float(np.mean(ms)) * 1e-3
     tflops = s.flops / t / 1e12
     gbs = s.algorithmic_bytes / t / 1e9
-    bound = "hbm" if s.flops / s.algorithmic_bytes < peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9) \
-        or s.dtype == "f32" else "tensor"
-    res = {"workload": name + ("+affine" if affine else ""), "kernel": plan.path, "ms": t * 1e3,
-           "tflops": tflops, "gbs": gbs,
+    if s.dtype == "f32" and s.G == 1:
+        bound = "alu"   # FP32 sums on CUDA cores, far below the ridge of their FMA peak
+    else:
+        bound = "hbm" if s.flops / s.algorithmic_bytes < peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9) \
+            or s.dtype == "f32" else "tensor"
+    res = {"workload": name + ("+affine" if affine else "") + ("+winograd" if winograd else ""),
+           "kernel": plan.path, "ms": t * 1e3, "tflops": tflops, "gbs": gbs,
            "bound": bound, "flops": s.flops, "bytes": s.algorithmic_bytes, "launches": steps,
-           "source_hash": kernel_source_hash(name), "launch": plan.launch}
+           "source_hash": kernel_source_hash("winograd" if plan.path == "winograd" else name), "launch": plan.launch}
     if bound == "tensor":
         res["frac"] = tflops / peaks["bf16_tflops"]
+    elif bound == "alu":
+        res["peak_tflops"] = FP32_FMA_TFLOPS
+        res["frac"] = tflops / FP32_FMA_TFLOPS   # conv FLOPs; Winograd executes 4/9 of the multiplies
     else:
         res["frac"] = gbs / peaks["hbm_gbs"]
     return res, (s, plan, host, (xd, wd, bd, y))
@@ -361,6 +371,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=sorted(WORKLOADS) + ["block"], default=None,
                     help="time one layer alone (no oracle, no e2e); used for ncu captures")
+    ap.add_argument("--winograd", action="store_true", help="with --only: plan the layer with CONV_FLAG_WINOGRAD")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -370,7 +381,7 @@ def main():
         if args.only == "block":
             r, _ = measure_block(args.steps, args.warmup, flush, load_peaks())
         else:
-            r, _ = measure_layer(args.only, args.steps, args.warmup, flush, load_peaks())
+            r, _ = measure_layer(args.only, args.steps, args.warmup, flush, load_peaks(), winograd=args.winograd)
         print(json.dumps(r))
         return
 
@@ -465,6 +476,9 @@ def main():
     for name in ("dw", "stem", "pw", "dilated", "upsample"):
         r, _ = measure_layer(name, max(10, args.steps // 2), args.warmup, flush, peaks)
         others[name] = r
+    for name, wino in (("f32_3x3", False), ("f32_3x3", True)):
+        r, _ = measure_layer(name, max(10, args.steps // 2), args.warmup, flush, peaks, winograd=wino)
+        others[r["workload"]] = r
     r, _ = measure_layer("body", max(10, args.steps // 2), args.warmup, flush, peaks, affine=True)
     others["body+affine"] = r
     others["block"], others["block_two_launches"] = measure_block(max(10, args.steps // 2), args.warmup, flush,

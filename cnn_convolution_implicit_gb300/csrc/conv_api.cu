@@ -15,6 +15,7 @@
 //   BF16, (C_in/G) % 64 == 0, aligned      -> tcgen05 implicit GEMM, TMA im2col
 //   BF16, G=1, C_in*Kh*Kw <= 64            -> tcgen05 small-K kernel (stem)
 //   BF16 transposed, aligned, S | H_out    -> tcgen05 implicit GEMM, phase mode
+//   FP32 3x3 s1 d1 G=1 with WINOGRAD flag  -> Winograd F(2x2, 3x3) kernel
 //   anything else                          -> direct CUDA-core kernel
 #include <mutex>
 #include <new>
@@ -443,7 +444,8 @@ conv_status conv_plan_create(conv_plan** out, int N, int C_in, int H, int W, int
         return CONV_ERR_INVALID_ARG;
     if (C_in % G != 0 || C_out % G != 0) return CONV_ERR_INVALID_ARG;
     if (dtype != CONV_F32 && dtype != CONV_BF16) return CONV_ERR_INVALID_ARG;
-    if (flags & ~(CONV_FLAG_BIAS | CONV_FLAG_RELU | CONV_FLAG_OUT_BF16 | CONV_FLAG_SM_PAIRS | CONV_FLAG_TRANSPOSED))
+    if (flags & ~(CONV_FLAG_BIAS | CONV_FLAG_RELU | CONV_FLAG_OUT_BF16 | CONV_FLAG_SM_PAIRS | CONV_FLAG_TRANSPOSED |
+                  CONV_FLAG_WINOGRAD))
         return CONV_ERR_INVALID_ARG;
     if ((flags & CONV_FLAG_OUT_BF16) && dtype != CONV_F32) return CONV_ERR_INVALID_ARG;
     const bool transposed = (flags & CONV_FLAG_TRANSPOSED) != 0;
@@ -491,7 +493,10 @@ conv_status conv_plan_create(conv_plan** out, int N, int C_in, int H, int W, int
     if (transposed) {
         if (dtype == CONV_BF16 && configure_tc(pl, false, true)) pl->path = CONV_PATH_IMPLICIT_GEMM;
     } else if (dtype == CONV_F32) {
-        if (configure_depthwise(pl)) pl->path = CONV_PATH_DEPTHWISE;
+        if ((flags & CONV_FLAG_WINOGRAD) && winograd_supported(g))
+            pl->path = CONV_PATH_WINOGRAD;
+        else if (configure_depthwise(pl))
+            pl->path = CONV_PATH_DEPTHWISE;
     } else {
         const bool pointwise = Kh == 1 && Kw == 1 && S == 1 && P == 0 && G == 1;
         if (pointwise && configure_tc(pl, true))
@@ -560,6 +565,14 @@ conv_status conv_plan_launch_info(const conv_plan* p, int* grid, int* block, int
             st = p->sk.stages;
             gr = p->sk.num_tiles < p->num_sms ? p->sk.num_tiles : p->num_sms;
             break;
+        case CONV_PATH_WINOGRAD: {
+            unsigned gx = 0, gy = 0;
+            winograd_grid(p->g, gx, gy);
+            gr = static_cast<int>(gx * gy);
+            bl = kWgThreads;
+            sm = winograd_smem_bytes();
+            break;
+        }
         case CONV_PATH_DEPTHWISE:
             bl = 256;
             sm = p->dw.smem_bytes;
@@ -637,6 +650,19 @@ conv_status forward_impl(conv_plan* p, const void* x, const void* w, const float
             s.y = static_cast<__nv_bfloat16*>(y);
             const int grid = s.num_tiles < p->num_sms ? s.num_tiles : p->num_sms;
             e = launch_tc_smallk(p->map_y, s, grid, st);
+            break;
+        }
+        case CONV_PATH_WINOGRAD: {
+            WinogradParams wp;
+            wp.g = p->g;
+            wp.x = x;
+            wp.w = w;
+            wp.bias = b;
+            wp.scale = scale;
+            wp.y = y;
+            wp.relu = (p->flags & CONV_FLAG_RELU) ? 1 : 0;
+            wp.out_bf16 = (p->flags & CONV_FLAG_OUT_BF16) ? 1 : 0;
+            e = launch_winograd(wp, st);
             break;
         }
         case CONV_PATH_DEPTHWISE: {

@@ -47,6 +47,23 @@ struct DirectParams {
 };
 cudaError_t launch_direct(const DirectParams& p, cudaStream_t stream);
 
+// ---------------------------------------------------------------- Winograd F(2x2, 3x3) (FP32)
+constexpr int kWgThreads = 256;
+struct WinogradParams {
+    ConvGeom g;           // 3x3, S = 1, D = 1, G = 1
+    const void* x;        // FP32 NHWC
+    const void* w;        // FP32 [C_out][3][3][C_in]
+    const float* bias;    // nullptr when no bias
+    const float* scale;   // nullptr when no per-channel scale
+    void* y;
+    int relu;
+    int out_bf16;
+};
+bool winograd_supported(const ConvGeom& g);
+void winograd_grid(const ConvGeom& g, unsigned& gx, unsigned& gy);
+int winograd_smem_bytes();
+cudaError_t launch_winograd(const WinogradParams& p, cudaStream_t stream);
+
 // ---------------------------------------------------------------- depthwise (FP32, TMA halo tile)
 struct DepthwiseParams {
     ConvGeom g;

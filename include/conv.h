@@ -57,7 +57,13 @@ enum {
     CONV_FLAG_SM_PAIRS = 8u,   /* tensor-core GEMM paths: run each MMA on an SM pair
                                   (clusters of 2, 256 pixels per MMA, weight rows split
                                   between the two SMs) instead of one SM per 128 pixels */
-    CONV_FLAG_TRANSPOSED = 16u /* transposed convolution (see below)                  */
+    CONV_FLAG_TRANSPOSED = 16u, /* transposed convolution (see below)                 */
+    CONV_FLAG_WINOGRAD = 32u   /* FP32 3x3, stride 1, dilation 1, G = 1: Winograd F(2x2, 3x3)
+                                  ("Convolution vs inner product", lnrq.cn, section 2.2;
+                                  variants page, section 3.3): 4 multiplies per output
+                                  instead of 9, rounding differs from the direct sum (the
+                                  pages' precision caveat; it stays within FP32 tolerance
+                                  on Kaiming-scale data).  Ignored for other plans. */
 };
 
 /*
@@ -99,9 +105,10 @@ typedef enum {
     CONV_PATH_DEPTHWISE = 1,      /* FP32 depthwise, TMA halo tile in shared memory        */
     CONV_PATH_GEMM_1X1 = 2,       /* BF16 1x1 / stride 1 / pad 0: tcgen05 GEMM, tiled TMA  */
     CONV_PATH_IMPLICIT_GEMM = 3,  /* BF16 implicit GEMM: TMA im2col + tcgen05 + TMEM        */
-    CONV_PATH_SMALL_K_GEMM = 4    /* BF16, C_in*Kh*Kw <= 64 (e.g. a 3-channel stem): rows
+    CONV_PATH_SMALL_K_GEMM = 4,   /* BF16, C_in*Kh*Kw <= 64 (e.g. a 3-channel stem): rows
                                      staged by bulk copy, K gathered in shared memory,
                                      tcgen05 + TMEM                                     */
+    CONV_PATH_WINOGRAD = 5        /* FP32 Winograd F(2x2, 3x3) on CUDA cores (opt-in)     */
 } conv_path;
 
 /*

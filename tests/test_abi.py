@@ -52,7 +52,7 @@ def _create(*args):
     (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 1, 4),        # OUT_BF16 with BF16 input
     (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 2, 0),        # bad dtype
     (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 64),       # unknown flag
-    (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 32),       # unknown flag
+    (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 128),      # unknown flag
     (1, 3, 2, 2, 4, 3, 3, 1, 3, 1, 1, 0, 16),       # transposed with an empty output: (2-1) - 6 + 2 + 1 < 1
 ])
 def test_create_rejects_bad_shapes(args):
@@ -198,3 +198,20 @@ def test_transposed_kernel_choice(shape, path):
     assert p.W_out == (W - 1) * S - 2 * P + D * (Kw - 1) + 1
     # matrix form Y_col = W^T X (variants page, section 4.2)
     assert p.gemm_mnk == (C_out * Kh * Kw, N * H * W, C_in // G)
+
+
+@pytest.mark.parametrize("shape,winograd,path", [
+    ((8, 64, 56, 56, 64, 3, 3, 1, 1, 1, 1, "f32"), True, "winograd"),
+    ((8, 64, 56, 56, 64, 3, 3, 1, 1, 1, 1, "f32"), False, "direct"),     # opt-in only
+    ((1, 3, 32, 32, 8, 3, 3, 1, 1, 1, 1, "f32"), True, "winograd"),      # ragged channels
+    ((2, 8, 9, 9, 8, 3, 3, 2, 1, 1, 1, "f32"), True, "direct"),          # stride 2
+    ((2, 8, 9, 9, 8, 3, 3, 1, 2, 2, 1, "f32"), True, "direct"),          # dilation 2
+    ((2, 8, 9, 9, 8, 5, 5, 1, 2, 1, 1, "f32"), True, "direct"),          # 5x5
+    ((2, 8, 9, 9, 8, 3, 3, 1, 1, 1, 2, "f32"), True, "direct"),          # groups
+    ((2, 64, 9, 9, 64, 3, 3, 1, 1, 1, 64, "f32"), True, "depthwise"),    # depthwise keeps its kernel
+    ((2, 128, 9, 9, 128, 3, 3, 1, 1, 1, 1, "bf16"), True, "implicit_gemm"),  # BF16: tensor cores
+])
+def test_winograd_kernel_choice(shape, winograd, path):
+    *dims, dtype = shape
+    p = cg.ConvPlan(*dims, dtype=dtype, bias=True, relu=True, winograd=winograd)
+    assert p.path == path

@@ -17,6 +17,8 @@ Shapes are the layer shapes the source pages discuss:
 * ``pw``         -- the block's pointwise 1x1, 256 -> 512, BF16, bias+ReLU.
 * ``dilated``    -- N=16, 256 -> 256, 64x64, 3x3 d2 p2 s1, groups 4, BF16,
   bias+ReLU (variants page, sections 2.2-2.3 and 4.2).
+* ``f32_3x3``    -- N=8, 64 -> 64, 56x56, 3x3 s1 p1, FP32, bias+ReLU (a first-stage
+  residual-network convolution kept in FP32: the Winograd F(2x2, 3x3) comparison).
 * ``upsample``   -- N=16, 256 -> 128, 56x56 -> 112x112 transposed convolution,
   4x4 s2 p1, BF16, bias+ReLU (the upsampling layer of the variants page,
   sections 2.3 and 4.2, with the kernel size divisible by the stride as the
@@ -132,6 +134,9 @@ WORKLOADS = {
     "dilated": Workload("dilated", 5,
                         ConvShape(16, 256, 64, 64, 256, 3, 3, 1, 2, 2, 4, "bf16", True, True),
                         description="dilated grouped conv bf16, N=16, 256->256, 64x64, 3x3 d2 p2 g4, bias+ReLU"),
+    "f32_3x3": Workload("f32_3x3", 7,
+                        ConvShape(8, 64, 56, 56, 64, 3, 3, 1, 1, 1, 1, "f32", True, True),
+                        description="conv fp32, N=8, 64->64, 56x56, 3x3 s1 p1, bias+ReLU"),
     "upsample": Workload("upsample", 6,
                          ConvShape(16, 256, 56, 56, 128, 4, 4, 2, 1, 1, 1, "bf16", True, True, transposed=True),
                          description="transposed conv bf16, N=16, 256->128, 56x56 -> 112x112, 4x4 s2 p1, bias+ReLU"),
