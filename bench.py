@@ -210,6 +210,22 @@ def clock_sampler(local):
         return ClockSampler(gpu_id)
 
 
+# ----------------------------------------------------------------------------- ranks
+def max_over_ranks(seconds, dist=None, device="cpu"):
+    """The slowest rank's time: the whole job is done only when every replica is."""
+    if dist is None:
+        return seconds
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, seconds_per_step):
+    """Aggregate throughput of `world` replicas that each process `units_per_rank` per step
+    (weak scaling: the per-GPU work is fixed as the number of GPUs grows)."""
+    return units_per_rank * world / seconds_per_step
+
+
 # ----------------------------------------------------------------------------- timing
 def time_steps(fn, steps, warmup, flush):
     """Per-step CUDA-event time of fn() on the current stream, L2 flushed
@@ -439,15 +455,11 @@ def main():
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    t_step = float(np.mean(ms)) * 1e-3
-    t_total = float(np.sum(ms)) * 1e-3
-    if dist:
-        tt = torch.tensor([t_total], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_total = float(tt.item())
-        t_step = t_total / args.steps
-    value = s.flops * world / t_step / 1e12
-    kern_tflops = s.flops / t_step / 1e12
+    t_step_local = float(np.mean(ms)) * 1e-3
+    t_total = max_over_ranks(float(np.sum(ms)) * 1e-3, dist, "cuda")
+    t_step = t_total / args.steps
+    value = whole_job_rate(s.flops, world, t_step) / 1e12
+    kern_tflops = s.flops / t_step_local / 1e12
 
     # ---- e2e through the public API with pinned host buffers
     x_h = xd.cpu().pin_memory()
@@ -467,9 +479,9 @@ def main():
     ms_e2e = time_steps(e2e_step, e2e_steps, 3, flush)
     h2d = x_h.numel() * 2 + w_h.numel() * 2 + b_h.numel() * 4
     d2h = y_h.numel() * 2
-    e2e = {"value": s.flops * world / (float(np.mean(ms_e2e)) * 1e-3) / 1e12, "unit": "TFLOP/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "ms_per_step": float(np.mean(ms_e2e))}
+    t_e2e = max_over_ranks(float(np.mean(ms_e2e)) * 1e-3, dist, "cuda")
+    e2e = {"value": whole_job_rate(s.flops, world, t_e2e) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3}
 
     # ---- the other layers of the metric (depthwise GB/s first)
     others = {}
