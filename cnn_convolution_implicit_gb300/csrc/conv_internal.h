@@ -89,7 +89,7 @@ cudaError_t launch_depthwise(const CUtensorMap& x_map, const DepthwiseParams& p,
 // ---------------------------------------------------------------- tcgen05 GEMM (1x1 and implicit)
 constexpr int kTcBlockM = 128;    // pixels per tile (TMEM lanes)
 constexpr int kTcBlockK = 64;     // BF16 elements per K-step (one 128-byte swizzle row)
-constexpr int kTcThreads = 320;   // producer warp, MMA warp, 2 x 4 epilogue warps
+constexpr int kTcThreads = 576;   // producer warp, MMA warp, 4 x 4 epilogue warps
 constexpr int kTcMaxGroupsPerTile = 8;  // groups packed side by side in one accumulator (<= ring stages)
 
 enum TcMode { kTcMode1x1 = 0, kTcModeIm2col = 1, kTcModeRect = 2, kTcModePhase = 3 };

@@ -24,12 +24,12 @@
 // Groups are independent GEMMs (variants page, sections 2.2 and 4.3): a tile
 // packs `gpc` groups side by side in TMEM columns, each with its own K loop.
 //
-// Warp roles (320 threads, one CTA per SM, persistent over tiles):
+// Warp roles (576 threads, one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer (one lane): A (pixels x 64 ch) and B (C_out x 64) per K-step
 //   warp 1      TMEM allocator; one lane issues tcgen05.mma and commits
-//   warps 2..9  epilogue, two groups of four (one per TMEM accumulator):
-//               tcgen05.ld -> +bias -> ReLU -> BF16 -> swizzled smem -> TMA store,
-//               64 columns (two store tiles, one proxy fence) per step
+//   warps 2..17 epilogue, four groups of four, two per TMEM accumulator (each
+//               group drains half of its columns): tcgen05.ld -> +bias -> ReLU ->
+//               BF16 -> swizzled smem -> TMA store, 32 columns per step
 // Shared memory holds a ring of `stages` (A, B) buffers; TMEM holds two
 // accumulators so the epilogue of tile i overlaps the MMAs of tile i+1.
 //
@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.tfull[b], 1);
-            mbar_init(&sm.tempty[b], PAIR ? 2 * 4 : 4);  // one arrival per warp of its epilogue group (both CTAs)
+            mbar_init(&sm.tempty[b], PAIR ? 2 * 8 : 8);  // one arrival per warp of its two epilogue groups (both CTAs)
         }
         mbar_init(sm.drain, 1);
         *sm.abort = 0;
@@ -377,13 +377,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        // Two groups of four warps, one per TMEM accumulator: group e takes the
-        // tiles that land in buffer e, so two tiles drain at once.  Per 64
-        // columns: two tcgen05.ld -> scale, +bias, ReLU, BF16 -> two swizzled
-        // smem tiles -> two TMA stores in one bulk group.
+        // Four groups of four warps, two per TMEM accumulator: the groups of
+        // buffer e take the tiles that land in it, each draining half of the
+        // columns, so two tiles drain at once with twice the warps on each.  Per
+        // 32 columns: tcgen05.ld -> scale, +bias, ReLU, BF16 -> swizzled smem
+        // tile (one per warp) -> TMA store.
         const int quarter = warp & 3;             // TMEM lane quarter this warp may access
-        const int group = (warp - 2) >> 2;        // = the accumulator buffer it drains
-        uint8_t* stg = sm.out + (warp - 2) * 2 * kOutTileBytes;
+        const int egroup = (warp - 2) >> 2;       // 0..3
+        const int group = egroup >> 1;            // = the accumulator buffer it drains
+        const int chalf = egroup & 1;             // which half of the columns
+        uint8_t* stg = sm.out + (warp - 2) * kOutTileBytes;
         int local = 0;
         for (int u = unit0; u < num_units; u += unit_step, ++local) {
             const int buf = local & 1;
@@ -424,39 +427,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int co0 = nt * p.n_tile;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(buf * p.n_tile);
-            // 64 columns per step: both 32-column TMEM loads in flight together, both
-            // chunks staged into this warp's 4 KB (the two staging tiles), then one
-            // proxy fence and one bulk group for the two TMA stores.
-            for (int c = 0; c < p.n_tile; c += 64) {
-                const bool two = c + 32 < p.n_tile;
-                uint32_t va[32], vb[32];
+            // this group's half of the columns, 32 per step, one staging tile per warp
+            const int chunks = p.n_tile / 32;
+            const int c_lo = chalf == 0 ? 0 : ((chunks + 1) / 2) * 32;
+            const int c_hi = chalf == 0 ? ((chunks + 1) / 2) * 32 : p.n_tile;
+            for (int c = c_lo; c < c_hi; c += 32) {
+                uint32_t v[32];
                 __syncwarp();
-                tmem_ld32(t_row + static_cast<uint32_t>(c), va);
-                if (two) tmem_ld32(t_row + static_cast<uint32_t>(c + 32), vb);
-                tmem_ld_wait(va);
-                if (two) tmem_ld_wait(vb);
-                if (lane == 0) bulk_wait_read_all();  // the previous step's stores have read the staging tiles
+                tmem_ld32(t_row + static_cast<uint32_t>(c), v);
+                tmem_ld_wait(v);
+                if (lane == 0) bulk_wait_read_all();
                 __syncwarp();
-                stage_row32(va, p.bias ? p.bias + co0 + c : nullptr, p.relu, stg, lane,
+                stage_row32(v, p.bias ? p.bias + co0 + c : nullptr, p.relu, stg, lane,
                             p.scale ? p.scale + co0 + c : nullptr);
-                if (two)
-                    stage_row32(vb, p.bias ? p.bias + co0 + c + 32 : nullptr, p.relu, stg + kOutTileBytes, lane,
-                                p.scale ? p.scale + co0 + c + 32 : nullptr);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0 && rows_exist) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        if (h == 1 && !two) break;
-                        const uint8_t* src = stg + h * kOutTileBytes;
-                        const int cc = c + 32 * h;
-                        if (PHASE)
-                            tma_store_5d(&y_map, src, co0 + cc, t.rw, yc1, t.rh, yc3 * p.hq + yc2);
-                        else if (p.mode == kTcModeRect)
-                            tma_store_4d(&y_map, src, co0 + cc, yc1, yc2, yc3);
-                        else
-                            tma_store_2d(&y_map, src, co0 + cc, yc1);
-                    }
+                    if (PHASE)
+                        tma_store_5d(&y_map, stg, co0 + c, t.rw, yc1, t.rh, yc3 * p.hq + yc2);
+                    else if (p.mode == kTcModeRect)
+                        tma_store_4d(&y_map, stg, co0 + c, yc1, yc2, yc3);
+                    else
+                        tma_store_2d(&y_map, stg, co0 + c, yc1);
                     bulk_commit();
                 }
             }
