@@ -145,32 +145,11 @@ __device__ __forceinline__ int tile_ksteps(const TcGemmParams& p, int rh, int rw
     return p.ksteps;
 }
 
-// Tap `tap` of a tile: kernel indices, input offsets (rect / phase modes) and
-// the weight tap it multiplies.
+// One tap of a tile's K loop: kernel indices, input offsets (rect / phase
+// modes) and the weight tap it multiplies.
 struct Tap {
     int kh, kw, dh, dw, wtap;
 };
-
-template <bool PHASE>
-__device__ __forceinline__ Tap tile_tap(const TcGemmParams& p, const PixTile& t, int tap) {
-    Tap r;
-    if constexpr (PHASE) {
-        const int cw = p.pw.cnt[t.rw];
-        const int a = tap / cw, b = tap - a * cw;
-        r.kh = p.ph.k[t.rh][a];
-        r.kw = p.pw.k[t.rw][b];
-        r.dh = p.ph.off[t.rh][a];
-        r.dw = p.pw.off[t.rw][b];
-        r.wtap = r.kh * p.g.Kw + r.kw;
-    } else {
-        r.kh = tap / p.g.Kw;
-        r.kw = tap - r.kh * p.g.Kw;
-        r.dh = r.kh * p.g.D - p.g.P;
-        r.dw = r.kw * p.g.D - p.g.P;
-        r.wtap = tap;
-    }
-    return r;
-}
 
 // A operand of one K-step: 128 pixels x 64 channels of tap (kh, kw).
 template <bool PAIR, bool PHASE>
@@ -269,15 +248,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int j = 0; j < p.gpc && ok; ++j) {
                     int grp, brow;
                     sub_gemm(p, nt, j, grp, brow);
+                    int c_kb = 0, c_kh = 0, c_kw = 0, c_tap = 0;
                     for (int ks = 0; ks < ksteps; ++ks) {
                         if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
                             record_status(p.status, kStatusTimeoutProducer, abort);
                             ok = false;
                             break;
                         }
-                        const int tap = ks / p.kblk;
-                        const int kb = ks - tap * p.kblk;
-                        const Tap tp = tile_tap<PHASE>(p, t, tap);
+                        Tap tp;
+                        int kb;
+                        if constexpr (PHASE) {  // running counters over the phase's row and column taps
+                            kb = c_kb;
+                            tp.kh = p.ph.k[t.rh][c_kh];
+                            tp.kw = p.pw.k[t.rw][c_kw];
+                            tp.dh = p.ph.off[t.rh][c_kh];
+                            tp.dw = p.pw.off[t.rw][c_kw];
+                            tp.wtap = tp.kh * p.g.Kw + tp.kw;
+                            if (++c_kb == p.kblk) {
+                                c_kb = 0;
+                                if (++c_kw == p.pw.cnt[t.rw]) {
+                                    c_kw = 0;
+                                    ++c_kh;
+                                }
+                            }
+                        } else {  // running counters: no division per K-step
+                            kb = c_kb;
+                            tp.kh = c_kh;
+                            tp.kw = c_kw;
+                            tp.dh = c_kh * p.g.D - p.g.P;
+                            tp.dw = c_kw * p.g.D - p.g.P;
+                            tp.wtap = c_tap;
+                            if (++c_kb == p.kblk) {
+                                c_kb = 0;
+                                ++c_tap;
+                                if (++c_kw == p.g.Kw) {
+                                    c_kw = 0;
+                                    ++c_kh;
+                                }
+                            }
+                        }
                         const int c = grp * p.g.cin_g + kb * kTcBlockK;
                         uint8_t* a_dst = sm.a + stage * kABytes;
                         uint8_t* b_dst = sm.b + stage * b_bytes;
