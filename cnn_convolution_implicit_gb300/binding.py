@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(HERE, "libconv.so")
 
 CONV_F32, CONV_BF16 = 0, 1
 CONV_FLAG_BIAS, CONV_FLAG_RELU, CONV_FLAG_OUT_BF16, CONV_FLAG_SM_PAIRS, CONV_FLAG_TRANSPOSED = 1, 2, 4, 8, 16
-CONV_FLAG_WINOGRAD = 32
+CONV_FLAG_WINOGRAD, CONV_FLAG_ONE_SM = 32, 64
 STATUS = {0: "CONV_OK", 1: "CONV_ERR_INVALID_ARG", 2: "CONV_ERR_UNSUPPORTED", 3: "CONV_ERR_MISALIGNED",
           4: "CONV_ERR_CUDA", 5: "CONV_ERR_NO_MEMORY", 6: "CONV_ERR_TIMEOUT"}
 PATHS = {0: "direct", 1: "depthwise", 2: "gemm_1x1", 3: "implicit_gemm", 4: "small_k_gemm", 5: "winograd"}
@@ -109,14 +109,17 @@ class ConvPlan:
     transposed convolution (the adjoint of the convolution with the same S, P,
     D, G; output (H - 1)*S - 2P + D(Kh - 1) + 1 rows), same weight layout.
     winograd=True asks FP32 3x3 stride-1 ungrouped plans to run Winograd F(2x2, 3x3).
+    sm_pairs: None lets the plan choose SM pairs or one SM per tile for the tensor-core
+    GEMM paths; True / False force one or the other.
     """
 
     def __init__(self, N, C_in, H, W, C_out, Kh, Kw, S=1, P=0, D=1, G=1, dtype="bf16",
-                 bias=True, relu=False, out_bf16=False, sm_pairs=False, transposed=False, winograd=False):
+                 bias=True, relu=False, out_bf16=False, sm_pairs=None, transposed=False, winograd=False):
         L = lib()
         self._plan = None
         flags = (CONV_FLAG_BIAS if bias else 0) | (CONV_FLAG_RELU if relu else 0) | \
-                (CONV_FLAG_OUT_BF16 if out_bf16 else 0) | (CONV_FLAG_SM_PAIRS if sm_pairs else 0) | \
+                (CONV_FLAG_OUT_BF16 if out_bf16 else 0) | (CONV_FLAG_SM_PAIRS if sm_pairs is True else 0) | \
+                (CONV_FLAG_ONE_SM if sm_pairs is False else 0) | \
                 (CONV_FLAG_TRANSPOSED if transposed else 0) | (CONV_FLAG_WINOGRAD if winograd else 0)
         dt = {"bf16": CONV_BF16, "f32": CONV_F32}[dtype]
         h = ctypes.c_void_p()
@@ -140,7 +143,7 @@ class ConvPlan:
         self.launch = dict(zip(("grid", "block", "smem_bytes", "stages", "cluster"), [v.value for v in li]))
 
     @classmethod
-    def for_shape(cls, s, sm_pairs=False, winograd=False):
+    def for_shape(cls, s, sm_pairs=None, winograd=False):
         """Plan from a workloads.ConvShape-like object."""
         return cls(s.N, s.C_in, s.H, s.W, s.C_out, s.Kh, s.Kw, s.S, s.P, s.D, s.G, s.dtype,
                    s.bias, s.relu, s.out_bf16, sm_pairs, getattr(s, "transposed", False), winograd)

@@ -211,7 +211,13 @@ bool configure_tc(conv_plan* pl, bool one_by_one, bool transposed = false) {
     t.ychunk = 32;
     // SM pairs (one MMA over 2 x 128 pixels, weight rows split between the two
     // CTAs) on request, when there are at least two pixel tiles to pair up.
-    t.pair = (t.num_m_tiles >= 2 && (pl->flags & CONV_FLAG_SM_PAIRS) && !transposed) ? 1 : 0;
+    // SM pairs (one MMA over 2 x 128 pixels, weight rows split between the two CTAs):
+    // on request, else by default where each tile is a long full-width reduction (the
+    // pair halves the weight bytes each SM loads per K-step, which pays when the MMAs
+    // dominate; for short reductions and narrow groups it measured slower)
+    const bool auto_pairs = !one_by_one && gpc == 1 && mma_n == 256 && t.ksteps >= 9;
+    const bool want_pairs = (pl->flags & CONV_FLAG_SM_PAIRS) || (auto_pairs && !(pl->flags & CONV_FLAG_ONE_SM));
+    t.pair = (t.num_m_tiles >= 2 && want_pairs && !transposed) ? 1 : 0;
     const int b_rows = t.pair ? mma_n / 2 : mma_n;
     const int stage_bytes = kTcBlockM * kTcBlockK * 2 + b_rows * 128;
     const int fixed = 1024 + 256 + 8 * 2 * 32 * 64;  // alignment, barriers, epilogue store tiles
@@ -445,8 +451,9 @@ conv_status conv_plan_create(conv_plan** out, int N, int C_in, int H, int W, int
     if (C_in % G != 0 || C_out % G != 0) return CONV_ERR_INVALID_ARG;
     if (dtype != CONV_F32 && dtype != CONV_BF16) return CONV_ERR_INVALID_ARG;
     if (flags & ~(CONV_FLAG_BIAS | CONV_FLAG_RELU | CONV_FLAG_OUT_BF16 | CONV_FLAG_SM_PAIRS | CONV_FLAG_TRANSPOSED |
-                  CONV_FLAG_WINOGRAD))
+                  CONV_FLAG_WINOGRAD | CONV_FLAG_ONE_SM))
         return CONV_ERR_INVALID_ARG;
+    if ((flags & CONV_FLAG_SM_PAIRS) && (flags & CONV_FLAG_ONE_SM)) return CONV_ERR_INVALID_ARG;
     if ((flags & CONV_FLAG_OUT_BF16) && dtype != CONV_F32) return CONV_ERR_INVALID_ARG;
     const bool transposed = (flags & CONV_FLAG_TRANSPOSED) != 0;
     const int Ho = transposed ? out_extent_transposed(H, Kh, S, P, D) : out_extent(H, Kh, S, P, D);

@@ -56,8 +56,13 @@ enum {
     CONV_FLAG_OUT_BF16 = 4u,   /* CONV_F32 only: write y as BF16 (round to nearest even) */
     CONV_FLAG_SM_PAIRS = 8u,   /* tensor-core GEMM paths: run each MMA on an SM pair
                                   (clusters of 2, 256 pixels per MMA, weight rows split
-                                  between the two SMs) instead of one SM per 128 pixels */
+                                  between the two SMs) instead of one SM per 128 pixels.
+                                  Without this flag or CONV_FLAG_ONE_SM the plan picks:
+                                  pairs for ungrouped non-1x1 layers with 256 output
+                                  channels per tile and at least 9 K-steps (taps x
+                                  64-channel blocks), one SM otherwise */
     CONV_FLAG_TRANSPOSED = 16u, /* transposed convolution (see below)                 */
+    CONV_FLAG_ONE_SM = 64u,    /* tensor-core GEMM paths: one SM per 128-pixel tile    */
     CONV_FLAG_WINOGRAD = 32u   /* FP32 3x3, stride 1, dilation 1, G = 1: Winograd F(2x2, 3x3)
                                   ("Convolution vs inner product", lnrq.cn, section 2.2;
                                   variants page, section 3.3): 4 multiplies per output

@@ -51,7 +51,7 @@ def _create(*args):
     (1, 3, 2, 2, 4, 5, 5, 1, 0, 1, 1, 0, 0),        # empty output
     (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 1, 4),        # OUT_BF16 with BF16 input
     (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 2, 0),        # bad dtype
-    (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 64),       # unknown flag
+    (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 256),      # unknown flag
     (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 128),      # unknown flag
     (1, 3, 2, 2, 4, 3, 3, 1, 3, 1, 1, 0, 16),       # transposed with an empty output: (2-1) - 6 + 2 + 1 < 1
 ])
@@ -215,3 +215,21 @@ def test_winograd_kernel_choice(shape, winograd, path):
     *dims, dtype = shape
     p = cg.ConvPlan(*dims, dtype=dtype, bias=True, relu=True, winograd=winograd)
     assert p.path == path
+
+
+@pytest.mark.parametrize("shape,sm_pairs,cluster", [
+    ((32, 128, 112, 112, 256, 3, 3, 1, 1, 1, 1), None, 2),    # body: long full-width reduction -> pairs
+    ((32, 128, 112, 112, 256, 3, 3, 1, 1, 1, 1), False, 1),   # forced one SM
+    ((64, 256, 56, 56, 512, 1, 1, 1, 0, 1, 1), None, 1),      # pointwise: 4 K-steps -> one SM
+    ((64, 256, 56, 56, 512, 1, 1, 1, 0, 1, 1), True, 2),      # forced pairs
+    ((16, 256, 64, 64, 256, 3, 3, 1, 2, 2, 4), None, 1),      # grouped: N = 64 per group -> one SM
+    ((4, 128, 31, 29, 256, 3, 3, 2, 1, 1, 1), None, 2),       # strided (im2col mode), 18 K-steps, 8 tiles
+])
+def test_sm_pair_choice(shape, sm_pairs, cluster):
+    p = cg.ConvPlan(*shape, dtype="bf16", bias=True, relu=True, sm_pairs=sm_pairs)
+    assert p.launch["cluster"] == cluster
+
+
+def test_sm_pair_flags_are_exclusive():
+    st, h = _create(1, 128, 8, 8, 256, 3, 3, 1, 1, 1, 1, 1, 8 | 64)
+    assert st == 1 and h.value is None

@@ -67,11 +67,13 @@ def test_stem_full_size_all_outputs():
     check_full(s, y, oracle_full(s, x, w, b))
 
 
-def test_body_full_size_sm_pairs_kernel():
-    """The SM-pair kernel on the full body layer: seeded points."""
+def test_body_full_size_one_sm_kernel():
+    """The one-SM-per-tile kernel on the full body layer (the plan's own choice there is SM
+    pairs): seeded points."""
     from cnn_convolution_implicit_gb300 import ConvPlan
     s, x, w, b = inputs("body")
-    plan, y = run(s, x, w, b, plan=ConvPlan.for_shape(s, sm_pairs=True))
+    plan, y = run(s, x, w, b, plan=ConvPlan.for_shape(s, sm_pairs=False))
+    assert plan.launch["cluster"] == 1
     check_points(s, y, x, w, b, sample_points(s, 4096, 13))
 
 
