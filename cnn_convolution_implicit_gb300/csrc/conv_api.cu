@@ -123,6 +123,9 @@ bool phase_axis(int K, int S, int P, int D, TcPhaseAxis& a) {
 }
 
 // tcgen05 GEMM configuration; false when the shape does not fit it.
+// Narrowest per-tile N the plan runs on SM pairs by default.
+constexpr int kPairMinN = 256;
+
 bool configure_tc(conv_plan* pl, bool one_by_one, bool transposed = false) {
     const ConvGeom& g = pl->g;
     TcGemmParams& t = pl->tc;
@@ -212,12 +215,26 @@ bool configure_tc(conv_plan* pl, bool one_by_one, bool transposed = false) {
     // SM pairs (one MMA over 2 x 128 pixels, weight rows split between the two
     // CTAs) on request, when there are at least two pixel tiles to pair up.
     // SM pairs (one MMA over 2 x 128 pixels, weight rows split between the two CTAs):
-    // on request, else by default where each tile is a long full-width reduction (the
-    // pair halves the weight bytes each SM loads per K-step, which pays when the MMAs
-    // dominate; for short reductions and narrow groups it measured slower)
-    const bool auto_pairs = !one_by_one && gpc == 1 && mma_n == 256 && t.ksteps >= 9;
+    // on request, else by default where each tile is a long reduction over a wide tile
+    // (a pair doubles the MMA work per K-step its producers issue, which pays when
+    // the MMAs dominate; for short reductions and narrow groups it measured slower)
+    int min_ksteps = t.ksteps;
+    if (transposed) {  // the shortest phase's reduction
+        int ch = 64, cw = 64;
+        for (int r = 0; r < t.ps; ++r) {
+            ch = t.ph.cnt[r] < ch ? t.ph.cnt[r] : ch;
+            cw = t.pw.cnt[r] < cw ? t.pw.cnt[r] : cw;
+        }
+        min_ksteps = ch * cw * t.kblk;
+    }
+    const bool auto_pairs = !one_by_one && gpc == 1 && mma_n >= kPairMinN && min_ksteps >= 9;
     const bool want_pairs = (pl->flags & CONV_FLAG_SM_PAIRS) || (auto_pairs && !(pl->flags & CONV_FLAG_ONE_SM));
-    t.pair = (t.num_m_tiles >= 2 && want_pairs && !transposed) ? 1 : 0;
+    t.pair = (t.num_m_tiles >= 2 && want_pairs) ? 1 : 0;
+    if (t.pair && transposed) {  // pairs of one phase: round each phase's tile count up to even
+        const long long spatial = static_cast<long long>(g.N) * t.rect_tiles_w * t.rect_tiles_h;
+        t.num_m_tiles = static_cast<int>(((spatial + 1) / 2) * 2 * t.ps * t.ps);
+        t.num_tiles = t.num_m_tiles * t.num_n_tiles;
+    }
     const int b_rows = t.pair ? mma_n / 2 : mma_n;
     const int stage_bytes = kTcBlockM * kTcBlockK * 2 + b_rows * 128;
     const int fixed = 1024 + 256 + 8 * 2 * 32 * 64;  // alignment, barriers, epilogue store tiles

@@ -100,18 +100,26 @@ struct PixTile {
     bool exists;  // m is a real tile (the pair kernel may run one past the end)
 };
 
-template <bool PHASE>
+template <bool PHASE, bool PAIR = false>
 __device__ __forceinline__ PixTile pix_tile(const TcGemmParams& p, int m) {
     PixTile t;
     t.exists = m < p.num_m_tiles;
     t.rh = t.rw = 0;
     if constexpr (PHASE) {  // phases fastest: neighbouring tiles read the same input rectangle
         const int nph = p.ps * p.ps;
-        const int ph = m % nph;
+        const int per_img = p.rect_tiles_h * p.rect_tiles_w;
+        int ph, q;
+        if constexpr (PAIR) {  // a pair is two neighbouring tiles of one phase (one tap list for both)
+            const int pr = m >> 1;
+            ph = pr % nph;
+            q = (pr / nph) * 2 + (m & 1);
+            t.exists = t.exists && q < p.g.N * per_img;  // an odd tile count leaves one tile unpaired
+        } else {
+            ph = m % nph;
+            q = m / nph;
+        }
         t.rh = ph / p.ps;
         t.rw = ph - t.rh * p.ps;
-        const int per_img = p.rect_tiles_h * p.rect_tiles_w;
-        const int q = m / nph;
         t.n = q / per_img;
         const int r = q - t.n * per_img;
         const int th = r / p.rect_tiles_w;
@@ -242,8 +250,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int mu = u / p.num_n_tiles;
                 const int nt = u - mu * p.num_n_tiles;
                 const int m = PAIR ? 2 * mu + static_cast<int>(rank) : mu;
-                PixTile t = pix_tile<PHASE>(p, m);
-                if (!t.exists) t = pix_tile<PHASE>(p, p.num_m_tiles - 1);  // a valid tile whose result is never stored
+                PixTile t = pix_tile<PHASE, PAIR>(p, m);
+                // a missing tile loads a valid one whose result is never stored (phase mode: its own
+                // coordinates, past the last image, which read as zeros: its phase stays its pair's)
+                if (!t.exists && !PHASE) t = pix_tile<PHASE, PAIR>(p, p.num_m_tiles - 1);
                 const int ksteps = tile_ksteps<PHASE>(p, t.rh, t.rw);
                 for (int j = 0; j < p.gpc && ok; ++j) {
                     int grp, brow;
@@ -411,7 +421,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int mu = u / p.num_n_tiles;
             const int nt = u - mu * p.num_n_tiles;
             const int m = PAIR ? 2 * mu + static_cast<int>(rank) : mu;
-            const PixTile t = pix_tile<PHASE>(p, m);
+            const PixTile t = pix_tile<PHASE, PAIR>(p, m);
             // this warp's 32 pixels: rect mode = 32/TW rows of the rectangle, else 32 linear pixels
             bool rows_exist;
             int yc1, yc2, yc3;
@@ -492,8 +502,12 @@ static int g_pair_smem_limits[64] = {};
 cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, const CUtensorMap& y_map,
                            const TcGemmParams& p, int grid, cudaStream_t stream) {
     if (p.pair) {
-        cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<true, false>), p.smem_bytes,
-                                          g_pair_smem_limits);
+        static int pair_phase_limits[64] = {};
+        cudaError_t e = p.mode == kTcModePhase
+                            ? ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<true, true>), p.smem_bytes,
+                                                pair_phase_limits)
+                            : ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<true, false>),
+                                                p.smem_bytes, g_pair_smem_limits);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid, 1, 1);
@@ -507,7 +521,8 @@ cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, c
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, tc_conv_kernel<true, false>, a_map, b_map, y_map, p);
+        e = p.mode == kTcModePhase ? cudaLaunchKernelEx(&cfg, tc_conv_kernel<true, true>, a_map, b_map, y_map, p)
+                                   : cudaLaunchKernelEx(&cfg, tc_conv_kernel<true, false>, a_map, b_map, y_map, p);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }

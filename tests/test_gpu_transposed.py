@@ -29,12 +29,14 @@ CASES = [
 ]
 
 
-def _run_case(case, seed, scale=False):
+def _run_case(case, seed, scale=False, sm_pairs=None):
     from cnn_convolution_implicit_gb300 import ConvPlan, device_status
     N, C_in, H, W, C_out, K, S, P, D, G, dtype, bias, relu, path = case
     s = ConvShape(N, C_in, H, W, C_out, K, K, S, P, D, G, dtype, bias, relu, transposed=True)
     x, w, b = draw(s, (seed, seed + 1, seed + 2))
-    plan = ConvPlan.for_shape(s)
+    plan = ConvPlan.for_shape(s, sm_pairs=sm_pairs)
+    if sm_pairs and path == "implicit_gemm":
+        assert plan.launch["cluster"] == 2
     assert plan.path == path, (plan.path, path)
     assert (plan.H_out, plan.W_out) == (s.H_out, s.W_out)
     sc = np.random.default_rng(seed + 3).uniform(-2, 2, C_out).astype(np.float32) if scale else None
@@ -58,6 +60,14 @@ def _run_case(case, seed, scale=False):
     c[10], c[5], c[6], c[7], c[8], c[9], c[2], c[3], c[13]))
 def test_transposed_matches_oracle(case):
     _run_case(case, 8100 + case[2] * 7 + case[5])
+
+
+@pytest.mark.parametrize("case", [c for c in CASES if c[13] == "implicit_gemm" and c[9] == 1],
+                         ids=lambda c: "pairs_K%dS%dP%dD%d_%dx%d" % (c[5], c[6], c[7], c[8], c[2], c[3]))
+def test_transposed_sm_pairs(case):
+    """The phase mode on SM pairs (forced): both tiles of a pair are neighbours in one phase,
+    an odd tile count leaves one tile paired with an empty one."""
+    _run_case(case, 8300 + case[2] * 5 + case[6], sm_pairs=True)
 
 
 def test_transposed_affine_epilogue():
