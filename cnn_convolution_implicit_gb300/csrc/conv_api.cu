@@ -125,6 +125,8 @@ bool phase_axis(int K, int S, int P, int D, TcPhaseAxis& a) {
 // tcgen05 GEMM configuration; false when the shape does not fit it.
 // Narrowest per-tile N the plan runs on SM pairs by default.
 constexpr int kPairMinN = 256;
+// Widest per-tile N that runs two pixel tiles per CTA.
+constexpr int kDualMaxN = 128;
 
 bool configure_tc(conv_plan* pl, bool one_by_one, bool transposed = false) {
     const ConvGeom& g = pl->g;
@@ -230,20 +232,24 @@ bool configure_tc(conv_plan* pl, bool one_by_one, bool transposed = false) {
     const bool auto_pairs = !one_by_one && gpc == 1 && mma_n >= kPairMinN && min_ksteps >= 9;
     const bool want_pairs = (pl->flags & CONV_FLAG_SM_PAIRS) || (auto_pairs && !(pl->flags & CONV_FLAG_ONE_SM));
     t.pair = (t.num_m_tiles >= 2 && want_pairs) ? 1 : 0;
-    if (t.pair && transposed) {  // pairs of one phase: round each phase's tile count up to even
+    // Two pixel tiles per CTA (M = 256 on one SM) for narrow tiles with a real
+    // reduction: each K-step then feeds twice the tensor work for one weight block and
+    // one more A copy (a 2-K-step 1x1 layer measured slower: its epilogue dominates).
+    t.dual = (!t.pair && gpc == 1 && n_tile <= kDualMaxN && t.num_m_tiles >= 2 && min_ksteps >= 4) ? 1 : 0;
+    if ((t.pair || t.dual) && transposed) {  // both tiles of a unit in one phase: round each phase's count up
         const long long spatial = static_cast<long long>(g.N) * t.rect_tiles_w * t.rect_tiles_h;
         t.num_m_tiles = static_cast<int>(((spatial + 1) / 2) * 2 * t.ps * t.ps);
         t.num_tiles = t.num_m_tiles * t.num_n_tiles;
     }
     const int b_rows = t.pair ? mma_n / 2 : mma_n;
-    const int stage_bytes = kTcBlockM * kTcBlockK * 2 + b_rows * 128;
+    const int stage_bytes = (t.dual ? 2 : 1) * kTcBlockM * kTcBlockK * 2 + b_rows * 128;
     const int fixed = 1024 + 256 + 8 * 2 * 32 * 64;  // alignment, barriers, epilogue store tiles
     int stages = (pl->smem_optin - fixed) / stage_bytes;
     if (stages > 8) stages = 8;
     if (stages < 2 || stages < gpc) return false;
     t.stages = stages;
     t.smem_bytes = fixed + stages * stage_bytes;
-    t.tmem_cols = pow2_at_least(2 * n_tile);
+    t.tmem_cols = pow2_at_least((t.dual ? 4 : 2) * n_tile);
     t.relu = (pl->flags & CONV_FLAG_RELU) ? 1 : 0;
     t.status = pl->status;
     return true;
@@ -578,6 +584,9 @@ conv_status conv_plan_launch_info(const conv_plan* p, int* grid, int* block, int
                 if (clusters > pair_tiles) clusters = pair_tiles;
                 gr = 2 * clusters;
                 cl = 2;
+            } else if (t.dual) {
+                const int units = ((t.num_m_tiles + 1) / 2) * t.num_n_tiles;
+                gr = units < p->num_sms ? units : p->num_sms;
             } else {
                 gr = t.num_tiles < p->num_sms ? t.num_tiles : p->num_sms;
             }

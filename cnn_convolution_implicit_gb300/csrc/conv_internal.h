@@ -122,6 +122,7 @@ struct TcGemmParams {
     int tmem_cols;     // power of two >= 2 * n_tile
     int smem_bytes;
     int pair;          // 1: CTA-pair kernel (B rows split across the two CTAs)
+    int dual;          // 1: two pixel tiles per CTA (M = 256, two accumulators; n_tile <= 128)
     int ps;            // kTcModePhase: the transposed convolution's stride S (phases = S*S)
     int hq, wq;        // kTcModePhase: output rows / columns per phase (H_out / S, W_out / S)
     TcPhaseAxis ph, pw;

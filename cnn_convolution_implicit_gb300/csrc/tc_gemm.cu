@@ -63,11 +63,11 @@ struct TcSmem {
     int* abort;
 };
 
-__device__ __forceinline__ TcSmem carve(uint8_t* raw, const TcGemmParams& p, uint32_t b_bytes) {
+__device__ __forceinline__ TcSmem carve(uint8_t* raw, const TcGemmParams& p, uint32_t a_bytes, uint32_t b_bytes) {
     TcSmem s;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.a = base;
-    s.b = base + p.stages * kABytes;
+    s.b = base + p.stages * a_bytes;
     s.out = s.b + p.stages * b_bytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(s.out + 8 * 2 * kOutTileBytes);
     s.full = bars;
@@ -189,14 +189,20 @@ __device__ __forceinline__ void load_a(const TcGemmParams& p, const CUtensorMap*
 
 // PHASE: the transposed-convolution phase mode (kTcModePhase), compiled
 // separately so the convolution modes keep their own loops.
-template <bool PAIR, bool PHASE>
+// DUAL: two pixel tiles per CTA (M = 256 on one SM) for tiles of at most 128
+// output channels: each K-step loads both tiles' A operands and one weight
+// block and issues the MMAs of both into two accumulators, so the producer's
+// per-K-step work feeds twice the tensor work.
+template <bool PAIR, bool PHASE, bool DUAL>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_conv_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
                    const __grid_constant__ CUtensorMap y_map, const TcGemmParams p) {
     extern __shared__ uint8_t smem_raw[];
+    constexpr bool TWO = PAIR || DUAL;                   // work units of two pixel tiles
+    constexpr uint32_t a_stage = DUAL ? 2 * kABytes : kABytes;
     const int b_rows = PAIR ? p.mma_n / 2 : p.mma_n;  // weight rows this CTA loads per K-step
     const uint32_t b_bytes = static_cast<uint32_t>(b_rows) * 128u;
-    const TcSmem sm = carve(smem_raw, p, b_bytes);
+    const TcSmem sm = carve(smem_raw, p, a_stage, b_bytes);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     volatile int* abort = sm.abort;
@@ -205,7 +211,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // work units: a tile (single) or a pair of adjacent pixel tiles (PAIR)
     const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
     const int unit_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-    const int num_units = PAIR ? ((p.num_m_tiles + 1) / 2) * p.num_n_tiles : p.num_tiles;
+    const int num_units = TWO ? ((p.num_m_tiles + 1) / 2) * p.num_n_tiles : p.num_tiles;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -245,15 +251,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
-            const uint32_t a_b_bytes = (PAIR ? 2u : 1u) * (kABytes + b_bytes);
+            const uint32_t a_b_bytes = PAIR ? 2u * (kABytes + b_bytes) : a_stage + b_bytes;
             for (int u = unit0; u < num_units && ok; u += unit_step) {
                 const int mu = u / p.num_n_tiles;
                 const int nt = u - mu * p.num_n_tiles;
-                const int m = PAIR ? 2 * mu + static_cast<int>(rank) : mu;
-                PixTile t = pix_tile<PHASE, PAIR>(p, m);
+                const int m = PAIR ? 2 * mu + static_cast<int>(rank) : (DUAL ? 2 * mu : mu);
+                PixTile t = pix_tile<PHASE, TWO>(p, m);
                 // a missing tile loads a valid one whose result is never stored (phase mode: its own
                 // coordinates, past the last image, which read as zeros: its phase stays its pair's)
-                if (!t.exists && !PHASE) t = pix_tile<PHASE, PAIR>(p, p.num_m_tiles - 1);
+                if (!t.exists && !PHASE) t = pix_tile<PHASE, TWO>(p, p.num_m_tiles - 1);
+                PixTile t1 = t;  // DUAL: the second tile of the unit
+                if constexpr (DUAL) {
+                    t1 = pix_tile<PHASE, true>(p, m + 1);
+                    if (!t1.exists && !PHASE) t1 = t;
+                }
                 const int ksteps = tile_ksteps<PHASE>(p, t.rh, t.rw);
                 for (int j = 0; j < p.gpc && ok; ++j) {
                     int grp, brow;
@@ -298,11 +309,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             }
                         }
                         const int c = grp * p.g.cin_g + kb * kTcBlockK;
-                        uint8_t* a_dst = sm.a + stage * kABytes;
+                        uint8_t* a_dst = sm.a + stage * a_stage;
                         uint8_t* b_dst = sm.b + stage * b_bytes;
                         const uint32_t full_leader = PAIR ? mapa_shared(smem_addr(&sm.full[stage]), 0) : 0u;
                         if (leader) mbar_arrive_expect_tx(&sm.full[stage], a_b_bytes);
                         load_a<PAIR, PHASE>(p, &a_map, a_dst, &sm.full[stage], full_leader, t, c, tp);
+                        if constexpr (DUAL) load_a<PAIR, PHASE>(p, &a_map, a_dst + kABytes, &sm.full[stage], 0u, t1, c, tp);
                         const int kcol = tp.wtap * p.g.cin_g + kb * kTcBlockK;
                         if constexpr (PAIR)
                             tma_load_2d_pair(b_dst, &b_map, full_leader, kcol, brow + static_cast<int>(rank) * b_rows);
@@ -345,7 +357,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_base = tmem_base + static_cast<uint32_t>(buf * p.n_tile);
+                const uint32_t d_base = tmem_base + static_cast<uint32_t>(buf * (DUAL ? 2 : 1) * p.n_tile);
                 int ksteps = p.ksteps;
                 if constexpr (PHASE) {  // the phase of tile m (no pairs in this mode)
                     const int ph = (u / p.num_n_tiles) % (p.ps * p.ps);
@@ -360,7 +372,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t adesc = sdesc_sw128(smem_addr(sm.a + stage * kABytes));
+                        const uint64_t adesc = sdesc_sw128(smem_addr(sm.a + stage * a_stage));
                         const uint64_t bdesc = sdesc_sw128(smem_addr(sm.b + stage * b_bytes));
 #pragma unroll
                         for (int k = 0; k < kTcBlockK / 16; ++k) {
@@ -369,6 +381,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                 mma_bf16_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
                             else
                                 mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
+                        }
+                        if constexpr (DUAL) {  // the unit's second tile: A at +16 KB, its own accumulator
+                            const uint64_t adesc1 = sdesc_sw128(smem_addr(sm.a + stage * a_stage + kABytes));
+#pragma unroll
+                            for (int k = 0; k < kTcBlockK / 16; ++k)
+                                mma_bf16(d + static_cast<uint32_t>(p.n_tile), adesc1 + 2 * k, bdesc + 2 * k, idesc,
+                                         (ks | k) != 0 ? 1u : 0u);
                         }
                         if constexpr (PAIR)
                             mma_commit_pair(&sm.empty[stage], 0x3);
@@ -420,8 +439,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_after();
             const int mu = u / p.num_n_tiles;
             const int nt = u - mu * p.num_n_tiles;
-            const int m = PAIR ? 2 * mu + static_cast<int>(rank) : mu;
-            const PixTile t = pix_tile<PHASE, PAIR>(p, m);
+            // DUAL: group half h drains tile h of the unit (all its columns)
+            const int m = PAIR ? 2 * mu + static_cast<int>(rank) : (DUAL ? 2 * mu + chalf : mu);
+            const PixTile t = pix_tile<PHASE, TWO>(p, m);
             // this warp's 32 pixels: rect mode = 32/TW rows of the rectangle, else 32 linear pixels
             bool rows_exist;
             int yc1, yc2, yc3;
@@ -445,11 +465,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             const int co0 = nt * p.n_tile;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                   static_cast<uint32_t>(buf * p.n_tile);
+                                   static_cast<uint32_t>(buf * (DUAL ? 2 : 1) * p.n_tile + (DUAL ? chalf * p.n_tile : 0));
             // this group's half of the columns, 32 per step, one staging tile per warp
             const int chunks = p.n_tile / 32;
-            const int c_lo = chalf == 0 ? 0 : ((chunks + 1) / 2) * 32;
-            const int c_hi = chalf == 0 ? ((chunks + 1) / 2) * 32 : p.n_tile;
+            const int c_lo = DUAL ? 0 : (chalf == 0 ? 0 : ((chunks + 1) / 2) * 32);
+            const int c_hi = DUAL ? p.n_tile : (chalf == 0 ? ((chunks + 1) / 2) * 32 : p.n_tile);
             for (int c = c_lo; c < c_hi; c += 32) {
                 uint32_t v[32];
                 __syncwarp();
@@ -504,9 +524,9 @@ cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, c
     if (p.pair) {
         static int pair_phase_limits[64] = {};
         cudaError_t e = p.mode == kTcModePhase
-                            ? ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<true, true>), p.smem_bytes,
+                            ? ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<true, true, false>), p.smem_bytes,
                                                 pair_phase_limits)
-                            : ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<true, false>),
+                            : ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<true, false, false>),
                                                 p.smem_bytes, g_pair_smem_limits);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
@@ -521,29 +541,42 @@ cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, c
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = p.mode == kTcModePhase ? cudaLaunchKernelEx(&cfg, tc_conv_kernel<true, true>, a_map, b_map, y_map, p)
-                                   : cudaLaunchKernelEx(&cfg, tc_conv_kernel<true, false>, a_map, b_map, y_map, p);
+        e = p.mode == kTcModePhase ? cudaLaunchKernelEx(&cfg, tc_conv_kernel<true, true, false>, a_map, b_map, y_map, p)
+                                   : cudaLaunchKernelEx(&cfg, tc_conv_kernel<true, false, false>, a_map, b_map, y_map, p);
         if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
+    if (p.dual) {  // two pixel tiles per CTA
+        static int dual_limits[64] = {}, dual_phase_limits[64] = {};
+        const bool ph = p.mode == kTcModePhase;
+        const void* fn = ph ? reinterpret_cast<const void*>(tc_conv_kernel<false, true, true>)
+                            : reinterpret_cast<const void*>(tc_conv_kernel<false, false, true>);
+        cudaError_t e = ensure_smem_limit(fn, p.smem_bytes, ph ? dual_phase_limits : dual_limits);
+        if (e != cudaSuccess) return e;
+        if (ph)
+            tc_conv_kernel<false, true, true><<<grid, kTcThreads, p.smem_bytes, stream>>>(a_map, b_map, y_map, p);
+        else
+            tc_conv_kernel<false, false, true><<<grid, kTcThreads, p.smem_bytes, stream>>>(a_map, b_map, y_map, p);
         return cudaGetLastError();
     }
     if (p.mode == kTcModePhase) {
         static int phase_limits[64] = {};
-        cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<false, true>), p.smem_bytes,
+        cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<false, true, false>), p.smem_bytes,
                                           phase_limits);
         if (e != cudaSuccess) return e;
-        tc_conv_kernel<false, true><<<grid, kTcThreads, p.smem_bytes, stream>>>(a_map, b_map, y_map, p);
+        tc_conv_kernel<false, true, false><<<grid, kTcThreads, p.smem_bytes, stream>>>(a_map, b_map, y_map, p);
         return cudaGetLastError();
     }
     static int limits[64] = {};
     cudaError_t e =
-        ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<false, false>), p.smem_bytes, limits);
+        ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<false, false, false>), p.smem_bytes, limits);
     if (e != cudaSuccess) return e;
-    tc_conv_kernel<false, false><<<grid, kTcThreads, p.smem_bytes, stream>>>(a_map, b_map, y_map, p);
+    tc_conv_kernel<false, false, false><<<grid, kTcThreads, p.smem_bytes, stream>>>(a_map, b_map, y_map, p);
     return cudaGetLastError();
 }
 
 int tc_gemm_pair_max_clusters(const TcGemmParams& p) {
-    if (ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<true, false>), p.smem_bytes,
+    if (ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<true, false, false>), p.smem_bytes,
                           g_pair_smem_limits) != cudaSuccess) {
         cudaGetLastError();
         return 0;
@@ -560,7 +593,7 @@ int tc_gemm_pair_max_clusters(const TcGemmParams& p) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_conv_kernel<true, false>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, tc_conv_kernel<true, false, false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
