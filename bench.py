@@ -545,6 +545,11 @@ def main():
                                                                   peaks)
 
     traffic = load_traffic()
+    for key, r in others.items():  # ncu DRAM bytes per launch where the summary matches the current source
+        tkey = "winograd" if r.get("kernel") == "winograd" else key.split("+")[0]
+        tl = traffic.get(tkey)
+        if tkey in KERNEL_SOURCES and not key.endswith("+affine"):
+            r["traffic"] = tl[0] if tl and tl[1] == kernel_source_hash(tkey) else None
     tr = traffic.get("body")
     roofline = {"bound": "tensor", "achieved": kern_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": kern_tflops / peaks["bf16_tflops"],

@@ -613,10 +613,12 @@ conv_status conv_plan_launch_info(const conv_plan* p, int* grid, int* block, int
             gr = p->dw.grid;
             break;
         default: {
-            const long long total = p->g.pixels * p->g.C_out;
-            const long long blocks = (total + 255) / 256;
-            gr = static_cast<int>(blocks < (1ll << 20) ? blocks : (1ll << 20));
-            bl = 256;
+            int tile_m = 0;
+            unsigned gx = 0, gy = 0;
+            direct_shape(p->g, p->num_sms, tile_m, gx, gy, bl);
+            const long long blocks = static_cast<long long>(gx) * gy;
+            gr = static_cast<int>(blocks < 0x7fffffffLL ? blocks : 0x7fffffffLL);
+            sm = tile_m == 0 ? 0 : 2 * kDtChunk * (tile_m + 4 + kDtTileN + 4) * 4;  // static shared memory
             break;
         }
     }
@@ -721,7 +723,8 @@ conv_status forward_impl(conv_plan* p, const void* x, const void* w, const float
             d.in_bf16 = p->dtype == CONV_BF16 ? 1 : 0;
             d.out_bf16 = (p->dtype == CONV_BF16 || (p->flags & CONV_FLAG_OUT_BF16)) ? 1 : 0;
             d.transposed = (p->flags & CONV_FLAG_TRANSPOSED) ? 1 : 0;
-            e = launch_direct(d, st);
+            d.tile_m = 0;  // chosen by the launcher
+            e = launch_direct(d, p->num_sms, st);
             break;
         }
     }

@@ -44,8 +44,15 @@ struct DirectParams {
     int in_bf16;     // x, w are BF16 (else FP32)
     int out_bf16;    // y is BF16 (else FP32)
     int transposed;  // transposed convolution (gather form): x is the H x W input, y the H_out x W_out output
+    int tile_m;      // 0: one thread per output; 64 or 128: register-tiled kernel with that many pixels per CTA
 };
-cudaError_t launch_direct(const DirectParams& p, cudaStream_t stream);
+// Register-tiled direct kernel: a CTA computes kDtTileN output channels of one
+// group for tile_m output pixels, the reduction in chunks of kDtChunk channels of one tap.
+constexpr int kDtTileN = 64;
+constexpr int kDtChunk = 8;
+// Launch shape of the direct path: tile_m as above, the grid and block size.
+void direct_shape(const ConvGeom& g, int num_sms, int& tile_m, unsigned& gx, unsigned& gy, int& block);
+cudaError_t launch_direct(const DirectParams& p, int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------------- Winograd F(2x2, 3x3) (FP32)
 constexpr int kWgThreads = 256;

@@ -24,6 +24,7 @@ def run_affine(s, x, w, b, sc, plan=None):
 @pytest.mark.parametrize("shape,path", [
     (ConvShape(2, 5, 9, 11, 6, 3, 3, 1, 1, 1, 1, "f32", True, True), "direct"),
     (ConvShape(2, 8, 9, 7, 8, 3, 3, 2, 1, 2, 2, "bf16", True, False), "direct"),
+    (ConvShape(2, 8, 9, 7, 48, 3, 3, 1, 1, 1, 1, "f32", True, True), "direct"),   # register-tiled kernel
     (ConvShape(2, 64, 17, 19, 64, 3, 3, 1, 1, 1, 64, "f32", True, True), "depthwise"),
     (ConvShape(2, 64, 17, 19, 64, 3, 3, 1, 1, 1, 64, "f32", False, False), "depthwise"),
     (ConvShape(2, 128, 13, 11, 256, 3, 3, 1, 1, 1, 1, "bf16", True, True), "implicit_gemm"),

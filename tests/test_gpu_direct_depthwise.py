@@ -29,6 +29,27 @@ def test_direct_random_sweep(dtype):
         check_full(s, y, oracle_full(s, x, w, b))
 
 
+@pytest.mark.parametrize("shape,tile_m", [
+    # register-tiled direct kernel: >= 32 output channels per group
+    (ConvShape(2, 16, 13, 11, 32, 3, 3, 1, 1, 1, 1, "f32", True, True), 64),      # half a channel block
+    (ConvShape(3, 13, 17, 19, 96, 3, 3, 2, 1, 1, 1, "f32", True, False), 64),     # ragged chunk, scalar loads
+    (ConvShape(2, 64, 20, 20, 64, 3, 3, 1, 2, 2, 2, "f32", True, True), 64),      # 2 groups, dilation 2
+    (ConvShape(1, 24, 9, 9, 40, 5, 5, 1, 2, 1, 1, "bf16", True, True), 64),       # BF16, C_out % 16 != 0
+    (ConvShape(2, 6, 10, 10, 36, 1, 1, 1, 0, 1, 1, "f32", False, False), 64),     # 1x1, 36 channels
+    (ConvShape(2, 8, 9, 7, 48, 3, 3, 1, 1, 1, 1, "f32", True, True, out_bf16=True), 64),  # FP32 in, BF16 out
+    (ConvShape(4, 8, 100, 100, 32, 3, 3, 1, 1, 1, 1, "f32", True, True), 128),    # 128-pixel tiles
+    (ConvShape(2, 12, 130, 121, 70, 3, 3, 1, 1, 1, 1, "f32", True, False), 128),  # 128 pixels, odd channels
+])
+def test_direct_tiled_kernel(shape, tile_m):
+    """Every output of the register-tiled direct kernel: both pixel-tile sizes, ragged
+    pixel tails, partial channel blocks and reduction chunks, groups, BF16 in and out."""
+    x, w, b = draw(shape, (400, 401, 402), "normal", "kaiming", "uniform")
+    plan, y = run(shape, x, w, b)
+    assert plan.path == "direct"
+    assert plan.launch["block"] == 2 * tile_m, plan.launch
+    check_full(shape, y, oracle_full(shape, x, w, b))
+
+
 def test_depthwise_full_size_layer():
     """N=64, C=256, 56x56, depthwise 3x3 s1 p1 FP32: every output (0.46 G MACs in FP64)."""
     s, x, w, b = inputs("dw")

@@ -26,6 +26,8 @@ CASES = [
     (2, 96, 5, 5, 32, 4, 2, 1, 1, 1, "bf16", True, True, "direct"),            # C_in % 64 != 0
     (1, 3, 8, 8, 8, 4, 2, 1, 1, 1, "f32", True, False, "direct"),              # FP32
     (2, 8, 5, 6, 12, 3, 2, 0, 2, 4, "f32", True, True, "direct"),              # FP32 groups + dilation
+    (2, 16, 7, 7, 40, 4, 2, 1, 1, 1, "f32", True, True, "direct"),             # FP32, register-tiled kernel
+    (1, 24, 6, 5, 64, 3, 3, 1, 2, 2, "f32", True, False, "direct"),            # FP32 tiled, 2 groups, S = 3
 ]
 
 
