@@ -49,7 +49,7 @@ struct DirectParams {
 // Register-tiled direct kernel: a CTA computes kDtTileN output channels of one
 // group for tile_m output pixels, the reduction in chunks of kDtChunk channels of one tap.
 constexpr int kDtTileN = 64;
-constexpr int kDtChunk = 8;
+constexpr int kDtChunk = 16;
 // Launch shape of the direct path: tile_m as above, the grid and block size.
 void direct_shape(const ConvGeom& g, int num_sms, int& tile_m, unsigned& gx, unsigned& gy, int& block);
 cudaError_t launch_direct(const DirectParams& p, int num_sms, cudaStream_t stream);

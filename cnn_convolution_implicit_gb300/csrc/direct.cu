@@ -13,7 +13,7 @@
 // form of the same sums (lesson 9, section 11: output-stationary tiling with
 // the operands staged in shared memory): a CTA owns 64 or 128 output pixels x
 // 64 output channels of one group, each thread 8 pixels x 4 channels in
-// registers; the reduction runs tap by tap in chunks of 8 input channels,
+// registers; the reduction runs tap by tap in chunks of 16 input channels,
 // double-buffered in shared memory, so every staged input value feeds 64 FMAs
 // of its CTA and every staged weight 64 or 128.
 //
@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(2 * BM) direct_tiled_kernel(const DirectParams
     constexpr int kPitchA = BM + 4;        // row pitch (floats): the two loader halves land 16 banks apart
     constexpr int kPitchB = kDtTileN + 4;  // the 8 rows of one warp's weight stores land 4 banks apart
     constexpr int kBLoads = kDtTileN * kDtChunk / kThreads;
+    constexpr int kALoads = kDtChunk / 2;  // channels of the chunk each loader thread fetches
     __shared__ __align__(16) float As[2][kDtChunk][kPitchA];
     __shared__ __align__(16) float Bs[2][kDtChunk][kPitchB];
     const ConvGeom& g = p.g;
@@ -152,9 +153,9 @@ __global__ void __launch_bounds__(2 * BM) direct_tiled_kernel(const DirectParams
     const int grp = blockIdx.y / co_blocks;
     const int cb0 = (blockIdx.y - grp * co_blocks) * kDtTileN;  // first output channel (within the group)
 
-    // loader role: one pixel of the tile, 4 of the chunk's 8 channels
+    // loader role: one pixel of the tile, half of the chunk's channels
     const int lp = tid >> 1;
-    const int lc = (tid & 1) * 4;
+    const int lc = (tid & 1) * kALoads;
     const long long lpix = pix0 + lp;
     const bool lpix_ok = lpix < g.pixels;
     int ln = 0, lho = 0, lwo = 0;
@@ -168,28 +169,30 @@ __global__ void __launch_bounds__(2 * BM) direct_tiled_kernel(const DirectParams
     const long long w_per_co = static_cast<long long>(g.Kh) * g.Kw * g.cin_g;
     const Tin* wg = w + static_cast<long long>(grp) * g.cout_g * w_per_co;
 
-    float ra[4], rb[kBLoads];
+    float ra[kALoads], rb[kBLoads];
     auto fetch = [&](int kh, int kw, int ci0) {
         const Tin* src = nullptr;
         int hi, wi;
         if (lpix_ok && source_pixel(g, p.transposed != 0, lho, lwo, kh, kw, hi, wi))
             src = xg + ((static_cast<long long>(ln) * g.H + hi) * g.W + wi) * g.C_in;
-        load4(src, ci0 + lc, g.cin_g, vec_x != 0, ra);
+#pragma unroll
+        for (int i = 0; i < kALoads; i += 4)
+            load4(src, ci0 + lc + i, g.cin_g, vec_x != 0, *reinterpret_cast<float(*)[4]>(ra + i));
         const int tap = kh * g.Kw + kw;
 #pragma unroll
         for (int i = 0; i < kBLoads; ++i) {
             const int e = tid + i * kThreads;
-            const int co = cb0 + (e >> 3), ci = ci0 + (e & 7);
+            const int co = cb0 + e / kDtChunk, ci = ci0 + e % kDtChunk;
             rb[i] = (co < g.cout_g && ci < g.cin_g) ? to_f32(wg[co * w_per_co + tap * g.cin_g + ci]) : 0.f;
         }
     };
     auto stash = [&](int buf) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) As[buf][lc + i][lp] = ra[i];
+        for (int i = 0; i < kALoads; ++i) As[buf][lc + i][lp] = ra[i];
 #pragma unroll
         for (int i = 0; i < kBLoads; ++i) {
             const int e = tid + i * kThreads;
-            Bs[buf][e & 7][e >> 3] = rb[i];
+            Bs[buf][e % kDtChunk][e / kDtChunk] = rb[i];
         }
     };
 

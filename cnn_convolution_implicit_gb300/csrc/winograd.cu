@@ -19,9 +19,10 @@
 // data for fewer, narrower MMAs.
 //
 // CTA: 4 x 8 Winograd tiles (8 x 16 outputs) of one image x 32 output
-// channels, 256 threads, input channels in chunks of 8:
+// channels, 256 threads, input channels in chunks of 16:
 //   1. the 10 x 18 input patch of the chunk into shared memory (zero outside
-//      the image: the padding);
+//      the image: the padding) by asynchronous copies issued during the
+//      previous chunk's products, into the other of two patch buffers;
 //   2. thread (tile, channel) computes V = B^T d B; thread (filter, channel)
 //      computes U = G g G^T;
 //   3. thread (component xi of 16, 8 tiles, 8 filters) accumulates its 8 x 8
@@ -38,7 +39,7 @@ namespace {
 constexpr int kWgTilesH = 4, kWgTilesW = 8;                    // Winograd tiles per CTA
 constexpr int kWgTiles = kWgTilesH * kWgTilesW;                // 32
 constexpr int kWgCo = 32;                                      // output channels per CTA
-constexpr int kWgCi = 8;                                       // input channels per chunk
+constexpr int kWgCi = 16;                                      // input channels per chunk
 constexpr int kWgPatchH = 2 * kWgTilesH + 2, kWgPatchW = 2 * kWgTilesW + 2;  // 10 x 18 inputs
 constexpr int kWgRow = 36;                                     // floats per (component, channel) row (32 + skew)
 constexpr int kWgMStride = 33;                                 // floats per tile row of M (32 + skew)
@@ -46,13 +47,24 @@ constexpr int kWgPatchFloats = kWgCi * kWgPatchH * kWgPatchW;  // 1440
 constexpr int kWgVFloats = 16 * kWgCi * kWgRow;                // 4608
 constexpr int kWgMFloats = 16 * kWgTiles * kWgMStride;         // 16896
 constexpr int kWgSmemFloats =
-    kWgMFloats > kWgPatchFloats + 2 * kWgVFloats ? kWgMFloats : kWgPatchFloats + 2 * kWgVFloats;
+    kWgMFloats > 2 * kWgPatchFloats + 2 * kWgVFloats ? kWgMFloats : 2 * kWgPatchFloats + 2 * kWgVFloats;
+
+// 4-byte asynchronous global -> shared copy; an invalid source reads nothing and fills zero.
+__device__ __forceinline__ void cp_async_f32(float* dst, const float* src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_addr(dst)), "l"(src),
+                 "r"(valid ? 4 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
 template <typename Tout>
 __global__ void __launch_bounds__(kWgThreads, 2) winograd_kernel(const WinogradParams p) {
     extern __shared__ __align__(16) float smem[];  // kWgSmemFloats
-    float* patch = smem;                   // [ci][10][18]
-    float* Vs = smem + kWgPatchFloats;     // [16][ci][kWgRow]: tiles
+    float* patch = smem;                   // two buffers of [ci][10][18]
+    float* Vs = smem + 2 * kWgPatchFloats; // [16][ci][kWgRow]: tiles
     float* Us = Vs + kWgVFloats;           // [16][ci][kWgRow]: filters
     float* Ms = smem;                      // after the channel loop: [16][tile][kWgMStride]
 
@@ -80,50 +92,31 @@ __global__ void __launch_bounds__(kWgThreads, 2) winograd_kernel(const WinogradP
 
     const float* x = static_cast<const float*>(p.x);
     const float* w = static_cast<const float*>(p.w);
-    for (int c0 = 0; c0 < g.C_in; c0 += kWgCi) {
-        // 1. input patch, channels fastest in global memory (NHWC)
-        for (int e = tid; e < kWgPatchFloats; e += kWgThreads) {
+    // patch element e = tid + i * kWgThreads: channel e % kWgCi of patch pixel e / kWgCi
+    constexpr int kPatchCopies = (kWgPatchFloats + kWgThreads - 1) / kWgThreads;
+    auto issue_patch = [&](int c0, float* dst) {
+#pragma unroll 1
+        for (int i = 0; i < kPatchCopies; ++i) {
+            const int e = tid + i * kWgThreads;
+            if (e >= kWgPatchFloats) break;
             const int ci = e % kWgCi, pix = e / kWgCi;
             const int r = pix / kWgPatchW, q = pix - r * kWgPatchW;
             const int h = in_h0 + r, ww = in_w0 + q, c = c0 + ci;
-            float v = 0.f;
-            if (h >= 0 && h < g.H && ww >= 0 && ww < g.W && c < g.C_in)
-                v = __ldg(x + ((static_cast<long long>(n) * g.H + h) * g.W + ww) * g.C_in + c);
-            patch[ci * (kWgPatchH * kWgPatchW) + pix] = v;
+            const bool ok = h >= 0 && h < g.H && ww >= 0 && ww < g.W && c < g.C_in;
+            const float* src = ok ? x + ((static_cast<long long>(n) * g.H + h) * g.W + ww) * g.C_in + c : x;
+            cp_async_f32(dst + ci * (kWgPatchH * kWgPatchW) + pix, src, ok);
         }
-        __syncthreads();
-        // 2a. V = B^T d B for (tile, channel)
-        {
-            const int t = tid & 31, ci = tid >> 5;
-            const int lh = t / kWgTilesW, lw = t - lh * kWgTilesW;
-            const float* d0 = patch + ci * (kWgPatchH * kWgPatchW) + (2 * lh) * kWgPatchW + 2 * lw;
-            float d[4][4], u[4][4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) d[i][j] = d0[i * kWgPatchW + j];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {  // rows: B^T d
-                u[0][j] = d[0][j] - d[2][j];
-                u[1][j] = d[1][j] + d[2][j];
-                u[2][j] = d[2][j] - d[1][j];
-                u[3][j] = d[1][j] - d[3][j];
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {  // columns: (B^T d) B
-                const float v0 = u[i][0] - u[i][2], v1 = u[i][1] + u[i][2];
-                const float v2 = u[i][2] - u[i][1], v3 = u[i][1] - u[i][3];
-                const int k = 4 * i;
-                Vs[((k + 0) * kWgCi + ci) * kWgRow + ((k + 0) & 1) * 4 + t] = v0;
-                Vs[((k + 1) * kWgCi + ci) * kWgRow + ((k + 1) & 1) * 4 + t] = v1;
-                Vs[((k + 2) * kWgCi + ci) * kWgRow + ((k + 2) & 1) * 4 + t] = v2;
-                Vs[((k + 3) * kWgCi + ci) * kWgRow + ((k + 3) & 1) * 4 + t] = v3;
-            }
-        }
-        // 2b. U = G g G^T for (filter, channel); weights [C_out][3][3][C_in], channel
-        // fastest across threads so a warp reads 32-byte runs
-        {
-            const int f = tid >> 3, ci = tid & 7;
+    };
+    issue_patch(0, patch);
+    cp_async_commit_wait_all();
+    __syncthreads();
+    for (int c0 = 0, pb = 0; c0 < g.C_in; c0 += kWgCi, pb ^= 1) {
+        const float* cur = patch + pb * kWgPatchFloats;
+        // 2b. U = G g G^T for (filter, channel) pairs; weights [C_out][3][3][C_in],
+        // channel fastest across threads so a warp reads 32-byte runs
+#pragma unroll 1
+        for (int half = 0; half < kWgCi / 8; ++half) {
+            const int f = tid >> 3, ci = (tid & 7) + 8 * half;
             const int co = co0 + f, c = c0 + ci;
             float gg[3][3], t[4][3];
 #pragma unroll
@@ -152,6 +145,41 @@ __global__ void __launch_bounds__(kWgThreads, 2) winograd_kernel(const WinogradP
             }
         }
         __syncthreads();
+        // 2a. V = B^T d B for (tile, channel) pairs
+#pragma unroll 1
+        for (int half = 0; half < kWgCi / 8; ++half) {
+            const int t = tid & 31, ci = (tid >> 5) + 8 * half;
+            const int lh = t / kWgTilesW, lw = t - lh * kWgTilesW;
+            const float* d0 = cur + ci * (kWgPatchH * kWgPatchW) + (2 * lh) * kWgPatchW + 2 * lw;
+            float d[4][4], u[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) d[i][j] = d0[i * kWgPatchW + j];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {  // rows: B^T d
+                u[0][j] = d[0][j] - d[2][j];
+                u[1][j] = d[1][j] + d[2][j];
+                u[2][j] = d[2][j] - d[1][j];
+                u[3][j] = d[1][j] - d[3][j];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {  // columns: (B^T d) B
+                const float v0 = u[i][0] - u[i][2], v1 = u[i][1] + u[i][2];
+                const float v2 = u[i][2] - u[i][1], v3 = u[i][1] - u[i][3];
+                const int k = 4 * i;
+                Vs[((k + 0) * kWgCi + ci) * kWgRow + ((k + 0) & 1) * 4 + t] = v0;
+                Vs[((k + 1) * kWgCi + ci) * kWgRow + ((k + 1) & 1) * 4 + t] = v1;
+                Vs[((k + 2) * kWgCi + ci) * kWgRow + ((k + 2) & 1) * 4 + t] = v2;
+                Vs[((k + 3) * kWgCi + ci) * kWgRow + ((k + 3) & 1) * 4 + t] = v3;
+            }
+        }
+        __syncthreads();
+        // the next chunk's patch copies are in flight during the products
+        if (c0 + kWgCi < g.C_in) {
+            issue_patch(c0 + kWgCi, patch + (pb ^ 1) * kWgPatchFloats);
+            cp_async_commit();
+        }
         // 3. M[xi] += V[xi] (8 tiles) x U[xi] (8 filters) over the chunk's channels
 #pragma unroll
         for (int ci = 0; ci < kWgCi; ++ci) {
@@ -165,7 +193,8 @@ __global__ void __launch_bounds__(kWgThreads, 2) winograd_kernel(const WinogradP
 #pragma unroll
                 for (int c = 0; c < 8; ++c) acc[a][c] = fmaf(v[a], u[c], acc[a][c]);
         }
-        __syncthreads();  // the next chunk overwrites patch, V and U
+        cp_async_commit_wait_all();
+        __syncthreads();  // the next patch has landed; the next chunk overwrites V and U
     }
 
     // the 16 components of every (tile, filter) into shared memory
