@@ -275,7 +275,8 @@ bool configure_smallk(conv_plan* pl) {
     s.num_segments = static_cast<int>(segments);
     s.row_bytes = static_cast<int>(row_bytes);
     const int b_bytes = (g.C_out * s.a_row_bytes + 1023) / 1024 * 1024;
-    const int fixed = 1024 + b_bytes + 8 * 2 * 32 * 64 + 1024 + 3 * 64 * 4 + 16 + 2 * (g.C_out + 4) * 4;
+    const int fixed = 1024 + b_bytes + 8 * 2 * 32 * 64 + 1024 + 3 * 64 * 4 + kSkMaxStages * kSkMaxRows * 4 + 16 +
+                      2 * (g.C_out + 4) * 4;
     // row segments per stage (2 * rows * C_out TMEM columns): as many as allow a two-stage ring
     int rows = 256 / g.C_out < 4 ? 256 / g.C_out : 4;
     int stages = 0;
@@ -290,8 +291,12 @@ bool configure_smallk(conv_plan* pl) {
         }
     }
     if (rows < 1 || stages < 2) return false;
-    if (stages > 8) stages = 8;
+    if (stages > kSkMaxStages) stages = kSkMaxStages;
     s.rows_per_tile = rows;
+    // consecutive output rows of one image read overlapping, contiguous input rows
+    // when the kernel rows are adjacent and the stride skips none of them: one copy
+    // of their union fits in the stage's Kh rows per segment
+    s.row_runs = (g.D == 1 && g.S <= g.Kh) ? 1 : 0;
     s.num_tiles = static_cast<int>((segments + rows - 1) / rows);
     s.stages = stages;
     s.smem_bytes = fixed + stages * (rows * 128 * s.a_row_bytes + s.raw_bytes);

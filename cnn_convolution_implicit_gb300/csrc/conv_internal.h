@@ -154,6 +154,8 @@ int tc_gemm_pair_max_clusters(const TcGemmParams& p);
 
 // ---------------------------------------------------------------- tcgen05 small-K (stem)
 constexpr int kSkTransformThreads = 192;  // 6 transform warps
+constexpr int kSkMaxStages = 8;
+constexpr int kSkMaxRows = 8;             // row segments per stage at most
 constexpr int kSkThreads = 320 + kSkTransformThreads;  // producer, MMA, 2 x 4 epilogue, transform warps
 
 struct SmallKParams {
@@ -173,6 +175,7 @@ struct SmallKParams {
     int num_tiles;     // ceil(num_segments / rows_per_tile)
     int row_bytes;     // W * C_in * 2
     int raw_bytes;     // rows_per_tile * Kh * row_bytes rounded up to 1024
+    int row_runs;      // 1: a stage's input rows come in as one bulk copy per run of overlapping rows
     int stages;
     int tmem_cols;
     int smem_bytes;

@@ -53,6 +53,7 @@ struct SkSmem {
     int* tab_off;    // per K index: kh*row_elems + kw*D*C_in + ci
     int* tab_kwd;    // per K index: kw*D
     int* tab_kh;     // per K index: kh, or -1 beyond the reduction (zero padding of K)
+    int* seg_base;   // per stage and row segment: raw-buffer row of the segment's kernel row 0
     float* bias;     // [C_out] copy of the bias
     float* scale;    // [C_out] copy of the per-channel scale (when given)
 };
@@ -80,7 +81,9 @@ __device__ __forceinline__ SkSmem carve(uint8_t* raw, const SmallKParams& p) {
     s.tab_kwd = s.tab_off + 64;
     s.tab_kh = s.tab_kwd + 64;
     // 16-byte aligned: the epilogue reads it as float4 (the barrier count above varies with `stages`)
-    s.bias = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(s.tab_kh + 64) + 15) & ~uintptr_t(15));
+    s.seg_base = s.tab_kh + 64;
+    s.bias = reinterpret_cast<float*>(
+        (reinterpret_cast<uintptr_t>(s.seg_base + kSkMaxStages * kSkMaxRows) + 15) & ~uintptr_t(15));
     s.scale = s.bias + ((p.g.C_out + 3) & ~3);
     return s;
 }
@@ -100,6 +103,58 @@ __device__ __forceinline__ SkSeg segment(const SmallKParams& p, int u) {
     t.wo0 = seg * 128;
     t.npix = min(128, p.g.W_out - t.wo0);
     return t;
+}
+
+// The input rows of the row segments of one stage.  With row runs, segments in
+// a row of one image whose input rows overlap or touch form one run, copied as
+// one contiguous block of whole NHWC rows (a 3x3 stride-2 stem reads 9 rows for
+// 4 output rows, not 12); rows outside the image are never copied (they read
+// as zero padding).  Otherwise every segment gets its Kh rows, one copy each.
+// emit(n, first_row, rows, raw_row) is called per copy; base[j] receives the
+// raw-buffer row that holds segment j's kernel row 0 (it may lie before the
+// copied rows when that row is padding).
+template <typename F>
+__device__ __forceinline__ void stage_rows(const SmallKParams& p, int tile, int* base, F&& emit) {
+    const int R = p.rows_per_tile;
+    if (!p.row_runs) {
+        for (int j = 0; j < R; ++j) {
+            const int u = tile * R + j;
+            if (u >= p.num_segments) break;
+            const SkSeg t = segment(p, u);
+            if (base) base[j] = j * p.g.Kh;
+            for (int kh = 0; kh < p.g.Kh; ++kh) {
+                const int hi = t.ho * p.g.S - p.g.P + kh * p.g.D;
+                if (hi >= 0 && hi < p.g.H) emit(t.n, hi, 1, j * p.g.Kh + kh);
+            }
+        }
+        return;
+    }
+    int run_n = -1, run_lo = 0, run_hi = -1, raw0 = 0, next_raw = 0;
+    for (int j = 0; j < R; ++j) {
+        const int u = tile * R + j;
+        if (u >= p.num_segments) break;
+        const SkSeg t = segment(p, u);
+        const int top = t.ho * p.g.S - p.g.P;  // input row of kernel row 0
+        const int lo = top > 0 ? top : 0;
+        const int last = top + p.g.Kh - 1;
+        const int hi = last < p.g.H - 1 ? last : p.g.H - 1;
+        if (lo > hi) {  // every kernel row is padding
+            if (base) base[j] = 0;
+            continue;
+        }
+        if (t.n != run_n || lo > run_hi + 1) {  // a new run
+            if (run_n >= 0) emit(run_n, run_lo, run_hi - run_lo + 1, raw0);
+            raw0 = next_raw;
+            run_n = t.n;
+            run_lo = lo;
+            run_hi = hi;
+        } else if (hi > run_hi) {
+            run_hi = hi;
+        }
+        next_raw = raw0 + (run_hi - run_lo + 1);
+        if (base) base[j] = raw0 + (top - run_lo);
+    }
+    if (run_n >= 0) emit(run_n, run_lo, run_hi - run_lo + 1, raw0);
 }
 
 // Byte offset of element k of row r in a swizzled K-major tile with 64- or
@@ -232,30 +287,18 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                     record_status(p.status, kStatusTimeoutProducer, abort);
                     break;
                 }
-                uint32_t bytes = 0;
-                for (int j = 0; j < R; ++j) {
-                    const int u = tile * R + j;
-                    if (u >= p.num_segments) break;
-                    const SkSeg t = segment(p, u);
-                    for (int kh = 0; kh < p.g.Kh; ++kh) {
-                        const int hi = t.ho * p.g.S - p.g.P + kh * p.g.D;
-                        if (hi >= 0 && hi < p.g.H) bytes += static_cast<uint32_t>(p.row_bytes);
-                    }
-                }
+                int* base = sm.seg_base + stage * kSkMaxRows;
+                uint32_t bytes = 0;  // segment bases (read by the transform warps) and the stage's byte count
+                stage_rows(p, tile, base, [&](int, int, int rows, int) {
+                    bytes += static_cast<uint32_t>(rows * p.row_bytes);
+                });
                 mbar_arrive_expect_tx(&sm.raw_full[stage], bytes);
                 uint8_t* dst = sm.raw + stage * p.raw_bytes;
-                for (int j = 0; j < R; ++j) {
-                    const int u = tile * R + j;
-                    if (u >= p.num_segments) break;
-                    const SkSeg t = segment(p, u);
-                    for (int kh = 0; kh < p.g.Kh; ++kh) {
-                        const int hi = t.ho * p.g.S - p.g.P + kh * p.g.D;
-                        if (hi < 0 || hi >= p.g.H) continue;
-                        const char* src = xb + (static_cast<long long>(t.n) * p.g.H + hi) * p.row_bytes;
-                        bulk_load(dst + (j * p.g.Kh + kh) * p.row_bytes, src, static_cast<uint32_t>(p.row_bytes),
-                                  &sm.raw_full[stage]);
-                    }
-                }
+                stage_rows(p, tile, nullptr, [&](int n, int row, int rows, int raw_row) {
+                    const char* src = xb + (static_cast<long long>(n) * p.g.H + row) * p.row_bytes;
+                    bulk_load(dst + raw_row * p.row_bytes, src, static_cast<uint32_t>(rows * p.row_bytes),
+                              &sm.raw_full[stage]);
+                });
                 ++issued;
                 if (++stage == p.stages) {
                     stage = 0;
@@ -403,7 +446,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                     wbase = (t.wo0 + r) * p.g.S - p.g.P;  // input column of tap kw = 0
                     if (r >= t.npix) rowmask = 0;         // rows past the segment: zeros
                 }
-                const uint16_t* src = raw16 + stage * raw_elems + j * p.g.Kh * row_elems;
+                const uint16_t* src = raw16 + stage * raw_elems + sm.seg_base[stage * kSkMaxRows + j] * row_elems;
                 if constexpr (CIN > 0) {
                     constexpr int kChunks = ((CIN * KH * KW + 15) / 16) * 2;
 #pragma unroll

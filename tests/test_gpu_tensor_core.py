@@ -38,6 +38,9 @@ pytestmark = pytest.mark.gpu
     (ConvShape(1, 4, 6, 300, 32, 3, 3, 1, 1, 1, 1, "bf16", True, True), "small_k_gemm"),      # 3 segments
     (ConvShape(2, 1, 20, 32, 32, 7, 7, 2, 3, 1, 1, "bf16", True, True), "small_k_gemm"),      # 49 taps
     (ConvShape(1, 8, 12, 16, 256, 2, 2, 1, 0, 2, 1, "bf16", False, True), "small_k_gemm"),    # dilation
+    (ConvShape(3, 3, 30, 24, 32, 3, 3, 2, 1, 1, 1, "bf16", True, True), "small_k_gemm"),      # H_out 15: stages cross images
+    (ConvShape(1, 3, 2, 16, 32, 3, 3, 1, 3, 1, 1, "bf16", True, False), "small_k_gemm"),      # rows that are all padding
+    (ConvShape(2, 3, 21, 16, 32, 1, 1, 2, 0, 1, 1, "bf16", True, True), "small_k_gemm"),      # S > K: row per copy
 ])
 @pytest.mark.parametrize("sm_pairs", [False, True], ids=["single_sm", "sm_pairs"])
 def test_tensor_core_small_shapes_full(shape, path, sm_pairs):
