@@ -275,7 +275,7 @@ bool configure_smallk(conv_plan* pl) {
     s.num_segments = static_cast<int>(segments);
     s.row_bytes = static_cast<int>(row_bytes);
     const int b_bytes = (g.C_out * s.a_row_bytes + 1023) / 1024 * 1024;
-    const int fixed = 1024 + b_bytes + 8 * 2 * 32 * 64 + 1024 + 3 * 64 * 4 + kSkMaxStages * kSkMaxRows * 4 + 16 +
+    const int fixed = 1024 + b_bytes + 1024 + 3 * 64 * 4 + 16 + kSkMaxStages * kSkMaxRows * 16 +
                       2 * (g.C_out + 4) * 4;
     // row segments per stage (2 * rows * C_out TMEM columns): as many as allow a two-stage ring
     int rows = 256 / g.C_out < 4 ? 256 / g.C_out : 4;
@@ -323,17 +323,6 @@ bool configure_depthwise(conv_plan* pl) {
 // pixels, 128-byte swizzle (64 channels) or 64-byte swizzle (32 channels).
 CUresult encode_y_map(conv_plan* pl, void* y) {
     const ConvGeom& g = pl->g;
-    if (pl->path == CONV_PATH_SMALL_K_GEMM) {  // {C_out, W_out, N*H_out}: a row segment never spills
-        const cuuint32_t box[3] = {32, 32, 1};
-        const cuuint32_t estr[3] = {1, 1, 1};
-        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(g.C_out), static_cast<cuuint64_t>(g.W_out),
-                                    static_cast<cuuint64_t>(g.N) * g.H_out};
-        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(g.C_out) * 2,
-                                       static_cast<cuuint64_t>(g.W_out) * g.C_out * 2};
-        return g_encode_tiled(&pl->map_y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, y, dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    }
     const TcGemmParams& t = pl->tc;
     const CUtensorMapSwizzle sw = t.ychunk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     if (t.mode == kTcModePhase) {
@@ -425,8 +414,6 @@ conv_status encode_maps(conv_plan* pl, const void* x, const void* w, void* y) {
                            bbox, bestr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return CONV_ERR_CUDA;
-        if (encode_y_map(pl, y) != CUDA_SUCCESS) return CONV_ERR_CUDA;
-    } else if (pl->path == CONV_PATH_SMALL_K_GEMM) {
         if (encode_y_map(pl, y) != CUDA_SUCCESS) return CONV_ERR_CUDA;
     } else if (pl->path == CONV_PATH_DEPTHWISE) {
         const cuuint64_t dims[4] = {static_cast<cuuint64_t>(g.C_in), static_cast<cuuint64_t>(g.W),
@@ -679,9 +666,7 @@ conv_status forward_impl(conv_plan* p, const void* x, const void* w, const float
             e = launch_tc_gemm(p->map_a, p->map_b, p->map_y, t, grid, st);
             break;
         }
-        case CONV_PATH_SMALL_K_GEMM: {
-            conv_status cs = encode_maps(p, x, w, y);
-            if (cs != CONV_OK) return cs;
+        case CONV_PATH_SMALL_K_GEMM: {  // plain and bulk copies only: no tensor maps
             SmallKParams s = p->sk;
             s.x = static_cast<const __nv_bfloat16*>(x);
             s.w = static_cast<const __nv_bfloat16*>(w);
@@ -689,7 +674,7 @@ conv_status forward_impl(conv_plan* p, const void* x, const void* w, const float
             s.scale = scale;
             s.y = static_cast<__nv_bfloat16*>(y);
             const int grid = s.num_tiles < p->num_sms ? s.num_tiles : p->num_sms;
-            e = launch_tc_smallk(p->map_y, s, grid, st);
+            e = launch_tc_smallk(s, grid, st);
             break;
         }
         case CONV_PATH_WINOGRAD: {

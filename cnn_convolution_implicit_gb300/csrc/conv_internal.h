@@ -181,8 +181,7 @@ struct SmallKParams {
     int smem_bytes;
     unsigned* status;
 };
-// y_map: 3-D {C_out, W_out, N*H_out} BF16, box {32, 32, 1}, 64-byte swizzle.
-cudaError_t launch_tc_smallk(const CUtensorMap& y_map, const SmallKParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_tc_smallk(const SmallKParams& p, int grid, cudaStream_t stream);
 
 // ---------------------------------------------------------------- fused depthwise 3x3 + pointwise 1x1 block
 constexpr int kBkTileH = 16;          // output tile: 16 rows x 8 columns = 128 pixels (TMEM lanes)

@@ -24,7 +24,8 @@
 //   warp 0       bulk-copy producer (one lane)
 //   warp 1       TMEM allocator; one lane issues tcgen05.mma
 //   warps 2..9   epilogue, two groups of four (one per TMEM accumulator buffer):
-//                tcgen05.ld -> +bias -> ReLU -> BF16 -> smem -> TMA store
+//                tcgen05.ld -> +bias -> ReLU -> BF16 -> 16-byte global stores (a lane
+//                owns one output pixel: its 32-channel run is 64 contiguous bytes)
 //   warps 10..15 transform: raw rows -> swizzled A tiles
 // The 3-channel 3x3 case is compiled with its K decomposition as constants;
 // other shapes read it from a per-CTA table.
@@ -35,25 +36,23 @@ namespace convgb {
 
 namespace {
 
-constexpr uint32_t kSkOutBytes = 32 * 64;  // one 32-row x 32-column BF16 store tile
-
 struct SkSmem {
     uint8_t* b;
     uint8_t* a;
     uint8_t* raw;
-    uint8_t* out;  // per epilogue warp: two store tiles
     uint64_t* raw_full;
     uint64_t* a_full;
     uint64_t* empty;
     uint64_t* tfull;
     uint64_t* tempty;
     uint64_t* drain;
+    uint64_t* ready;  // the resident weights, tables and bias are in place
     uint32_t* tmem_slot;
     int* abort;
     int* tab_off;    // per K index: kh*row_elems + kw*D*C_in + ci
     int* tab_kwd;    // per K index: kw*D
     int* tab_kh;     // per K index: kh, or -1 beyond the reduction (zero padding of K)
-    int* seg_base;   // per stage and row segment: raw-buffer row of the segment's kernel row 0
+    int4* seg_info;  // per stage and row segment: {raw row of kernel row 0, live kernel rows, w0, pixels}
     float* bias;     // [C_out] copy of the bias
     float* scale;    // [C_out] copy of the per-channel scale (when given)
 };
@@ -67,23 +66,22 @@ __device__ __forceinline__ SkSmem carve(uint8_t* raw, const SmallKParams& p) {
     const uint32_t b_bytes = (static_cast<uint32_t>(p.g.C_out * p.a_row_bytes) + 1023u) & ~1023u;
     s.a = s.b + b_bytes;
     s.raw = s.a + p.stages * p.rows_per_tile * a_tile_bytes(p);
-    s.out = s.raw + p.stages * p.raw_bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s.out + 8 * 2 * kSkOutBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s.raw + p.stages * p.raw_bytes);
     s.raw_full = bars;
     s.a_full = bars + p.stages;
     s.empty = bars + 2 * p.stages;
     s.tfull = bars + 3 * p.stages;
     s.tempty = s.tfull + 2;
     s.drain = s.tempty + 2;
-    s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
+    s.ready = s.drain + 1;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(s.ready + 1);
     s.abort = reinterpret_cast<int*>(s.tmem_slot + 1);
     s.tab_off = s.abort + 1;
     s.tab_kwd = s.tab_off + 64;
     s.tab_kh = s.tab_kwd + 64;
     // 16-byte aligned: the epilogue reads it as float4 (the barrier count above varies with `stages`)
-    s.seg_base = s.tab_kh + 64;
-    s.bias = reinterpret_cast<float*>(
-        (reinterpret_cast<uintptr_t>(s.seg_base + kSkMaxStages * kSkMaxRows) + 15) & ~uintptr_t(15));
+    s.seg_info = reinterpret_cast<int4*>((reinterpret_cast<uintptr_t>(s.tab_kh + 64) + 15) & ~uintptr_t(15));
+    s.bias = reinterpret_cast<float*>(s.seg_info + kSkMaxStages * kSkMaxRows);
     s.scale = s.bias + ((p.g.C_out + 3) & ~3);
     return s;
 }
@@ -105,54 +103,105 @@ __device__ __forceinline__ SkSeg segment(const SmallKParams& p, int u) {
     return t;
 }
 
+// The segment after t (no division: segments run along the row, then rows, then images).
+__device__ __forceinline__ void next_segment(const SmallKParams& p, SkSeg& t) {
+    t.wo0 += 128;
+    if (t.wo0 >= p.g.W_out) {
+        t.wo0 = 0;
+        if (++t.ho == p.g.H_out) {
+            t.ho = 0;
+            ++t.n;
+        }
+    }
+    t.npix = min(128, p.g.W_out - t.wo0);
+}
+
+// The first segments of a CTA's stages: segment blockIdx.x * R, then gridDim.x * R
+// segments further each time, stepped as a mixed-radix number (segment, row,
+// image) with one carry per digit instead of divisions.
+struct SkStageWalk {
+    SkSeg t;
+    int seg, d_seg, d_ho, d_n;
+    __device__ __forceinline__ SkStageWalk(const SmallKParams& p) {
+        t = segment(p, blockIdx.x * p.rows_per_tile);
+        seg = t.wo0 / 128;
+        const SkSeg d = segment(p, gridDim.x * p.rows_per_tile);
+        d_seg = d.wo0 / 128;
+        d_ho = d.ho;
+        d_n = d.n;
+    }
+    __device__ __forceinline__ void next(const SmallKParams& p) {
+        seg += d_seg;
+        int c = 0;
+        if (seg >= p.segs) {
+            seg -= p.segs;
+            c = 1;
+        }
+        t.ho += d_ho + c;
+        c = 0;
+        if (t.ho >= p.g.H_out) {
+            t.ho -= p.g.H_out;
+            c = 1;
+        }
+        t.n += d_n + c;
+        t.wo0 = seg * 128;
+        t.npix = min(128, p.g.W_out - t.wo0);
+    }
+};
+
 // The input rows of the row segments of one stage.  With row runs, segments in
 // a row of one image whose input rows overlap or touch form one run, copied as
 // one contiguous block of whole NHWC rows (a 3x3 stride-2 stem reads 9 rows for
 // 4 output rows, not 12); rows outside the image are never copied (they read
 // as zero padding).  Otherwise every segment gets its Kh rows, one copy each.
-// emit(n, first_row, rows, raw_row) is called per copy; base[j] receives the
-// raw-buffer row that holds segment j's kernel row 0 (it may lie before the
-// copied rows when that row is padding).
+// emit(n, first_row, rows, raw_row) is called per copy.  info[j] (when given)
+// receives what the transform warps need of segment j: the raw-buffer row that
+// holds its kernel row 0 (it may lie before the copied rows when that row is
+// padding), its live kernel rows kh_lo | kh_hi << 8 (kh_lo > kh_hi: none), the
+// input column of its first pixel's tap kw = 0, and its pixel count (0 past
+// the last segment).
+// `t` is the stage's first segment, tile * rows_per_tile.
 template <typename F>
-__device__ __forceinline__ void stage_rows(const SmallKParams& p, int tile, int* base, F&& emit) {
+__device__ __forceinline__ void stage_rows(const SmallKParams& p, int tile, SkSeg t, int4* info, F&& emit) {
     const int R = p.rows_per_tile;
-    if (!p.row_runs) {
-        for (int j = 0; j < R; ++j) {
-            const int u = tile * R + j;
-            if (u >= p.num_segments) break;
-            const SkSeg t = segment(p, u);
-            if (base) base[j] = j * p.g.Kh;
-            for (int kh = 0; kh < p.g.Kh; ++kh) {
-                const int hi = t.ho * p.g.S - p.g.P + kh * p.g.D;
-                if (hi >= 0 && hi < p.g.H) emit(t.n, hi, 1, j * p.g.Kh + kh);
-            }
-        }
-        return;
-    }
     int run_n = -1, run_lo = 0, run_hi = -1, raw0 = 0, next_raw = 0;
-    for (int j = 0; j < R; ++j) {
-        const int u = tile * R + j;
-        if (u >= p.num_segments) break;
-        const SkSeg t = segment(p, u);
-        const int top = t.ho * p.g.S - p.g.P;  // input row of kernel row 0
-        const int lo = top > 0 ? top : 0;
-        const int last = top + p.g.Kh - 1;
-        const int hi = last < p.g.H - 1 ? last : p.g.H - 1;
-        if (lo > hi) {  // every kernel row is padding
-            if (base) base[j] = 0;
+    for (int j = 0; j < R; ++j, next_segment(p, t)) {
+        if (tile * R + j >= p.num_segments) {
+            if (info) info[j] = make_int4(0, 1, 0, 0);
             continue;
         }
-        if (t.n != run_n || lo > run_hi + 1) {  // a new run
-            if (run_n >= 0) emit(run_n, run_lo, run_hi - run_lo + 1, raw0);
-            raw0 = next_raw;
-            run_n = t.n;
-            run_lo = lo;
-            run_hi = hi;
-        } else if (hi > run_hi) {
-            run_hi = hi;
+        const int top = t.ho * p.g.S - p.g.P;  // input row of kernel row 0
+        // live kernel rows: top + kh*D inside [0, H)
+        int kh_lo, kh_last;
+        if (p.g.D == 1) {
+            kh_lo = top >= 0 ? 0 : -top;
+            kh_last = p.g.H - 1 - top;
+        } else {
+            kh_lo = top >= 0 ? 0 : (-top + p.g.D - 1) / p.g.D;
+            kh_last = (p.g.H - 1 - top) >= 0 ? (p.g.H - 1 - top) / p.g.D : -1;
         }
-        next_raw = raw0 + (run_hi - run_lo + 1);
-        if (base) base[j] = raw0 + (top - run_lo);
+        const int kh_hi = kh_last < p.g.Kh - 1 ? kh_last : p.g.Kh - 1;
+        int base;
+        if (!p.row_runs) {
+            base = j * p.g.Kh;
+            for (int kh = kh_lo; kh <= kh_hi; ++kh) emit(t.n, top + kh * p.g.D, 1, j * p.g.Kh + kh);
+        } else if (kh_lo > kh_hi) {  // every kernel row is padding
+            base = 0;
+        } else {
+            const int lo = top + kh_lo, hi = top + kh_hi;  // D = 1 in run mode
+            if (t.n != run_n || lo > run_hi + 1) {  // a new run
+                if (run_n >= 0) emit(run_n, run_lo, run_hi - run_lo + 1, raw0);
+                raw0 = next_raw;
+                run_n = t.n;
+                run_lo = lo;
+                run_hi = hi;
+            } else if (hi > run_hi) {
+                run_hi = hi;
+            }
+            next_raw = raw0 + (run_hi - run_lo + 1);
+            base = raw0 + (top - run_lo);
+        }
+        if (info) info[j] = make_int4(base, kh_lo | (kh_hi << 8), t.wo0 * p.g.S - p.g.P, t.npix);
     }
     if (run_n >= 0) emit(run_n, run_lo, run_hi - run_lo + 1, raw0);
 }
@@ -213,7 +262,7 @@ __device__ __forceinline__ uint4 gather_chunk(const SkSmem& sm, const SmallKPara
 
 template <int CIN, int KH, int KW>
 __global__ void __launch_bounds__(kSkThreads, 1)
-    tc_smallk_kernel(const __grid_constant__ CUtensorMap y_map, const SmallKParams p) {
+    tc_smallk_kernel(const SmallKParams p) {
     extern __shared__ uint8_t smem_raw[];
     const SkSmem sm = carve(smem_raw, p);
     const int warp = threadIdx.x >> 5;
@@ -222,36 +271,6 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     const int R = p.rows_per_tile;
     const int n_tile = p.g.C_out;
 
-    // Resident weights: row co = w[co][0..ktot), zero beyond ktot, swizzled.
-    {
-        const uint16_t* w16 = reinterpret_cast<const uint16_t*>(p.w);
-        const int kw = p.a_row_bytes / 2;
-        for (int idx = threadIdx.x; idx < p.g.C_out * kw; idx += blockDim.x) {
-            const int co = idx / kw;
-            const int k = idx - co * kw;
-            const uint16_t v = k < p.ktot ? w16[static_cast<long long>(co) * p.ktot + k] : uint16_t(0);
-            *reinterpret_cast<uint16_t*>(sm.b + sw_offset(co, k, p.a_row_bytes)) = v;
-        }
-        fence_proxy_async_smem();
-        // K index -> (kh, kw, ci) decomposition, once per CTA (no divisions in the gather loop)
-        for (int k = threadIdx.x; k < 64; k += blockDim.x) {
-            if (k < p.ktot) {
-                const int ci = k % p.g.C_in, tap = k / p.g.C_in;
-                const int kh = tap / p.g.Kw, kwi = tap - kh * p.g.Kw;
-                sm.tab_off[k] = kh * (p.row_bytes >> 1) + kwi * p.g.D * p.g.C_in + ci;
-                sm.tab_kwd[k] = kwi * p.g.D;
-                sm.tab_kh[k] = kh;
-            } else {
-                sm.tab_off[k] = 0;
-                sm.tab_kwd[k] = 0;
-                sm.tab_kh[k] = -1;
-            }
-        }
-        for (int c = threadIdx.x; c < p.g.C_out; c += blockDim.x) {
-            sm.bias[c] = p.bias ? p.bias[c] : 0.f;
-            sm.scale[c] = p.scale ? p.scale[c] : 1.f;
-        }
-    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&sm.raw_full[s], 1);
@@ -263,6 +282,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             mbar_init(&sm.tempty[b], 128);
         }
         mbar_init(sm.drain, 1);
+        mbar_init(sm.ready, kSkThreads - 32);
         *sm.abort = 0;
         fence_barrier_init();
     }
@@ -275,6 +295,42 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *sm.tmem_slot;
 
+    if (warp != 0) {
+        // Resident operands, loaded by every warp but the producer's while its first
+        // input copies are in flight.  Weights: row co = w[co][0..ktot), zero beyond
+        // ktot, swizzled.
+        const int t0 = threadIdx.x - 32, nt = kSkThreads - 32;
+        const uint16_t* w16 = reinterpret_cast<const uint16_t*>(p.w);
+        const int kw = p.a_row_bytes / 2;
+        for (int idx = t0; idx < p.g.C_out * kw; idx += nt) {
+            const int co = idx / kw;
+            const int k = idx - co * kw;
+            const uint16_t v = k < p.ktot ? w16[static_cast<long long>(co) * p.ktot + k] : uint16_t(0);
+            *reinterpret_cast<uint16_t*>(sm.b + sw_offset(co, k, p.a_row_bytes)) = v;
+        }
+        fence_proxy_async_smem();
+        // K index -> (kh, kw, ci) decomposition, once per CTA (no divisions in the gather loop)
+        for (int k = t0; k < 64; k += nt) {
+            if (k < p.ktot) {
+                const int ci = k % p.g.C_in, tap = k / p.g.C_in;
+                const int kh = tap / p.g.Kw, kwi = tap - kh * p.g.Kw;
+                sm.tab_off[k] = kh * (p.row_bytes >> 1) + kwi * p.g.D * p.g.C_in + ci;
+                sm.tab_kwd[k] = kwi * p.g.D;
+                sm.tab_kh[k] = kh;
+            } else {
+                sm.tab_off[k] = 0;
+                sm.tab_kwd[k] = 0;
+                sm.tab_kh[k] = -1;
+            }
+        }
+        for (int c = t0; c < p.g.C_out; c += nt) {
+            sm.bias[c] = p.bias ? p.bias[c] : 0.f;
+            sm.scale[c] = p.scale ? p.scale[c] : 1.f;
+        }
+        mbar_arrive(sm.ready);
+        if (!mbar_wait(sm.ready, 0, abort)) record_status(p.status, kStatusTimeoutTransform, abort);
+    }
+
     if (warp == 0) {
         // ------------------------------------------------------------ bulk-copy producer
         if (lane == 0) {
@@ -282,23 +338,23 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             uint32_t phase = 0;
             long long issued = 0;
             const char* xb = reinterpret_cast<const char*>(p.x);
+            SkStageWalk walk(p);
             for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
                 if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
                     record_status(p.status, kStatusTimeoutProducer, abort);
                     break;
                 }
-                int* base = sm.seg_base + stage * kSkMaxRows;
-                uint32_t bytes = 0;  // segment bases (read by the transform warps) and the stage's byte count
-                stage_rows(p, tile, base, [&](int, int, int rows, int) {
-                    bytes += static_cast<uint32_t>(rows * p.row_bytes);
-                });
-                mbar_arrive_expect_tx(&sm.raw_full[stage], bytes);
+                // segment info for the transform warps, then one copy per run of rows; the
+                // stage's arrival comes last, after every copy's bytes are expected
                 uint8_t* dst = sm.raw + stage * p.raw_bytes;
-                stage_rows(p, tile, nullptr, [&](int n, int row, int rows, int raw_row) {
-                    const char* src = xb + (static_cast<long long>(n) * p.g.H + row) * p.row_bytes;
-                    bulk_load(dst + raw_row * p.row_bytes, src, static_cast<uint32_t>(rows * p.row_bytes),
-                              &sm.raw_full[stage]);
+                stage_rows(p, tile, walk.t, sm.seg_info + stage * kSkMaxRows, [&](int n, int row, int rows, int raw_row) {
+                    const uint32_t bytes = static_cast<uint32_t>(rows * p.row_bytes);
+                    mbar_expect_tx(&sm.raw_full[stage], bytes);
+                    bulk_load(dst + raw_row * p.row_bytes, xb + (static_cast<long long>(n) * p.g.H + row) * p.row_bytes,
+                              bytes, &sm.raw_full[stage]);
                 });
+                mbar_arrive(&sm.raw_full[stage]);
+                walk.next(p);
                 ++issued;
                 if (++stage == p.stages) {
                     stage = 0;
@@ -348,15 +404,14 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     } else if (warp < 10) {
         // ------------------------------------------------------------ epilogue
         // Two groups of four warps, one per TMEM accumulator buffer (so two
-        // stages drain at once); the next chunk's TMEM load is in flight while
-        // the current one is converted and staged.
+        // stages drain at once).  One 32-column TMEM load at a time keeps the
+        // epilogue within its registers (a second buffer spilled and measured slower).
         const int quarter = warp & 3;
         const int group = (warp - 2) >> 2;
-        uint8_t* stg = sm.out + (warp - 2) * 2 * kSkOutBytes;
         const int chunks = n_tile / 32;
-        int sbuf = 0;
         int local = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+        SkStageWalk walk(p);
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local, walk.next(p)) {
             const int buf = local & 1;
             if (buf != group) continue;
             const uint32_t use = static_cast<uint32_t>(local >> 1) & 1u;
@@ -377,45 +432,49 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             auto process = [&](const uint32_t(&v)[32], int it) {
                 const int j = it / chunks;
                 const int c = (it - j * chunks) * 32;
-                const SkSeg t = segment(p, tile * R + j);
-                const int wo_row0 = t.wo0 + quarter * 32;  // first output column of this warp's rows
-                const bool rows_exist = quarter * 32 < t.npix;
-                if (lane == 0) bulk_wait_read_le1();
-                __syncwarp();
-                uint8_t* dst = stg + sbuf * kSkOutBytes;
-                stage_row32<true>(v, p.bias ? sm.bias + c : nullptr, p.relu, dst, lane,
-                                  p.scale ? sm.scale + c : nullptr);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0 && rows_exist) {  // columns past W_out fall outside the map: not written
-                    tma_store_3d(&y_map, dst, c, wo_row0, t.n * p.g.H_out + t.ho);
-                    bulk_commit();
-                }
-                sbuf ^= 1;
-            };
-            uint32_t va[32], vb[32];
-            __syncwarp();
-            tmem_ld32(t_addr(0), va);
-            for (int it = 0; it < items; it += 2) {
-                tmem_ld_wait(va);
-                if (it + 1 < items) {
-                    __syncwarp();
-                    tmem_ld32(t_addr(it + 1), vb);
-                }
-                process(va, it);
-                if (it + 1 < items) {
-                    tmem_ld_wait(vb);
-                    if (it + 2 < items) {
-                        __syncwarp();
-                        tmem_ld32(t_addr(it + 2), va);
+                SkSeg t = walk.t;  // segment tile * R + j
+                for (int q = 0; q < j; ++q) next_segment(p, t);
+                if (quarter * 32 + lane < t.npix) {
+                    const int wo = t.wo0 + quarter * 32 + lane;
+                    float f[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+                    if (p.scale) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) f[i] *= sm.scale[c + i];
                     }
-                    process(vb, it + 1);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) f[i] += sm.bias[c + i];
+                    uint4* dst = reinterpret_cast<uint4*>(
+                        p.y + ((static_cast<long long>(t.n) * p.g.H_out + t.ho) * p.g.W_out + wo) * p.g.C_out + c);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint4 w4;
+                        if (p.relu) {
+                            w4.x = pack_bf16x2_relu(f[8 * q4 + 0], f[8 * q4 + 1]);
+                            w4.y = pack_bf16x2_relu(f[8 * q4 + 2], f[8 * q4 + 3]);
+                            w4.z = pack_bf16x2_relu(f[8 * q4 + 4], f[8 * q4 + 5]);
+                            w4.w = pack_bf16x2_relu(f[8 * q4 + 6], f[8 * q4 + 7]);
+                        } else {
+                            w4.x = pack_bf16x2(f[8 * q4 + 0], f[8 * q4 + 1]);
+                            w4.y = pack_bf16x2(f[8 * q4 + 2], f[8 * q4 + 3]);
+                            w4.z = pack_bf16x2(f[8 * q4 + 4], f[8 * q4 + 5]);
+                            w4.w = pack_bf16x2(f[8 * q4 + 6], f[8 * q4 + 7]);
+                        }
+                        dst[q4] = w4;
+                    }
                 }
+            };
+            for (int it = 0; it < items; ++it) {
+                uint32_t va[32];
+                __syncwarp();
+                tmem_ld32(t_addr(it), va);
+                tmem_ld_wait(va);
+                process(va, it);
             }
             tc_fence_before();
             mbar_arrive(&sm.tempty[buf]);
         }
-        if (lane == 0) bulk_wait_all();
     } else {
         // ------------------------------------------------------------ transform (im2col in smem)
         const int tid = threadIdx.x - 320;  // 0..kSkTransformThreads-1
@@ -433,20 +492,58 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             for (int idx = tid; idx < R * 128; idx += kSkTransformThreads) {
                 const int j = idx >> 7;   // row segment within the stage
                 const int r = idx & 127;  // A row = pixel within the segment
-                const int u = tile * R + j;
                 uint8_t* arow = sm.a + (stage * R + j) * a_tile_bytes(p);
-                unsigned long long rowmask = 0;  // input rows that exist (the rest read as zero)
-                int wbase = 0;
-                if (u < p.num_segments) {
-                    const SkSeg t = segment(p, u);
-                    for (int kh = 0; kh < p.g.Kh; ++kh) {
-                        const int hi = t.ho * p.g.S - p.g.P + kh * p.g.D;
-                        if (hi >= 0 && hi < p.g.H) rowmask |= 1ull << kh;
+                const int4 info = sm.seg_info[stage * kSkMaxRows + j];
+                if (r >= info.w) continue;  // past the segment: its products are never stored
+                const int kh_lo = info.y & 0xff, kh_hi = info.y >> 8;
+                // input rows that exist (the rest read as zero)
+                const unsigned long long rowmask =
+                    kh_lo <= kh_hi ? ((2ull << kh_hi) - 1) & ~((1ull << kh_lo) - 1) : 0ull;
+                const int wbase = info.z + r * p.g.S;  // input column of tap kw = 0
+                const uint16_t* src = raw16 + stage * raw_elems + info.x * row_elems;
+                if constexpr (CIN == 3 && KH == 3 && KW == 3) {
+                    // adjacent taps: each kernel row's 9 values (3 taps x 3 channels) are one
+                    // contiguous run of the input row; read it as 5 words, realign by the
+                    // run's 16-bit parity, zero the taps outside the row (a run that starts
+                    // or ends up to two pixels outside reads a few bytes of the neighbouring
+                    // shared memory, then masks them) and pack the three runs back to back
+                    if (p.g.D == 1 && rowmask != 0 && wbase >= -2 && wbase < p.g.W) {
+                        const int o = wbase * 3;
+                        const uint32_t sh = static_cast<uint32_t>(o & 1) * 16u;
+                        uint32_t hmask = 0;  // bit m: value m of the run (tap m / 3) lies in the row
+#pragma unroll
+                        for (int kw = 0; kw < 3; ++kw)
+                            if (wbase + kw >= 0 && wbase + kw < p.g.W) hmask |= 7u << (3 * kw);
+                        uint32_t wm[5];
+#pragma unroll
+                        for (int i = 0; i < 5; ++i)
+                            wm[i] = (((hmask >> (2 * i)) & 1u) ? 0x0000ffffu : 0u) |
+                                    (((hmask >> (2 * i + 1)) & 1u) ? 0xffff0000u : 0u);
+                        uint32_t a[3][5];
+#pragma unroll
+                        for (int kh = 0; kh < 3; ++kh) {
+                            const uint32_t* w32 = reinterpret_cast<const uint32_t*>(src + kh * row_elems) + (o >> 1);
+                            const bool live = (rowmask >> kh) & 1ull;
+                            uint32_t wv[5];
+#pragma unroll
+                            for (int i = 0; i < 5; ++i) wv[i] = live ? w32[i] : 0u;
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) a[kh][i] = __funnelshift_r(wv[i], wv[i + 1], sh) & wm[i];
+                            a[kh][4] = (wv[4] >> sh) & wm[4];
+                        }
+                        const uint4 q0 = make_uint4(a[0][0], a[0][1], a[0][2], a[0][3]);
+                        const uint4 q1 = make_uint4(a[0][4] | (a[1][0] << 16), __funnelshift_r(a[1][0], a[1][1], 16),
+                                                    __funnelshift_r(a[1][1], a[1][2], 16),
+                                                    __funnelshift_r(a[1][2], a[1][3], 16));
+                        const uint4 q2 = make_uint4(__funnelshift_r(a[1][3], a[1][4], 16), a[2][0], a[2][1], a[2][2]);
+                        const uint4 q3 = make_uint4(a[2][3], a[2][4], 0u, 0u);
+                        *reinterpret_cast<uint4*>(arow + sw_offset(r, 0, p.a_row_bytes)) = q0;
+                        *reinterpret_cast<uint4*>(arow + sw_offset(r, 8, p.a_row_bytes)) = q1;
+                        *reinterpret_cast<uint4*>(arow + sw_offset(r, 16, p.a_row_bytes)) = q2;
+                        *reinterpret_cast<uint4*>(arow + sw_offset(r, 24, p.a_row_bytes)) = q3;
+                        continue;
                     }
-                    wbase = (t.wo0 + r) * p.g.S - p.g.P;  // input column of tap kw = 0
-                    if (r >= t.npix) rowmask = 0;         // rows past the segment: zeros
                 }
-                const uint16_t* src = raw16 + stage * raw_elems + sm.seg_base[stage * kSkMaxRows + j] * row_elems;
                 if constexpr (CIN > 0) {
                     constexpr int kChunks = ((CIN * KH * KW + 15) / 16) * 2;
 #pragma unroll
@@ -477,18 +574,18 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 }
 
 template <int CIN, int KH, int KW>
-static cudaError_t launch_sk(const CUtensorMap& y_map, const SmallKParams& p, int grid, cudaStream_t stream) {
+static cudaError_t launch_sk(const SmallKParams& p, int grid, cudaStream_t stream) {
     static int limits[64] = {};
     cudaError_t e =
         ensure_smem_limit(reinterpret_cast<const void*>(tc_smallk_kernel<CIN, KH, KW>), p.smem_bytes, limits);
     if (e != cudaSuccess) return e;
-    tc_smallk_kernel<CIN, KH, KW><<<grid, kSkThreads, p.smem_bytes, stream>>>(y_map, p);
+    tc_smallk_kernel<CIN, KH, KW><<<grid, kSkThreads, p.smem_bytes, stream>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_tc_smallk(const CUtensorMap& y_map, const SmallKParams& p, int grid, cudaStream_t stream) {
-    if (p.g.C_in == 3 && p.g.Kh == 3 && p.g.Kw == 3) return launch_sk<3, 3, 3>(y_map, p, grid, stream);
-    return launch_sk<0, 0, 0>(y_map, p, grid, stream);
+cudaError_t launch_tc_smallk(const SmallKParams& p, int grid, cudaStream_t stream) {
+    if (p.g.C_in == 3 && p.g.Kh == 3 && p.g.Kw == 3) return launch_sk<3, 3, 3>(p, grid, stream);
+    return launch_sk<0, 0, 0>(p, grid, stream);
 }
 
 }  // namespace convgb

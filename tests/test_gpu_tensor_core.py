@@ -40,6 +40,7 @@ pytestmark = pytest.mark.gpu
     (ConvShape(1, 8, 12, 16, 256, 2, 2, 1, 0, 2, 1, "bf16", False, True), "small_k_gemm"),    # dilation
     (ConvShape(3, 3, 30, 24, 32, 3, 3, 2, 1, 1, 1, "bf16", True, True), "small_k_gemm"),      # H_out 15: stages cross images
     (ConvShape(1, 3, 2, 16, 32, 3, 3, 1, 3, 1, 1, "bf16", True, False), "small_k_gemm"),      # rows that are all padding
+    (ConvShape(2, 3, 16, 24, 32, 3, 3, 1, 2, 1, 1, "bf16", True, True), "small_k_gemm"),      # P = 2: two taps off each side
     (ConvShape(2, 3, 21, 16, 32, 1, 1, 2, 0, 1, 1, "bf16", True, True), "small_k_gemm"),      # S > K: row per copy
 ])
 @pytest.mark.parametrize("sm_pairs", [False, True], ids=["single_sm", "sm_pairs"])
