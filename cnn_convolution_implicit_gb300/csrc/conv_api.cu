@@ -229,6 +229,20 @@ bool configure_tc(conv_plan* pl, bool one_by_one, bool transposed = false) {
         }
         min_ksteps = ch * cw * t.kblk;
     }
+    // One group per tile where two pixel tiles per CTA can pair up instead: packing
+    // groups side by side adds no operand reuse (each group reads its own channels
+    // and weights), but it makes units coarse (36 K-steps for four packed 3x3
+    // groups, 3.4 units per SM on the dilated layer) and rules out the two-tile mode
+    // (dilated grouped layer 56.0 -> 41.6 us).
+    if (gpc > 1 && !(pl->flags & CONV_FLAG_SM_PAIRS) && g.cout_g <= kDualMaxN && g.cout_g % 32 == 0 &&
+        t.num_m_tiles >= 2 && min_ksteps >= 4) {  // (the epilogue drains 32-column chunks)
+        gpc = 1;
+        n_tile = g.cout_g;
+        t.gpc = 1;
+        t.n_tile = n_tile;
+        t.num_n_tiles = g.C_out / n_tile;
+        t.num_tiles = t.num_m_tiles * t.num_n_tiles;
+    }
     const bool auto_pairs = !one_by_one && gpc == 1 && mma_n >= kPairMinN && min_ksteps >= 9;
     const bool want_pairs = (pl->flags & CONV_FLAG_SM_PAIRS) || (auto_pairs && !(pl->flags & CONV_FLAG_ONE_SM));
     t.pair = (t.num_m_tiles >= 2 && want_pairs) ? 1 : 0;

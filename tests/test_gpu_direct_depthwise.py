@@ -50,6 +50,33 @@ def test_direct_tiled_kernel(shape, tile_m):
     check_full(shape, y, oracle_full(shape, x, w, b))
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_direct_tiled_random_sweep(dtype):
+    """Random shapes with >= 32 output channels per group that plan to the direct path
+    (so the register-tiled kernel runs): K in {1,2,3,5}, S, P, D, groups, ragged
+    channel counts, both pixel-tile sizes' code paths; every output against the oracle."""
+    from cnn_convolution_implicit_gb300 import ConvPlan
+    rng = np.random.default_rng(21 if dtype == "f32" else 22)
+    done = 0
+    while done < 12:
+        G = int(rng.choice([1, 1, 2]))
+        cin_g = int(rng.integers(1, 41))
+        if dtype == "bf16" and cin_g % 64 == 0:
+            continue
+        cout_g = int(rng.choice([32, 40, 48, 64, 72, 96]))
+        K = int(rng.choice([1, 2, 3, 5]))
+        s = ConvShape(int(rng.integers(1, 3)), G * cin_g, int(rng.integers(3, 21)), int(rng.integers(3, 21)),
+                      G * cout_g, K, K, int(rng.choice([1, 2, 3])), int(rng.integers(0, 4)), int(rng.choice([1, 2])),
+                      G, dtype, bool(rng.integers(0, 2)), bool(rng.integers(0, 2)))
+        if s.H_out < 1 or s.W_out < 1 or ConvPlan.for_shape(s).path != "direct":
+            continue
+        x, w, b = draw(s, (700 + done, 710 + done, 720 + done), "uniform", "uniform", "uniform")
+        plan, y = run(s, x, w, b)
+        assert plan.launch["block"] in (128, 256), plan.launch
+        check_full(s, y, oracle_full(s, x, w, b))
+        done += 1
+
+
 def test_depthwise_full_size_layer():
     """N=64, C=256, 56x56, depthwise 3x3 s1 p1 FP32: every output (0.46 G MACs in FP64)."""
     s, x, w, b = inputs("dw")

@@ -54,6 +54,31 @@ def test_tensor_core_small_shapes_full(shape, path, sm_pairs):
     check_full(shape, y, oracle_full(shape, x, w, b))
 
 
+def test_small_k_random_sweep():
+    """Random BF16 shapes that plan to the small-K kernel (C_in * Kh * Kw <= 64): strides,
+    paddings, dilations and widths that split rows into several segments; every output."""
+    from cnn_convolution_implicit_gb300 import ConvPlan
+    rng = np.random.default_rng(23)
+    done = 0
+    while done < 12:
+        C_in = int(rng.integers(1, 8))
+        K = int(rng.choice([1, 2, 3, 5, 7]))
+        if C_in * K * K > 64:
+            continue
+        W = int(rng.choice([8, 16, 24, 40, 136, 264]))
+        if (W * C_in * 2) % 16 != 0:
+            continue
+        s = ConvShape(int(rng.integers(1, 4)), C_in, int(rng.integers(2, 24)), W, int(rng.choice([32, 64, 96, 128])),
+                      K, K, int(rng.choice([1, 2, 3])), int(rng.integers(0, 4)), int(rng.choice([1, 2])), 1, "bf16",
+                      bool(rng.integers(0, 2)), bool(rng.integers(0, 2)))
+        if s.H_out < 1 or s.W_out < 1 or ConvPlan.for_shape(s).path != "small_k_gemm":
+            continue
+        x, w, b = draw(s, (800 + done, 810 + done, 820 + done))
+        plan, y = run(s, x, w, b)
+        check_full(s, y, oracle_full(s, x, w, b))
+        done += 1
+
+
 def test_two_calls_same_plan_are_identical():
     s = ConvShape(2, 128, 13, 13, 256, 3, 3, 1, 1, 1, 1, "bf16", True, True)
     x, w, b = draw(s, (41, 42, 43))

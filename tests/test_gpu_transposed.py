@@ -14,7 +14,7 @@ CASES = [
     # N, C_in, H, W, C_out, K, S, P, D, G, dtype, bias, relu, expected path
     (2, 64, 7, 9, 32, 4, 2, 1, 1, 1, "bf16", True, True, "implicit_gemm"),     # 4x4 s2 p1: 4 taps per phase
     (2, 128, 6, 5, 64, 2, 2, 0, 1, 1, "bf16", True, False, "implicit_gemm"),   # K = S: one tap per phase
-    (1, 128, 5, 6, 64, 4, 2, 1, 1, 2, "bf16", True, True, "implicit_gemm"),    # two groups packed per tile
+    (1, 128, 5, 6, 64, 4, 2, 1, 1, 2, "bf16", True, True, "implicit_gemm"),    # two groups (packed per tile with SM pairs)
     (2, 64, 9, 7, 64, 3, 1, 1, 1, 1, "bf16", False, True, "implicit_gemm"),    # stride 1: one phase, 9 taps
     (2, 64, 9, 7, 48, 3, 1, 1, 1, 1, "bf16", False, True, "direct"),           # C_out % 32 != 0
     (1, 64, 6, 6, 32, 3, 3, 0, 1, 1, "bf16", True, False, "implicit_gemm"),    # S = 3
