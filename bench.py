@@ -71,10 +71,10 @@ KERNEL_SOURCES = {
     "upsample": ["tc_gemm.cu", "tc_common.cuh", "ptx.cuh", "conv_internal.h"],
     "stem": ["tc_smallk.cu", "tc_common.cuh", "ptx.cuh", "conv_internal.h"],
     "dw": ["depthwise.cu", "ptx.cuh", "conv_internal.h"],
-    "tiny_f32": ["direct.cu", "conv_internal.h"],
-    "block": ["dwpw_block.cu", "tc_common.cuh", "ptx.cuh", "conv_internal.h"],
-    "winograd": ["winograd.cu", "conv_internal.h"],
-    "f32_3x3": ["direct.cu", "conv_internal.h"],
+    "tiny_f32": ["direct.cu", "conv_internal.h", "fp32x2.cuh"],
+    "block": ["dwpw_block.cu", "tc_common.cuh", "ptx.cuh", "conv_internal.h", "fp32x2.cuh"],
+    "winograd": ["winograd.cu", "conv_internal.h", "fp32x2.cuh"],
+    "f32_3x3": ["direct.cu", "conv_internal.h", "fp32x2.cuh"],
 }
 
 

@@ -24,6 +24,7 @@
 // i = (ho + P - kh*D) / S for every kernel row kh where the division is exact
 // and i is inside the input, likewise for columns.
 #include "conv_internal.h"
+#include "fp32x2.cuh"
 #include "ptx.cuh"
 
 namespace convgb {
@@ -198,11 +199,9 @@ __global__ void __launch_bounds__(2 * BM) direct_tiled_kernel(const DirectParams
 
     // compute role: pixels [ty*8, ty*8 + 8) x channels [tx*4, tx*4 + 4) of the tile
     const int tx = tid & 15, ty = tid >> 4;
-    float acc[8][4];
+    unsigned long long acc2[8][2];  // channel pairs {4tx, 4tx+1}, {4tx+2, 4tx+3} of each pixel
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    for (int i = 0; i < 8; ++i) acc2[i][0] = acc2[i][1] = 0ull;
 
     const int chunks_per_tap = (g.cin_g + kDtChunk - 1) / kDtChunk;
     const int nchunks = g.Kh * g.Kw * chunks_per_tap;
@@ -234,16 +233,24 @@ __global__ void __launch_bounds__(2 * BM) direct_tiled_kernel(const DirectParams
             const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][k][ty * 8 + 4]);
             const float4 b = *reinterpret_cast<const float4*>(&Bs[buf][k][tx * 4]);
             const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float bv[4] = {b.x, b.y, b.z, b.w};
+            const unsigned long long b01 = f32x2_pack(b.x, b.y), b23 = f32x2_pack(b.z, b.w);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+            for (int i = 0; i < 8; ++i) {
+                const unsigned long long ai = f32x2_dup(av[i]);
+                f32x2_fma(acc2[i][0], ai, b01);
+                f32x2_fma(acc2[i][1], ai, b23);
+            }
         }
         if (more) stash(buf ^ 1);
         __syncthreads();
     }
 
+    float acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        f32x2_unpack(acc2[i][0], acc[i][0], acc[i][1]);
+        f32x2_unpack(acc2[i][1], acc[i][2], acc[i][3]);
+    }
     // epilogue: scale, bias, ReLU, NHWC store of 4 consecutive channels per pixel
     const int co = cb0 + tx * 4;
     if (co >= g.cout_g) return;

@@ -27,10 +27,13 @@
 //     pointwise weights through a ring;
 //   * the MMA warp (1) runs, per N slice of the output channels, the K = C
 //     reduction into one of two TMEM accumulators; a k-block of A is released
-//     to the depthwise warps of the next tile once the last slice has read it;
+//     to the depthwise warps of the next tile once the last slice has read it.
+//     With exactly two slices (both accumulators) it goes k-block major, both
+//     slices per k-block, so each k-block returns as soon as it is consumed;
 //   * eight epilogue warps (2..9, one group per accumulator) apply the
 //     pointwise scale, bias and ReLU, round to BF16 and TMA-store NHWC rows.
 #include "conv_internal.h"
+#include "fp32x2.cuh"
 #include "tc_common.cuh"
 
 namespace convgb {
@@ -110,11 +113,16 @@ __device__ __forceinline__ BkTile bk_tile(const BlockParams& p, int m) {
     return t;
 }
 
+// acc += a * w on four channels as two packed FP32 FMAs (each lane rounds as
+// fmaf, so the sums match the standalone depthwise kernel bit for bit): half
+// the FMA instructions of the depthwise warps, which share their issue slots
+// with the epilogue warps.
 __device__ __forceinline__ void fma4(float4& acc, const float4& a, const float4& w) {
-    acc.x = fmaf(a.x, w.x, acc.x);
-    acc.y = fmaf(a.y, w.y, acc.y);
-    acc.z = fmaf(a.z, w.z, acc.z);
-    acc.w = fmaf(a.w, w.w, acc.w);
+    unsigned long long lo = f32x2_pack(acc.x, acc.y), hi = f32x2_pack(acc.z, acc.w);
+    f32x2_fma(lo, f32x2_pack(a.x, a.y), f32x2_pack(w.x, w.y));
+    f32x2_fma(hi, f32x2_pack(a.z, a.w), f32x2_pack(w.z, w.w));
+    f32x2_unpack(lo, acc.x, acc.y);
+    f32x2_unpack(hi, acc.z, acc.w);
 }
 
 // Wait until every fill issued into a ring of `stages` barriers has landed.
@@ -243,21 +251,23 @@ __global__ void __launch_bounds__(kBkThreads, 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
+            // the MMA issuer's order: k-block major with two slices, else slice major
+            const bool kb_major = p.slices == 2;
             for (int m = blockIdx.x; m < p.num_tiles && ok; m += gridDim.x) {
-                for (int sl = 0; sl < p.slices && ok; ++sl) {
-                    for (int kb = 0; kb < p.kblk; ++kb) {
-                        if (!mbar_wait(&sm.bempty[stage], phase ^ 1u, abort)) {
-                            record_status(p.status, kStatusTimeoutProducer, abort);
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&sm.bfull[stage], b_bytes);
-                        tma_load_2d(sm.b + stage * b_bytes, &w_map, &sm.bfull[stage], kb * kTcBlockK, sl * p.slice_n);
-                        ++issued;
-                        if (++stage == p.b_stages) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
+                for (int i = 0; i < p.slices * p.kblk; ++i) {
+                    const int sl = kb_major ? (i & 1) : i / p.kblk;
+                    const int kb = kb_major ? (i >> 1) : i - sl * p.kblk;
+                    if (!mbar_wait(&sm.bempty[stage], phase ^ 1u, abort)) {
+                        record_status(p.status, kStatusTimeoutProducer, abort);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&sm.bfull[stage], b_bytes);
+                    tma_load_2d(sm.b + stage * b_bytes, &w_map, &sm.bfull[stage], kb * kTcBlockK, sl * p.slice_n);
+                    ++issued;
+                    if (++stage == p.b_stages) {
+                        stage = 0;
+                        phase ^= 1u;
                     }
                 }
             }
@@ -273,6 +283,51 @@ __global__ void __launch_bounds__(kBkThreads, 1)
             bool ok = true;
             for (int m = blockIdx.x; m < p.num_tiles && ok; m += gridDim.x, ++local_tile) {
                 const uint32_t tile_par = static_cast<uint32_t>(local_tile) & 1u;
+                if (p.slices == 2) {
+                    // Two slices fill both TMEM accumulators: k-block major, each k-block of A
+                    // feeds both slices and returns to the depthwise warps at once, so the
+                    // next tile's depthwise work never waits for the second slice's MMAs.
+                    const uint32_t use = tile_par;
+                    if (!mbar_wait(&sm.tempty[0], use ^ 1u, abort) || !mbar_wait(&sm.tempty[1], use ^ 1u, abort)) {
+                        record_status(p.status, kStatusTimeoutMma, abort);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int kb = 0; kb < p.kblk && ok; ++kb) {
+                        if (!mbar_wait(&sm.afull[kb], tile_par, abort)) {
+                            record_status(p.status, kStatusTimeoutMma, abort);
+                            ok = false;
+                            break;
+                        }
+                        for (int sl = 0; sl < 2; ++sl) {
+                            if (!mbar_wait(&sm.bfull[stage], phase, abort)) {
+                                record_status(p.status, kStatusTimeoutMma, abort);
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t d = tmem_base + static_cast<uint32_t>(sl * p.slice_n);
+                            const uint64_t adesc = sdesc_sw128(smem_addr(sm.a + kb * kBkKblkBytes));
+                            const uint64_t bdesc = sdesc_sw128(smem_addr(sm.b + stage * b_bytes));
+#pragma unroll
+                            for (int k = 0; k < kTcBlockK / 16; ++k)
+                                mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+                            mma_commit(&sm.bempty[stage]);
+                            if (++stage == p.b_stages) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
+                        }
+                        if (ok) mma_commit(&sm.aempty[kb]);  // the next tile may overwrite it
+                    }
+                    if (ok) {
+                        mma_commit(&sm.tfull[0]);
+                        mma_commit(&sm.tfull[1]);
+                    }
+                    unit += 2;
+                    continue;
+                }
                 for (int sl = 0; sl < p.slices && ok; ++sl, ++unit) {
                     const int buf = unit & 1;
                     const uint32_t use = static_cast<uint32_t>(unit >> 1) & 1u;

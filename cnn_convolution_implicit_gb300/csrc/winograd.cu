@@ -26,10 +26,11 @@
 //   2. thread (tile, channel) computes V = B^T d B; thread (filter, channel)
 //      computes U = G g G^T;
 //   3. thread (component xi of 16, 8 tiles, 8 filters) accumulates its 8 x 8
-//      block of M[xi] over the chunk: 64 FMAs per 16 shared loads;
+//      block of M[xi] over the chunk: 64 FMAs (32 packed pairs) per 16 shared loads;
 // then the 16 components of each (tile, filter) meet in shared memory and
 // thread (tile, filter) computes Y = A^T M A, scale, bias, ReLU and stores.
 #include "conv_internal.h"
+#include "fp32x2.cuh"
 #include "ptx.cuh"
 
 namespace convgb {
@@ -84,11 +85,11 @@ __global__ void __launch_bounds__(kWgThreads, 2) winograd_kernel(const WinogradP
     // product-phase roles: component xi, 8 tiles (tg), 8 filters (cg)
     const int xi = tid >> 4, tg = (tid >> 2) & 3, cg = tid & 3;
     const int skew = (xi & 1) * 4;  // the two components of a warp read different banks
-    float acc[8][8];
+    unsigned long long acc2[8][4];  // filter pairs {2c, 2c+1} of each tile
 #pragma unroll
     for (int a = 0; a < 8; ++a)
 #pragma unroll
-        for (int c = 0; c < 8; ++c) acc[a][c] = 0.f;
+        for (int c = 0; c < 4; ++c) acc2[a][c] = 0ull;
 
     const float* x = static_cast<const float*>(p.x);
     const float* w = static_cast<const float*>(p.w);
@@ -187,11 +188,14 @@ __global__ void __launch_bounds__(kWgThreads, 2) winograd_kernel(const WinogradP
             const float4* up = reinterpret_cast<const float4*>(Us + (xi * kWgCi + ci) * kWgRow + skew + 8 * cg);
             const float4 va = vp[0], vb = vp[1], ua = up[0], ub = up[1];
             const float v[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-            const float u[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+            const unsigned long long u2[4] = {f32x2_pack(ua.x, ua.y), f32x2_pack(ua.z, ua.w), f32x2_pack(ub.x, ub.y),
+                                              f32x2_pack(ub.z, ub.w)};
 #pragma unroll
-            for (int a = 0; a < 8; ++a)
+            for (int a = 0; a < 8; ++a) {
+                const unsigned long long va2 = f32x2_dup(v[a]);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) acc[a][c] = fmaf(v[a], u[c], acc[a][c]);
+                for (int c = 0; c < 4; ++c) f32x2_fma(acc2[a][c], va2, u2[c]);
+            }
         }
         cp_async_commit_wait_all();
         __syncthreads();  // the next patch has landed; the next chunk overwrites V and U
@@ -201,7 +205,10 @@ __global__ void __launch_bounds__(kWgThreads, 2) winograd_kernel(const WinogradP
 #pragma unroll
     for (int a = 0; a < 8; ++a)
 #pragma unroll
-        for (int c = 0; c < 8; ++c) Ms[(xi * kWgTiles + 8 * tg + a) * kWgMStride + 8 * cg + c] = acc[a][c];
+        for (int c = 0; c < 4; ++c) {
+            float* m = Ms + (xi * kWgTiles + 8 * tg + a) * kWgMStride + 8 * cg + 2 * c;
+            f32x2_unpack(acc2[a][c], m[0], m[1]);
+        }
     __syncthreads();
 
     // Y = A^T M A, then scale, bias, ReLU; thread = (tile, filter), filters fastest
