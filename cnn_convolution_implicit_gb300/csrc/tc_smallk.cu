@@ -405,7 +405,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         // ------------------------------------------------------------ epilogue
         // Two groups of four warps, one per TMEM accumulator buffer (so two
         // stages drain at once).  One 32-column TMEM load at a time keeps the
-        // epilogue within its registers (a second buffer spilled and measured slower).
+        // epilogue within its registers (a second buffer spilled and measured slower;
+        // 16-column halves, each load in flight during the other's stores, slower too).
         const int quarter = warp & 3;
         const int group = (warp - 2) >> 2;
         const int chunks = n_tile / 32;
@@ -489,7 +490,87 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 record_status(p.status, kStatusTimeoutTransform, abort);
                 break;
             }
-            for (int idx = tid; idx < R * 128; idx += kSkTransformThreads) {
+            uint32_t done_mask = 0;  // bit q: this thread's q-th row was packed by the fast path
+            if constexpr (CIN == 3 && KH == 3 && KW == 3) {
+                // Adjacent taps (D = 1): each kernel row's 9 values (3 taps x 3 channels) are
+                // one contiguous run of the input row; read it as 5 words, realign by the
+                // run's 16-bit parity, zero the taps outside the row (a run that starts or
+                // ends up to two pixels outside reads a few bytes of the neighbouring shared
+                // memory, then masks them) and pack the three runs back to back.  A thread's
+                // (at most 3) rows issue all their loads before any packing, so their
+                // shared-memory latencies overlap.
+                if (p.g.D == 1) {
+                    uint32_t wv[3][3][5];
+                    uint32_t hm[3], shq[3];
+                    uint8_t* arow_q[3];
+                    int rq[3];
+#pragma unroll
+                    for (int q = 0; q < 3; ++q) {
+                        const int idx = tid + q * kSkTransformThreads;
+                        hm[q] = 0;
+                        shq[q] = 0;
+                        rq[q] = 0;
+                        arow_q[q] = sm.a;
+                        if (idx >= R * 128) continue;
+                        const int j = idx >> 7, r = idx & 127;
+                        const int4 info = sm.seg_info[stage * kSkMaxRows + j];
+                        if (r >= info.w) {  // past the segment: its products are never stored
+                            done_mask |= 1u << q;
+                            continue;
+                        }
+                        const int kh_lo = info.y & 0xff, kh_hi = info.y >> 8;
+                        const int wbase = info.z + r * p.g.S;  // input column of tap kw = 0
+                        if (kh_lo > kh_hi || wbase < -2 || wbase >= p.g.W) continue;  // generic path
+                        const int o = wbase * 3;
+                        shq[q] = static_cast<uint32_t>(o & 1) * 16u;
+#pragma unroll
+                        for (int kw = 0; kw < 3; ++kw)
+                            if (wbase + kw >= 0 && wbase + kw < p.g.W) hm[q] |= 7u << (3 * kw);
+                        const uint16_t* src = raw16 + stage * raw_elems + info.x * row_elems;
+#pragma unroll
+                        for (int kh = 0; kh < 3; ++kh) {
+                            const uint32_t* w32 = reinterpret_cast<const uint32_t*>(src + kh * row_elems) + (o >> 1);
+                            const bool live = kh >= kh_lo && kh <= kh_hi;
+#pragma unroll
+                            for (int i = 0; i < 5; ++i) wv[q][kh][i] = live ? w32[i] : 0u;
+                        }
+                        arow_q[q] = sm.a + (stage * R + j) * a_tile_bytes(p);
+                        rq[q] = r;
+                        done_mask |= 1u << q;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 3; ++q) {
+                        if (hm[q] == 0) continue;  // not packed here (or skipped)
+                        uint32_t wm[5];
+#pragma unroll
+                        for (int i = 0; i < 5; ++i)
+                            wm[i] = (((hm[q] >> (2 * i)) & 1u) ? 0x0000ffffu : 0u) |
+                                    (((hm[q] >> (2 * i + 1)) & 1u) ? 0xffff0000u : 0u);
+                        uint32_t a[3][5];
+#pragma unroll
+                        for (int kh = 0; kh < 3; ++kh) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                a[kh][i] = __funnelshift_r(wv[q][kh][i], wv[q][kh][i + 1], shq[q]) & wm[i];
+                            a[kh][4] = (wv[q][kh][4] >> shq[q]) & wm[4];
+                        }
+                        const uint4 q0 = make_uint4(a[0][0], a[0][1], a[0][2], a[0][3]);
+                        const uint4 q1 = make_uint4(a[0][4] | (a[1][0] << 16), __funnelshift_r(a[1][0], a[1][1], 16),
+                                                    __funnelshift_r(a[1][1], a[1][2], 16),
+                                                    __funnelshift_r(a[1][2], a[1][3], 16));
+                        const uint4 q2 = make_uint4(__funnelshift_r(a[1][3], a[1][4], 16), a[2][0], a[2][1], a[2][2]);
+                        const uint4 q3 = make_uint4(a[2][3], a[2][4], 0u, 0u);
+                        uint8_t* arow = arow_q[q];
+                        const int r = rq[q];
+                        *reinterpret_cast<uint4*>(arow + sw_offset(r, 0, p.a_row_bytes)) = q0;
+                        *reinterpret_cast<uint4*>(arow + sw_offset(r, 8, p.a_row_bytes)) = q1;
+                        *reinterpret_cast<uint4*>(arow + sw_offset(r, 16, p.a_row_bytes)) = q2;
+                        *reinterpret_cast<uint4*>(arow + sw_offset(r, 24, p.a_row_bytes)) = q3;
+                    }
+                }
+            }
+            for (int idx = tid, q = 0; idx < R * 128; idx += kSkTransformThreads, ++q) {
+                if (q < 3 && ((done_mask >> q) & 1u)) continue;  // packed by the fast path
                 const int j = idx >> 7;   // row segment within the stage
                 const int r = idx & 127;  // A row = pixel within the segment
                 uint8_t* arow = sm.a + (stage * R + j) * a_tile_bytes(p);
@@ -501,49 +582,6 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                     kh_lo <= kh_hi ? ((2ull << kh_hi) - 1) & ~((1ull << kh_lo) - 1) : 0ull;
                 const int wbase = info.z + r * p.g.S;  // input column of tap kw = 0
                 const uint16_t* src = raw16 + stage * raw_elems + info.x * row_elems;
-                if constexpr (CIN == 3 && KH == 3 && KW == 3) {
-                    // adjacent taps: each kernel row's 9 values (3 taps x 3 channels) are one
-                    // contiguous run of the input row; read it as 5 words, realign by the
-                    // run's 16-bit parity, zero the taps outside the row (a run that starts
-                    // or ends up to two pixels outside reads a few bytes of the neighbouring
-                    // shared memory, then masks them) and pack the three runs back to back
-                    if (p.g.D == 1 && rowmask != 0 && wbase >= -2 && wbase < p.g.W) {
-                        const int o = wbase * 3;
-                        const uint32_t sh = static_cast<uint32_t>(o & 1) * 16u;
-                        uint32_t hmask = 0;  // bit m: value m of the run (tap m / 3) lies in the row
-#pragma unroll
-                        for (int kw = 0; kw < 3; ++kw)
-                            if (wbase + kw >= 0 && wbase + kw < p.g.W) hmask |= 7u << (3 * kw);
-                        uint32_t wm[5];
-#pragma unroll
-                        for (int i = 0; i < 5; ++i)
-                            wm[i] = (((hmask >> (2 * i)) & 1u) ? 0x0000ffffu : 0u) |
-                                    (((hmask >> (2 * i + 1)) & 1u) ? 0xffff0000u : 0u);
-                        uint32_t a[3][5];
-#pragma unroll
-                        for (int kh = 0; kh < 3; ++kh) {
-                            const uint32_t* w32 = reinterpret_cast<const uint32_t*>(src + kh * row_elems) + (o >> 1);
-                            const bool live = (rowmask >> kh) & 1ull;
-                            uint32_t wv[5];
-#pragma unroll
-                            for (int i = 0; i < 5; ++i) wv[i] = live ? w32[i] : 0u;
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) a[kh][i] = __funnelshift_r(wv[i], wv[i + 1], sh) & wm[i];
-                            a[kh][4] = (wv[4] >> sh) & wm[4];
-                        }
-                        const uint4 q0 = make_uint4(a[0][0], a[0][1], a[0][2], a[0][3]);
-                        const uint4 q1 = make_uint4(a[0][4] | (a[1][0] << 16), __funnelshift_r(a[1][0], a[1][1], 16),
-                                                    __funnelshift_r(a[1][1], a[1][2], 16),
-                                                    __funnelshift_r(a[1][2], a[1][3], 16));
-                        const uint4 q2 = make_uint4(__funnelshift_r(a[1][3], a[1][4], 16), a[2][0], a[2][1], a[2][2]);
-                        const uint4 q3 = make_uint4(a[2][3], a[2][4], 0u, 0u);
-                        *reinterpret_cast<uint4*>(arow + sw_offset(r, 0, p.a_row_bytes)) = q0;
-                        *reinterpret_cast<uint4*>(arow + sw_offset(r, 8, p.a_row_bytes)) = q1;
-                        *reinterpret_cast<uint4*>(arow + sw_offset(r, 16, p.a_row_bytes)) = q2;
-                        *reinterpret_cast<uint4*>(arow + sw_offset(r, 24, p.a_row_bytes)) = q3;
-                        continue;
-                    }
-                }
                 if constexpr (CIN > 0) {
                     constexpr int kChunks = ((CIN * KH * KW + 15) / 16) * 2;
 #pragma unroll
