@@ -63,6 +63,8 @@ def load_traffic():
     return out
 
 
+METRIC = "conv2d TFLOP/s (body 3x3 layer, % of BF16 tensor peak); depthwise GB/s (% of HBM peak)"
+
 # Source files that make up each kernel (for matching ncu traffic to the code it was taken from).
 KERNEL_SOURCES = {
     "body": ["tc_gemm.cu", "tc_common.cuh", "ptx.cuh", "conv_internal.h"],
@@ -491,8 +493,8 @@ def main():
             vals.append(tf)
             samples.append(sample)
         v = float(np.mean(vals))
-        line = {"impl": "reference", "metric": "conv2d TFLOP/s (body 3x3 layer)", "value": v,
-                "unit": "TFLOP/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        line = {"impl": "reference", "metric": METRIC, "value": v,
+                "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "higher_is_better": True, "dtype": "f64", "data": "synthetic (seeded)",
                 "config": config,
                 "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
@@ -570,7 +572,7 @@ def main():
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
 
     if rank == 0:
-        line = {"metric": "conv2d TFLOP/s (body 3x3 layer, % of BF16 tensor peak); depthwise GB/s (% of HBM peak)",
+        line = {"metric": METRIC,
                 "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs, Kaiming weights)",
