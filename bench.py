@@ -559,6 +559,17 @@ def main():
                 "traffic": (tr[0] if tr and tr[1] == kernel_source_hash("body") else None),
                 "kernel": "tc_conv_kernel (implicit GEMM, TMA im2col, tcgen05)",
                 "algorithmic_flops_per_launch": s.flops}
+    # clock-derived tensor peak: this GPU's own tcgen05 rate per SM per clock x SMs x the
+    # SM clock sampled during the timed loop (a second denominator beside the cuBLAS one)
+    from cnn_convolution_implicit_gb300 import measure_mma_rate
+    fpc, _, sms = measure_mma_rate(1 << 16)
+    clk_mhz = clk.get("sm_mhz") or clk.get("sm_max_mhz")
+    if clk_mhz:
+        theo = fpc * sms * clk_mhz * 1e6 / 1e12
+        roofline["theoretical"] = {"peak": theo, "unit": "TFLOP/s", "frac": kern_tflops / theo,
+                                   "flop_per_clk_sm": fpc, "sms": sms, "sm_mhz": clk_mhz,
+                                   "how": "tcgen05.mma M128 N256 K16 chain per SM (conv_measure_mma_rate) "
+                                          "x SM count x median SM clock during the timed loop"}
     dwr = others["dw"]
     trd = traffic.get("dw")
     dw_roof = {"bound": "hbm", "achieved": dwr["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",

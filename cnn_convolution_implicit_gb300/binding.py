@@ -26,7 +26,7 @@ EXPORTS = ("conv_plan_create", "conv_plan_output_shape", "conv_plan_info", "conv
            "conv_plan_destroy", "conv_status_string", "conv_device_status", "conv_plan_num_sms",
            "conv_plan_launch_info", "conv_forward_affine", "conv_block_plan_create",
            "conv_block_plan_output_shape", "conv_block_forward", "conv_block_plan_launch_info",
-           "conv_block_plan_destroy")
+           "conv_block_plan_destroy", "conv_measure_mma_rate")
 CONV_BLOCK_DW_RELU, CONV_BLOCK_PW_RELU = 1, 2
 
 _lock = threading.Lock()
@@ -87,6 +87,8 @@ def lib():
             L.conv_block_plan_launch_info.restype = c_int
             L.conv_block_plan_destroy.argtypes = [vp]
             L.conv_block_plan_destroy.restype = c_int
+            L.conv_measure_mma_rate.argtypes = [c_int, vp, c_int, vp]
+            L.conv_measure_mma_rate.restype = c_int
             _lib = L
         return _lib
 
@@ -292,6 +294,28 @@ class BlockPlan:
 
 
 _plan_cache = {}
+
+
+def measure_mma_rate(iters: int = 1 << 16, device=None):
+    """Dense BF16 tcgen05 rate of every SM (conv_measure_mma_rate): returns
+    (FLOP per clock per SM, one value per SM, median first) and the SM count."""
+    import numpy as np
+    import torch
+    L = lib()
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    cycles = torch.zeros(sms, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    st = L.conv_measure_mma_rate(int(iters), ctypes.c_void_p(cycles.data_ptr()), sms,
+                                 ctypes.c_void_p(stream.cuda_stream))
+    if st != 0:
+        raise ConvError(st, "conv_measure_mma_rate")
+    torch.cuda.synchronize(dev)
+    if device_status() != 0:
+        raise ConvError(6, "conv_measure_mma_rate")
+    c = cycles.cpu().numpy().astype(np.float64)
+    per_sm = 2.0 * 128 * 256 * 16 * iters / c
+    return float(np.median(per_sm)), per_sm, sms
 
 
 def conv2d(x, w, bias=None, stride=1, padding=0, dilation=1, groups=1, relu=False, out_bf16=False,

@@ -188,6 +188,19 @@ conv_status conv_device_status(int *code);
 /* Number of SMs the plan's grid sizing uses (device property of the plan's device). */
 int conv_plan_num_sms(const conv_plan *p);
 
+/* Measured dense BF16 tensor rate (a measurement helper, not a convolution):
+ * launches `grid` CTAs, one per SM (each holds more than half of an SM's shared
+ * memory, so pass grid <= the SM count), and each issues `iters` (1..2^20)
+ * back-to-back tcgen05.mma of M = 128, N = 256, K = 16 (BF16 in, FP32
+ * accumulate in tensor memory) and writes the SM cycles from its first issue
+ * to the last completion to cycles[cta] (a 8-byte aligned device array of
+ * `grid` entries, caller-owned; 0 where the completion wait timed out, which
+ * also sets conv_device_status).  FLOP per clock per SM =
+ * 2 * 128 * 256 * 16 * iters / cycles[cta].  Asynchronous on `stream`.
+ * Returns CONV_ERR_INVALID_ARG / CONV_ERR_MISALIGNED without launching, or
+ * CONV_ERR_CUDA if the launch fails. */
+conv_status conv_measure_mma_rate(int iters, unsigned long long *cycles, int grid, void *stream);
+
 /*
  * Launch configuration conv_forward uses for this plan: grid and block size
  * (CTAs, threads), dynamic shared memory per CTA in bytes, pipeline stages,

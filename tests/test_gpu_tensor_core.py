@@ -79,6 +79,18 @@ def test_small_k_random_sweep():
         done += 1
 
 
+def test_measured_mma_rate():
+    """conv_measure_mma_rate: every SM's chain of M128 N256 K16 MMAs completes and gives a
+    FLOP-per-clock rate in a plausible band (dense BF16 on one SM is a few thousand FLOP
+    per clock), the same on every SM within 10 %."""
+    from cnn_convolution_implicit_gb300 import measure_mma_rate
+    fpc, per_sm, sms = measure_mma_rate(1 << 14)
+    assert sms == torch.cuda.get_device_properties(0).multi_processor_count
+    assert np.all(np.isfinite(per_sm)) and len(per_sm) == sms
+    assert 2048 <= fpc <= 16384, fpc
+    assert np.all(np.abs(per_sm / fpc - 1) < 0.1), (per_sm.min(), per_sm.max())
+
+
 def test_two_calls_same_plan_are_identical():
     s = ConvShape(2, 128, 13, 13, 256, 3, 3, 1, 1, 1, 1, "bf16", True, True)
     x, w, b = draw(s, (41, 42, 43))
