@@ -562,7 +562,7 @@ def main():
     # clock-derived tensor peak: this GPU's own tcgen05 rate per SM per clock x SMs x the
     # SM clock sampled during the timed loop (a second denominator beside the cuBLAS one)
     from cnn_convolution_implicit_gb300 import measure_mma_rate
-    fpc, _, sms = measure_mma_rate(1 << 16)
+    fpc, _, sms = measure_mma_rate(1 << 14)
     clk_mhz = clk.get("sm_mhz") or clk.get("sm_max_mhz")
     if clk_mhz:
         theo = fpc * sms * clk_mhz * 1e6 / 1e12
