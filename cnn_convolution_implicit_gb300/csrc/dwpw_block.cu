@@ -31,7 +31,9 @@
 //     With exactly two slices (both accumulators) it goes k-block major, both
 //     slices per k-block, so each k-block returns as soon as it is consumed;
 //   * eight epilogue warps (2..9, one group per accumulator) apply the
-//     pointwise scale, bias and ReLU, round to BF16 and TMA-store NHWC rows.
+//     pointwise scale, bias and ReLU, round to BF16 and TMA-store NHWC rows
+//     through one staging tile each (the shared memory this leaves for a third
+//     halo stage measured faster than a second staging tile).
 #include "conv_internal.h"
 #include "fp32x2.cuh"
 #include "tc_common.cuh"
@@ -56,8 +58,6 @@ struct BkSmem {
     float* wdw;  // [chunk][tap][32]
     float* dsc;  // [C]
     float* dbi;  // [C]
-    float* pbi;  // [C_out] pointwise shift
-    float* psc;  // [C_out] pointwise scale
     uint64_t* hfull;
     uint64_t* hempty;
     uint64_t* bfull;
@@ -77,13 +77,11 @@ __device__ __forceinline__ BkSmem bk_carve(uint8_t* raw, const BlockParams& p) {
     s.a = base;
     s.b = s.a + p.kblk * kBkKblkBytes;
     s.out = s.b + p.b_stages * p.slice_n * 128;
-    s.halo = s.out + 8 * 2 * kBkStoreTile;
+    s.halo = s.out + 8 * kBkStoreTile;
     s.wdw = reinterpret_cast<float*>(s.halo + p.halo_stages * kBkHaloBytes);
     s.dsc = s.wdw + p.C * 9;
     s.dbi = s.dsc + p.C;
-    s.pbi = s.dbi + p.C;
-    s.psc = s.pbi + p.C_out;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s.psc + p.C_out);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s.dbi + p.C);
     s.hfull = bars;
     s.hempty = s.hfull + p.halo_stages;
     s.bfull = s.hempty + p.halo_stages;
@@ -179,10 +177,6 @@ __global__ void __launch_bounds__(kBkThreads, 1)
     for (int c = threadIdx.x; c < p.C; c += blockDim.x) {
         sm.dsc[c] = p.dw_scale ? __ldg(p.dw_scale + c) : 1.f;
         sm.dbi[c] = p.dw_bias ? __ldg(p.dw_bias + c) : 0.f;
-    }
-    for (int c = threadIdx.x; c < p.C_out; c += blockDim.x) {  // read by the epilogue from shared memory
-        sm.psc[c] = p.pw_scale ? __ldg(p.pw_scale + c) : 1.f;
-        sm.pbi[c] = p.pw_bias ? __ldg(p.pw_bias + c) : 0.f;
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.halo_stages; ++s) {
@@ -448,8 +442,7 @@ __global__ void __launch_bounds__(kBkThreads, 1)
         // quarter q owns TMEM lanes 32q..32q+31 = tile rows 4q..4q+3.
         const int quarter = warp & 3;
         const int group = (warp - 2) >> 2;
-        uint8_t* stg = sm.out + (warp - 2) * 2 * kBkStoreTile;
-        int sbuf = 0;
+        uint8_t* stg = sm.out + (warp - 2) * kBkStoreTile;
         int unit = 0;
         for (int m = blockIdx.x; m < p.num_tiles; m += gridDim.x) {
             const BkTile t = bk_tile(p, m);
@@ -477,18 +470,17 @@ __global__ void __launch_bounds__(kBkThreads, 1)
                     __syncwarp();
                     tmem_ld32(t_row + static_cast<uint32_t>(cc), v);
                     tmem_ld_wait(v);
-                    if (lane == 0) bulk_wait_read_le1();  // the tile written two chunks ago is free
+                    if (lane == 0) bulk_wait_read_all();
                     __syncwarp();
-                    uint8_t* dst = stg + sbuf * kBkStoreTile;
-                    stage_row32<true>(v, p.pw_bias ? sm.pbi + co0 + cc : nullptr, p.pw_relu, dst, lane,
-                                      p.pw_scale ? sm.psc + co0 + cc : nullptr);
+                    uint8_t* dst = stg;
+                    stage_row32<false>(v, p.pw_bias ? p.pw_bias + co0 + cc : nullptr, p.pw_relu, dst, lane,
+                                       p.pw_scale ? p.pw_scale + co0 + cc : nullptr);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0 && rows_exist) {
                         tma_store_4d(&y_map, dst, co0 + cc, t.wo0, h, t.n);
                         bulk_commit();
                     }
-                    sbuf ^= 1;
                 }
                 tmem_ld_wait();
                 tc_fence_before();
@@ -510,8 +502,9 @@ __global__ void __launch_bounds__(kBkThreads, 1)
 
 int dwpw_block_smem_bytes(int C, int C_out, int slice_n, int halo_stages, int b_stages) {
     const int bars = (2 * halo_stages + 2 * b_stages + 2 * kBkMaxKblk + 5) * 8 + 16;
+    (void)C_out;
     return 1024 + (C / 64) * static_cast<int>(kBkKblkBytes) + b_stages * slice_n * 128 +
-           8 * 2 * static_cast<int>(kBkStoreTile) + halo_stages * kBkHaloBytes + C * 11 * 4 + C_out * 2 * 4 + bars;
+           8 * static_cast<int>(kBkStoreTile) + halo_stages * kBkHaloBytes + C * 11 * 4 + bars;
 }
 
 cudaError_t launch_dwpw_block(const CUtensorMap& x_map, const CUtensorMap& w_map, const CUtensorMap& y_map,
