@@ -46,6 +46,7 @@ constexpr uint32_t kBkKblkBytes = kTcBlockM * kTcBlockK * 2;  // 16 KB: 128 pixe
 constexpr uint32_t kBkStoreTile = 32 * 64;                     // 32 pixels x 32 channels BF16
 constexpr int kBkHaloW = kBkTileW + 2;
 constexpr int kBkHaloH = kBkTileH + 2;
+static_assert(kBkHaloBytes == kBkHaloH * kBkHaloW * kBkChunk * 4, "one halo copy: 18 x 10 pixels x 32 FP32 channels");
 constexpr int kBkDwWarp0 = 10;
 constexpr int kBkDwWarps = 4;
 constexpr int kBkWeightWarp = 14;
