@@ -269,6 +269,13 @@ bool configure_tc(conv_plan* pl, bool one_by_one, bool transposed = false) {
     return true;
 }
 
+// The Winograd launch grid (spatial blocks x 32-channel blocks) within CUDA's limits.
+bool winograd_grid_fits(const ConvGeom& g) {
+    const long long tiles_w = (g.W_out + 1) / 2, tiles_h = (g.H_out + 1) / 2;
+    const long long blocks = static_cast<long long>(g.N) * ((tiles_h + 3) / 4) * ((tiles_w + 7) / 8);
+    return blocks <= 0x7fffffffLL && (g.C_out + 31) / 32 <= 65535;
+}
+
 bool configure_smallk(conv_plan* pl) {
     const ConvGeom& g = pl->g;
     SmallKParams& s = pl->sk;
@@ -529,7 +536,7 @@ conv_status conv_plan_create(conv_plan** out, int N, int C_in, int H, int W, int
     if (transposed) {
         if (dtype == CONV_BF16 && configure_tc(pl, false, true)) pl->path = CONV_PATH_IMPLICIT_GEMM;
     } else if (dtype == CONV_F32) {
-        if ((flags & CONV_FLAG_WINOGRAD) && winograd_supported(g))
+        if ((flags & CONV_FLAG_WINOGRAD) && winograd_supported(g) && winograd_grid_fits(g))
             pl->path = CONV_PATH_WINOGRAD;
         else if (configure_depthwise(pl))
             pl->path = CONV_PATH_DEPTHWISE;
