@@ -210,6 +210,7 @@ def test_transposed_kernel_choice(shape, path):
     ((2, 8, 9, 9, 8, 3, 3, 1, 1, 1, 2, "f32"), True, "direct"),          # groups
     ((2, 64, 9, 9, 64, 3, 3, 1, 1, 1, 64, "f32"), True, "depthwise"),    # depthwise keeps its kernel
     ((2, 128, 9, 9, 128, 3, 3, 1, 1, 1, 1, "bf16"), True, "implicit_gemm"),  # BF16: tensor cores
+    ((2 ** 27, 4, 64, 64, 8, 3, 3, 1, 1, 1, 1, "f32"), True, "direct"),  # its grid would pass 2**31 blocks
 ])
 def test_winograd_kernel_choice(shape, winograd, path):
     *dims, dtype = shape
