@@ -119,14 +119,15 @@ def test_body_full_size_one_sm_kernel():
 
 
 def test_body_full_size():
-    """N=32, 128->256, 112x112, 3x3 s1 p1, bias+ReLU: image 31 in full, plus seeded
-    points over the whole batch (every corner included)."""
+    """N=32, 128->256, 112x112, 3x3 s1 p1, bias+ReLU: the first and last images in full,
+    plus 65,536 seeded points over the whole batch (every corner included)."""
     s, x, w, b = inputs("body")
     plan, y = run(s, x, w, b)
     assert plan.path == "implicit_gemm"
-    check_points(s, y, x, w, b, sample_points(s, 8192, 3))
-    ref31 = oracle.conv2d(x[31:32], w, b, 1, 1, 1, 1, True)
-    check_full(s, y[31:32], ref31)
+    check_points(s, y, x, w, b, sample_points(s, 65536, 3))
+    for n in (0, s.N - 1):
+        ref = oracle.conv2d(x[n:n + 1], w, b, 1, 1, 1, 1, True)
+        check_full(s, y[n:n + 1], ref)
 
 
 def test_pointwise_full_size():
