@@ -400,7 +400,7 @@ class OracleSampler:
     """Times the FP64 oracle (as it stands, never tuned) on bounded seeded samples
     of a workload's outputs, on this host's cores.  Inputs are drawn once."""
 
-    def __init__(self, name):
+    def __init__(self, name, max_points=1 << 26):
         import oracle
         self.oracle = oracle
         self.name = name
@@ -412,12 +412,13 @@ class OracleSampler:
         self.rng = np.random.default_rng(77)
         self.per_pt_flops = 2 * (s.C_in // s.G) * s.Kh * s.Kw
         self.rate = None  # points per second
+        self.max_points = max_points
         n = 2048
         while True:  # calibrate on growing samples until one takes 0.5 s
             dt = self._run(n)
-            if dt > 0.5 or n >= 1 << 26:
+            if dt > 0.5 or n >= max_points:
                 break
-            n *= 4
+            n = min(4 * n, max_points)
         self.rate = n / dt
 
     def _points(self, n):
@@ -428,9 +429,21 @@ class OracleSampler:
     def _run(self, n):
         s = self.s
         p = self._points(n)
+        points = self.oracle.conv_transpose2d_points if s.transposed else self.oracle.conv2d_points
         t0 = time.perf_counter()
-        self.oracle.conv2d_points(self.xf, self.wf, self.bf, p, s.S, s.P, s.D, s.G, s.relu)
+        points(self.xf, self.wf, self.bf, p, s.S, s.P, s.D, s.G, s.relu)
         return time.perf_counter() - t0
+
+    def full_layer(self, seconds):
+        """One bounded sample of about `seconds`, scaled to every output of the layer:
+        the oracle's wall time for the whole layer and its algorithmic TFLOP/s."""
+        s = self.s
+        n = max(256, min(int(self.rate * seconds), self.max_points, s.pixels * s.C_out))
+        dt = self._run(n)
+        full_s = dt * (s.pixels * s.C_out) / n
+        return {"full_layer_s": full_s, "tflops": s.flops / full_s / 1e12, "cores": self.oracle.max_threads(),
+                "sample": "%d seeded output points, FP64, %.2f s, scaled to the layer's %d outputs" % (
+                    n, dt, s.pixels * s.C_out)}
 
     def step(self, seconds):
         """One bounded sample of about `seconds`; returns (TFLOP/s, threads, description)."""
@@ -441,6 +454,29 @@ class OracleSampler:
         sample = "%d seeded output points of %s (%.4f%% of the layer's outputs), FP64, %.2f s" % (
             n, self.name, 100 * frac, dt)
         return self.per_pt_flops * n / dt / 1e12, self.oracle.max_threads(), sample
+
+
+def oracle_beside_layers(gpu_ms, seconds=2.0, samplers=None):
+    """The oracle's wall time per workload (a bounded sample scaled to the whole layer)
+    and the GPU speedup over it: gpu_ms maps a result key (a workload name, or
+    name+variant) to the GPU's milliseconds per launch.  A workload whose oracle run
+    fails records the error instead; the bench line is printed either way."""
+    samplers = {} if samplers is None else samplers
+    out = {}
+    for key, ms in gpu_ms.items():
+        name = key.split("+")[0]
+        if name not in WORKLOADS:
+            continue
+        try:
+            if name not in samplers:
+                samplers[name] = OracleSampler(name, max_points=1 << 22)
+            est = dict(samplers[name].full_layer(seconds))
+            est["gpu_ms"] = ms
+            est["gpu_speedup"] = est["full_layer_s"] / (ms * 1e-3)
+            out[key] = est
+        except Exception as exc:  # report, never abort the bench line
+            out[key] = {"error": "%s: %s" % (type(exc).__name__, exc)}
+    return out
 
 
 # ----------------------------------------------------------------------------- main
@@ -578,9 +614,14 @@ def main():
                "kernel": "depthwise_kernel (TMA halo tile)", "algorithmic_bytes_per_launch": dwr["bytes"]}
 
     cpu = None
+    oracle_layers = None
     if rank == 0 and not args.no_cpu_baseline:
-        tf, cores, sample = OracleSampler("body").step(12.0)
+        body_sampler = OracleSampler("body")
+        tf, cores, sample = body_sampler.step(12.0)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
+        gpu_ms = {"body": t_step_local * 1e3}
+        gpu_ms.update({k: r["ms"] for k, r in others.items() if k.split("+")[0] in WORKLOADS and "ms" in r})
+        oracle_layers = oracle_beside_layers(gpu_ms, samplers={"body": body_sampler})
 
     if rank == 0:
         line = {"metric": METRIC,
@@ -591,7 +632,7 @@ def main():
                 "gpu_launches": args.steps, "clocks": clk,
                 "depthwise": {"value": dwr["gbs"], "unit": "GB/s", "ms": dwr["ms"], "roofline": dw_roof,
                               "workload": WORKLOADS["dw"].description},
-                "layers": others, "peaks": peaks,
+                "layers": others, "oracle_per_layer": oracle_layers, "peaks": peaks,
                 "kernel_source_hash": {k: kernel_source_hash(k) for k in ("body", "dw", "stem")}}
         print(json.dumps(line))
     if dist:

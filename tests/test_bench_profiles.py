@@ -1,7 +1,9 @@
 """CPU checks of the benchmark's bookkeeping: the committed ncu summaries under profiles/
 are text, give the command that made them (ncu always with --clock-control none), and
 their per-launch DRAM traffic lines name a known workload with a source hash the
-benchmark can match."""
+benchmark can match; the oracle's per-layer wall-time estimates scale a bounded sample
+to the whole layer, take the transposed oracle for a transposed layer, and report a
+failure instead of raising."""
 import importlib.util
 import os
 import re
@@ -46,3 +48,27 @@ def test_both_arms_report_one_metric():
     src = open(os.path.join(ROOT, "bench.py")).read()
     assert src.count('"metric": METRIC') == 2  # the GPU arm and the reference arm
     assert "TFLOP/s" in bench.METRIC
+
+
+def test_oracle_beside_layers_scales_samples_and_skips_composites():
+    bench = _bench()
+    gpu_ms = {"tiny_f32": 0.01, "upsample": 0.05, "block": 0.1}
+    out = bench.oracle_beside_layers(gpu_ms, seconds=0.05)
+    assert set(out) == {"tiny_f32", "upsample"}  # the two-kernel block has no single oracle call
+    for key, est in out.items():
+        assert "error" not in est, est  # the transposed layer goes through its own oracle
+        assert est["full_layer_s"] > 0 and est["tflops"] > 0 and est["cores"] >= 1
+        assert abs(est["gpu_speedup"] - est["full_layer_s"] / (gpu_ms[key] * 1e-3)) < 1e-9 * est["gpu_speedup"]
+    s = bench.WORKLOADS["tiny_f32"].shape
+    assert "scaled to the layer's %d outputs" % (s.pixels * s.C_out) in out["tiny_f32"]["sample"]
+
+
+def test_oracle_beside_layers_reports_a_failure_without_raising():
+    bench = _bench()
+
+    class Broken:
+        def full_layer(self, seconds):
+            raise RuntimeError("no oracle here")
+
+    out = bench.oracle_beside_layers({"stem": 0.02}, samplers={"stem": Broken()})
+    assert out == {"stem": {"error": "RuntimeError: no oracle here"}}
