@@ -234,3 +234,25 @@ def test_sm_pair_choice(shape, sm_pairs, cluster):
 def test_sm_pair_flags_are_exclusive():
     st, h = _create(1, 128, 8, 8, 256, 3, 3, 1, 1, 1, 1, 1, 8 | 64)
     assert st == 1 and h.value is None
+
+
+# ----------------------------------------------------------------- tensor-rate measurement helper
+def test_mma_rate_rejects_bad_arguments_without_launching():
+    """Invalid counts, a null or misaligned cycles array, or an empty grid return before
+    any CUDA call (the pointers are only checked, never dereferenced)."""
+    L = cg.lib()
+    buf = (ctypes.c_ulonglong * 4)()
+    base = ctypes.addressof(buf)
+    assert L.conv_measure_mma_rate(0, ctypes.c_void_p(base), 1, None) == 1  # CONV_ERR_INVALID_ARG
+    assert L.conv_measure_mma_rate((1 << 20) + 1, ctypes.c_void_p(base), 1, None) == 1
+    assert L.conv_measure_mma_rate(16, None, 1, None) == 1
+    assert L.conv_measure_mma_rate(16, ctypes.c_void_p(base), 0, None) == 1
+    assert L.conv_measure_mma_rate(16, ctypes.c_void_p(base + 4), 1, None) == 3  # CONV_ERR_MISALIGNED
+    assert list(buf) == [0, 0, 0, 0]
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device behaviour")
+def test_mma_rate_without_device_fails_loudly():
+    L = cg.lib()
+    buf = (ctypes.c_ulonglong * 1)()
+    assert L.conv_measure_mma_rate(16, ctypes.c_void_p(ctypes.addressof(buf)), 1, None) == 4  # CONV_ERR_CUDA
