@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(HERE, "libconv.so")
 
 CONV_F32, CONV_BF16 = 0, 1
 CONV_FLAG_BIAS, CONV_FLAG_RELU, CONV_FLAG_OUT_BF16, CONV_FLAG_SM_PAIRS, CONV_FLAG_TRANSPOSED = 1, 2, 4, 8, 16
-CONV_FLAG_WINOGRAD, CONV_FLAG_ONE_SM = 32, 64
+CONV_FLAG_WINOGRAD, CONV_FLAG_ONE_SM, CONV_FLAG_PER_TAP = 32, 64, 128
 STATUS = {0: "CONV_OK", 1: "CONV_ERR_INVALID_ARG", 2: "CONV_ERR_UNSUPPORTED", 3: "CONV_ERR_MISALIGNED",
           4: "CONV_ERR_CUDA", 5: "CONV_ERR_NO_MEMORY", 6: "CONV_ERR_TIMEOUT"}
 PATHS = {0: "direct", 1: "depthwise", 2: "gemm_1x1", 3: "implicit_gemm", 4: "small_k_gemm", 5: "winograd"}
@@ -116,13 +116,15 @@ class ConvPlan:
     """
 
     def __init__(self, N, C_in, H, W, C_out, Kh, Kw, S=1, P=0, D=1, G=1, dtype="bf16",
-                 bias=True, relu=False, out_bf16=False, sm_pairs=None, transposed=False, winograd=False):
+                 bias=True, relu=False, out_bf16=False, sm_pairs=None, transposed=False, winograd=False,
+                 per_tap=False):
         L = lib()
         self._plan = None
         flags = (CONV_FLAG_BIAS if bias else 0) | (CONV_FLAG_RELU if relu else 0) | \
                 (CONV_FLAG_OUT_BF16 if out_bf16 else 0) | (CONV_FLAG_SM_PAIRS if sm_pairs is True else 0) | \
                 (CONV_FLAG_ONE_SM if sm_pairs is False else 0) | \
-                (CONV_FLAG_TRANSPOSED if transposed else 0) | (CONV_FLAG_WINOGRAD if winograd else 0)
+                (CONV_FLAG_TRANSPOSED if transposed else 0) | (CONV_FLAG_WINOGRAD if winograd else 0) | \
+                (CONV_FLAG_PER_TAP if per_tap else 0)
         dt = {"bf16": CONV_BF16, "f32": CONV_F32}[dtype]
         h = ctypes.c_void_p()
         st = L.conv_plan_create(ctypes.byref(h), N, C_in, H, W, C_out, Kh, Kw, S, P, D, G, dt, flags)
@@ -145,10 +147,10 @@ class ConvPlan:
         self.launch = dict(zip(("grid", "block", "smem_bytes", "stages", "cluster"), [v.value for v in li]))
 
     @classmethod
-    def for_shape(cls, s, sm_pairs=None, winograd=False):
+    def for_shape(cls, s, sm_pairs=None, winograd=False, per_tap=False):
         """Plan from a workloads.ConvShape-like object."""
         return cls(s.N, s.C_in, s.H, s.W, s.C_out, s.Kh, s.Kw, s.S, s.P, s.D, s.G, s.dtype,
-                   s.bias, s.relu, s.out_bf16, sm_pairs, getattr(s, "transposed", False), winograd)
+                   s.bias, s.relu, s.out_bf16, sm_pairs, getattr(s, "transposed", False), winograd, per_tap)
 
     def close(self):
         if self._plan is not None and _lib is not None:

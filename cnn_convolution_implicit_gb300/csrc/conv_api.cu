@@ -199,6 +199,11 @@ bool configure_tc(conv_plan* pl, bool one_by_one, bool transposed = false) {
                 best_area = area;
             }
         }
+        // halo mode (stride 1, not forced per tap): 8 x 16 tiles, one halo per channel block
+        if (t.mode == kTcModeRect && !(pl->flags & CONV_FLAG_PER_TAP)) {
+            t.mode = kTcModeHalo;
+            best = kTcHaloTileW;
+        }
         t.rect_w = best;
         t.rect_h = kTcBlockM / best;
         t.rect_tiles_w = (ew + t.rect_w - 1) / t.rect_w;
@@ -256,13 +261,84 @@ bool configure_tc(conv_plan* pl, bool one_by_one, bool transposed = false) {
         t.num_tiles = t.num_m_tiles * t.num_n_tiles;
     }
     const int b_rows = t.pair ? mma_n / 2 : mma_n;
-    const int stage_bytes = (t.dual ? 2 : 1) * kTcBlockM * kTcBlockK * 2 + b_rows * 128;
     const int fixed = 1024 + 256 + 8 * 2 * 32 * 64;  // alignment, barriers, epilogue store tiles
-    int stages = (pl->smem_optin - fixed) / stage_bytes;
-    if (stages > 8) stages = 8;
-    if (stages < 2 || stages < gpc) return false;
-    t.stages = stages;
-    t.smem_bytes = fixed + stages * stage_bytes;
+    t.halo = 0;
+    t.halo_w = t.halo_h = t.halo_bytes = t.halo_stages = 0;
+    t.btaps = 1;
+    if (t.mode == kTcModeHalo) {
+        // one box {64 ch, halo_w, halo_h} per 64-channel block: the tile (two side by side
+        // for two tiles per CTA) plus the (K-1)*D border its taps reach
+        long long hw = (t.dual ? 2 : 1) * kTcHaloTileW + static_cast<long long>(g.Kw - 1) * g.D;
+        const long long hh = kTcHaloTileH + static_cast<long long>(g.Kh - 1) * g.D;
+        const int taps = g.Kh * g.Kw;
+        // Taps per weight stage: each barrier wait of the MMA issuer costs a few hundred
+        // clocks under load, so a stage should carry >= 1,536 clocks of tensor work (a
+        // K = 16 MMA of M = 128 rows and N columns takes N/2 clocks per SM at the full
+        // rate; measured on the body layer: 1, 2, 3 taps per stage took 191, 154, 136 us).
+        // The largest such count that still leaves two halos and two weight stages in
+        // shared memory, with three halos when that keeps as many weight stages.
+        const int tap_clk = (t.dual ? 2 : 1) * (kTcBlockK / 16) * (mma_n / 2);
+        int bt_max = (1536 + tap_clk - 1) / tap_clk;
+        if (bt_max > taps) bt_max = taps;
+        int hs = 0, bs = 0, hbytes = 0, bt = 0;
+        if (hw <= 256 && hh <= 256) {
+            hbytes = static_cast<int>((hw * hh * 128 + 1023) / 1024 * 1024);
+            for (int cbt = bt_max; cbt >= 1 && hs == 0; --cbt) {
+                const long long stage = static_cast<long long>(cbt) * b_rows * 128;
+                auto fit = [&](int h) {
+                    const long long left = static_cast<long long>(pl->smem_optin) - fixed - static_cast<long long>(h) * hbytes;
+                    return left > 0 ? left / stage : 0;
+                };
+                const long long n2 = fit(2), n3 = fit(3);
+                if (n2 < 2) continue;
+                bt = cbt;
+                hs = (n3 >= 2 && n3 >= (n2 < 8 ? n2 : 8)) ? 3 : 2;
+                const long long nb = hs == 3 ? n3 : n2;
+                bs = static_cast<int>(nb > 8 ? 8 : nb);
+            }
+        }
+        if (hs > 0) {
+            t.halo = 1;
+            t.halo_w = static_cast<int>(hw);
+            t.halo_h = static_cast<int>(hh);
+            t.halo_bytes = hbytes;
+            t.halo_stages = hs;
+            if (t.dual) {  // a unit is a 16 x 16 region: both of its 8 x 16 tiles sit in one tile row
+                t.rect_tiles_w = 2 * ((g.W_out + 2 * kTcHaloTileW - 1) / (2 * kTcHaloTileW));
+                t.num_m_tiles = g.N * t.rect_tiles_w * t.rect_tiles_h;
+                t.num_tiles = t.num_m_tiles * t.num_n_tiles;
+            }
+            t.btaps = bt;
+            t.stages = bs;
+            t.smem_bytes = fixed + hs * hbytes + bs * bt * b_rows * 128;
+        } else {  // the halo does not fit: per-tap rectangle tiles
+            t.mode = kTcModeRect;
+            int best = 0;
+            long long best_area = 0;
+            auto padded = [](int extent, int tl) { return static_cast<long long>((extent + tl - 1) / tl) * tl; };
+            for (int tw : {16, 8, 32}) {
+                const long long area = padded(g.W_out, tw) * padded(g.H_out, kTcBlockM / tw);
+                if (best == 0 || area < best_area) {
+                    best = tw;
+                    best_area = area;
+                }
+            }
+            t.rect_w = best;
+            t.rect_h = kTcBlockM / best;
+            t.rect_tiles_w = (g.W_out + t.rect_w - 1) / t.rect_w;
+            t.rect_tiles_h = (g.H_out + t.rect_h - 1) / t.rect_h;
+            t.num_m_tiles = g.N * t.rect_tiles_w * t.rect_tiles_h;
+            t.num_tiles = t.num_m_tiles * t.num_n_tiles;
+        }
+    }
+    if (!t.halo) {
+        const int stage_bytes = (t.dual ? 2 : 1) * kTcBlockM * kTcBlockK * 2 + b_rows * 128;
+        int stages = (pl->smem_optin - fixed) / stage_bytes;
+        if (stages > 8) stages = 8;
+        if (stages < 2 || stages < gpc) return false;
+        t.stages = stages;
+        t.smem_bytes = fixed + stages * stage_bytes;
+    }
     t.tmem_cols = pow2_at_least((t.dual ? 4 : 2) * n_tile);
     t.relu = (pl->flags & CONV_FLAG_RELU) ? 1 : 0;
     t.status = pl->status;
@@ -361,7 +437,7 @@ CUresult encode_y_map(conv_plan* pl, void* y) {
                               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
-    if (t.mode == kTcModeRect) {  // {C_out, W_out, H_out, N}: 32/TW rows of TW pixels per store
+    if (t.mode == kTcModeRect || t.mode == kTcModeHalo) {  // {C_out, W_out, H_out, N}: 32/TW rows of TW pixels per store
         const cuuint32_t box[4] = {static_cast<cuuint32_t>(t.ychunk), static_cast<cuuint32_t>(t.rect_w),
                                    static_cast<cuuint32_t>(32 / t.rect_w), 1};
         const cuuint32_t estr[4] = {1, 1, 1, 1};
@@ -396,6 +472,18 @@ conv_status encode_maps(conv_plan* pl, const void* x, const void* w, void* y) {
             const cuuint32_t box[2] = {kTcBlockK, kTcBlockM};
             const cuuint32_t estr[2] = {1, 1};
             r = g_encode_tiled(&pl->map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides,
+                               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        } else if (pl->tc.mode == kTcModeHalo) {  // one box per 64-channel block: the tile's halo
+            const cuuint64_t dims[4] = {static_cast<cuuint64_t>(g.C_in), static_cast<cuuint64_t>(g.W),
+                                        static_cast<cuuint64_t>(g.H), static_cast<cuuint64_t>(g.N)};
+            const cuuint64_t strides[3] = {static_cast<cuuint64_t>(g.C_in) * 2,
+                                           static_cast<cuuint64_t>(g.W) * g.C_in * 2,
+                                           static_cast<cuuint64_t>(g.H) * g.W * g.C_in * 2};
+            const cuuint32_t box[4] = {kTcBlockK, static_cast<cuuint32_t>(pl->tc.halo_w),
+                                       static_cast<cuuint32_t>(pl->tc.halo_h), 1};
+            const cuuint32_t estr[4] = {1, 1, 1, 1};
+            r = g_encode_tiled(&pl->map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides,
                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         } else if (pl->tc.mode == kTcModeRect || pl->tc.mode == kTcModePhase) {
@@ -487,7 +575,7 @@ conv_status conv_plan_create(conv_plan** out, int N, int C_in, int H, int W, int
     if (C_in % G != 0 || C_out % G != 0) return CONV_ERR_INVALID_ARG;
     if (dtype != CONV_F32 && dtype != CONV_BF16) return CONV_ERR_INVALID_ARG;
     if (flags & ~(CONV_FLAG_BIAS | CONV_FLAG_RELU | CONV_FLAG_OUT_BF16 | CONV_FLAG_SM_PAIRS | CONV_FLAG_TRANSPOSED |
-                  CONV_FLAG_WINOGRAD | CONV_FLAG_ONE_SM))
+                  CONV_FLAG_WINOGRAD | CONV_FLAG_ONE_SM | CONV_FLAG_PER_TAP))
         return CONV_ERR_INVALID_ARG;
     if ((flags & CONV_FLAG_SM_PAIRS) && (flags & CONV_FLAG_ONE_SM)) return CONV_ERR_INVALID_ARG;
     if ((flags & CONV_FLAG_OUT_BF16) && dtype != CONV_F32) return CONV_ERR_INVALID_ARG;
@@ -588,7 +676,7 @@ conv_status conv_plan_launch_info(const conv_plan* p, int* grid, int* block, int
         case CONV_PATH_GEMM_1X1:
         case CONV_PATH_IMPLICIT_GEMM: {
             const TcGemmParams& t = p->tc;
-            bl = kTcThreads;
+            bl = t.halo ? kTcHaloThreads : kTcThreads;
             sm = t.smem_bytes;
             st = t.stages;
             if (t.pair) {

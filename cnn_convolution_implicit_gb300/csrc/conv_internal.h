@@ -97,9 +97,21 @@ cudaError_t launch_depthwise(const CUtensorMap& x_map, const DepthwiseParams& p,
 constexpr int kTcBlockM = 128;    // pixels per tile (TMEM lanes)
 constexpr int kTcBlockK = 64;     // BF16 elements per K-step (one 128-byte swizzle row)
 constexpr int kTcThreads = 576;   // producer warp, MMA warp, 4 x 4 epilogue warps
+constexpr int kTcHaloThreads = 608;  // halo mode: + a weight producer warp (the halo producer is warp 0)
+constexpr int kTcBWarp = 18;      // halo mode: the weight (B operand) producer warp
 constexpr int kTcMaxGroupsPerTile = 8;  // groups packed side by side in one accumulator (<= ring stages)
 
-enum TcMode { kTcMode1x1 = 0, kTcModeIm2col = 1, kTcModeRect = 2, kTcModePhase = 3 };
+enum TcMode { kTcMode1x1 = 0, kTcModeIm2col = 1, kTcModeRect = 2, kTcModePhase = 3, kTcModeHalo = 4 };
+
+// kTcModeHalo (stride 1): pixel tiles are 8 wide x 16 high, so each 8-row core-matrix
+// group of the MMA's A operand is one output row segment.  One TMA box per 64-channel
+// block brings the tile's input halo (kTcHaloTileW + (Kw-1)*D) x (16 + (Kh-1)*D) pixels
+// (x2 wide for two tiles per CTA) into shared memory, and every tap (kh, kw) reads it
+// through a descriptor whose start is shifted by kh*D*halo_w + kw*D pixel rows and
+// whose 8-row stride is halo_w rows.
+constexpr int kTcHaloTileW = 8;
+constexpr int kTcHaloTileH = 16;
+constexpr int kTcMaxHaloStages = 4;
 
 // Transposed convolution (kTcModePhase, any stride S): output pixels split into
 // S x S phases by (h mod S, w mod S); phase residue r of one axis uses the kernel
@@ -130,6 +142,11 @@ struct TcGemmParams {
     int smem_bytes;
     int pair;          // 1: CTA-pair kernel (B rows split across the two CTAs)
     int dual;          // 1: two pixel tiles per CTA (M = 256, two accumulators; n_tile <= 128)
+    int halo;          // 1: kTcModeHalo (one input halo per 64-channel block feeds every tap)
+    int halo_w, halo_h;  // kTcModeHalo: halo box extent in pixels (TMA box {64, halo_w, halo_h, 1})
+    int halo_bytes;      // kTcModeHalo: one halo stage (box bytes rounded up to 1024)
+    int halo_stages;     // kTcModeHalo: halos in flight (stages is then the weight ring)
+    int btaps;           // kTcModeHalo: taps per weight stage (one barrier wait feeds btaps x 4 MMAs)
     int ps;            // kTcModePhase: the transposed convolution's stride S (phases = S*S)
     int hq, wq;        // kTcModePhase: output rows / columns per phase (H_out / S, W_out / S)
     TcPhaseAxis ph, pw;

@@ -277,6 +277,20 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
            (static_cast<uint64_t>(2) << 61);
 }
 
+// The same K-major 128-byte-swizzle operand, read from a tile whose rows need
+// not start on a 1,024-byte swizzle atom and whose 8-row groups lie `sbo_bytes`
+// apart (a multiple of 128): row r = 8g + i is at start + g*sbo + i*128.  The
+// TMA wrote every row with the swizzle phase of its own shared-memory address,
+// and the tensor core applies the pattern by absolute address as well, so the
+// descriptor's base-offset field (bits 49-51) stays 0 for any start.  (Setting
+// it to the start's phase within the atom, (start >> 7) & 7, read the rows
+// with the wrong phase on this part: the parity checks failed.)
+__device__ __forceinline__ uint64_t sdesc_sw128_rows(uint32_t saddr, uint32_t sbo_bytes) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
 // ------------------------------------------------------------------ CTA pairs (clusters of 2)
 // These forms drive one MMA across two SMs: A is split along M (128 rows per
 // CTA), B along N (N/2 rows per CTA), each CTA's TMEM holds its 128 rows of D.

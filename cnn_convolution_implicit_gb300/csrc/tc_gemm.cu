@@ -24,8 +24,10 @@
 // Groups are independent GEMMs (variants page, sections 2.2 and 4.3): a tile
 // packs `gpc` groups side by side in TMEM columns, each with its own K loop.
 //
-// Warp roles (576 threads, one CTA per SM, persistent over tiles):
-//   warp 0      TMA producer (one lane): A (pixels x 64 ch) and B (C_out x 64) per K-step
+// Warp roles (576 threads, 608 in halo mode; one CTA per SM, persistent over tiles):
+//   warp 0      TMA producer (one lane): A (pixels x 64 ch) and B (C_out x 64) per
+//               K-step; in halo mode the halos only
+//   warp 18     halo mode: TMA producer (one lane) of the weight stages
 //   warp 1      TMEM allocator; one lane issues tcgen05.mma and commits
 //   warps 2..17 epilogue, four groups of four, two per TMEM accumulator (each
 //               group drains half of its columns): tcgen05.ld -> +bias -> ReLU ->
@@ -51,7 +53,7 @@ constexpr uint32_t kABytes = kTcBlockM * kTcBlockK * 2;  // 16 KB
 constexpr uint32_t kOutTileBytes = 32 * 64;               // one store tile: 32 pixels x 32 channels
 
 struct TcSmem {
-    uint8_t* a;
+    uint8_t* a;    // A ring (per-tap modes) or halo ring (halo mode)
     uint8_t* b;
     uint8_t* out;  // per epilogue warp: two store tiles
     uint64_t* full;
@@ -59,15 +61,19 @@ struct TcSmem {
     uint64_t* tfull;
     uint64_t* tempty;
     uint64_t* drain;
+    uint64_t* hfull;   // halo mode: halo landed
+    uint64_t* hempty;  // halo mode: every tap of the halo consumed
     uint32_t* tmem_slot;
     int* abort;
 };
 
+// a_bytes: one A stage (per-tap modes) or one halo stage (halo mode, p.halo_stages of them).
 __device__ __forceinline__ TcSmem carve(uint8_t* raw, const TcGemmParams& p, uint32_t a_bytes, uint32_t b_bytes) {
     TcSmem s;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    const int a_stages = p.halo ? p.halo_stages : p.stages;
     s.a = base;
-    s.b = base + p.stages * a_bytes;
+    s.b = s.a + a_stages * a_bytes;
     s.out = s.b + p.stages * b_bytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(s.out + 8 * 2 * kOutTileBytes);
     s.full = bars;
@@ -75,7 +81,9 @@ __device__ __forceinline__ TcSmem carve(uint8_t* raw, const TcGemmParams& p, uin
     s.tfull = bars + 2 * p.stages;
     s.tempty = s.tfull + 2;
     s.drain = s.tempty + 2;
-    s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
+    s.hfull = s.drain + 1;
+    s.hempty = s.hfull + kTcMaxHaloStages;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(s.hempty + kTcMaxHaloStages);
     s.abort = reinterpret_cast<int*>(s.tmem_slot + 1);
     return s;
 }
@@ -92,7 +100,8 @@ __device__ __forceinline__ void sub_gemm(const TcGemmParams& p, int nt, int j, i
 }
 
 // Where pixel tile m sits.  Linear modes: pixels [m*128, m*128 + 128) in
-// (n, ho, wo) order.  Rect mode: image n, rows [ho0, ho0 + TH), cols [wo0, wo0 + TW).
+// (n, ho, wo) order.  Rect and halo modes: image n, rows [ho0, ho0 + TH), cols
+// [wo0, wo0 + TW).
 struct PixTile {
     long long pix0;
     int n, ho0, wo0;
@@ -126,7 +135,7 @@ __device__ __forceinline__ PixTile pix_tile(const TcGemmParams& p, int m) {
         t.ho0 = th * p.rect_h;
         t.wo0 = (r - th * p.rect_tiles_w) * p.rect_w;
         t.pix0 = 0;
-    } else if (p.mode == kTcModeRect) {
+    } else if (p.mode == kTcModeRect || p.mode == kTcModeHalo) {
         const int per_img = p.rect_tiles_h * p.rect_tiles_w;
         t.n = m / per_img;
         const int r = m - t.n * per_img;
@@ -185,6 +194,262 @@ __device__ __forceinline__ void load_a(const TcGemmParams& p, const CUtensorMap*
     }
 }
 
+// ---------------------------------------------------------------- halo mode
+// The halo mode's K loop runs channel blocks outer, taps inner: a "block" is
+// one (unit, sub-GEMM, 64-channel block) and owns one halo; its Kh*Kw taps each
+// take one weight stage.  A CTA walks its blocks with running counters (the
+// producer keeps two walkers, one for the halos it issues ahead and one for the
+// weights): only a new unit costs divisions, to place its pixel tile.
+struct HaloWalk {
+    int u, nt, j, kb;  // unit, its n-tile, sub-GEMM, channel block
+    int c, brow;       // first input channel and first weight row of the block
+    int w0, h0, n;     // the halo box origin of the unit's tile
+};
+
+template <bool PAIR, bool DUAL>
+__device__ __forceinline__ void halo_walk_block(const TcGemmParams& p, HaloWalk& w) {
+    int grp, brow;
+    sub_gemm(p, w.nt, w.j, grp, brow);
+    w.c = grp * p.g.cin_g + w.kb * kTcBlockK;
+    w.brow = brow;
+}
+
+template <bool PAIR, bool DUAL>
+__device__ __forceinline__ void halo_walk_unit(const TcGemmParams& p, HaloWalk& w, uint32_t rank) {
+    const int mu = w.u / p.num_n_tiles;
+    w.nt = w.u - mu * p.num_n_tiles;
+    const int m = PAIR ? 2 * mu + static_cast<int>(rank) : (DUAL ? 2 * mu : mu);
+    PixTile t = pix_tile<false, PAIR || DUAL>(p, m);
+    if (!t.exists) t = pix_tile<false, PAIR || DUAL>(p, p.num_m_tiles - 1);  // loaded, never stored
+    w.w0 = t.wo0 - p.g.P;
+    w.h0 = t.ho0 - p.g.P;
+    w.n = t.n;
+    halo_walk_block<PAIR, DUAL>(p, w);
+}
+
+template <bool PAIR, bool DUAL>
+__device__ __forceinline__ void halo_walk_start(const TcGemmParams& p, HaloWalk& w, int unit0, uint32_t rank) {
+    w.u = unit0;
+    w.j = w.kb = 0;
+    halo_walk_unit<PAIR, DUAL>(p, w, rank);
+}
+
+template <bool PAIR, bool DUAL>
+__device__ __forceinline__ void halo_walk_next(const TcGemmParams& p, HaloWalk& w, int unit_step, int num_units,
+                                               uint32_t rank) {
+    if (++w.kb < p.kblk) {
+        halo_walk_block<PAIR, DUAL>(p, w);
+        return;
+    }
+    w.kb = 0;
+    if (++w.j < p.gpc) {
+        halo_walk_block<PAIR, DUAL>(p, w);
+        return;
+    }
+    w.j = 0;
+    w.u += unit_step;
+    if (w.u < num_units) halo_walk_unit<PAIR, DUAL>(p, w, rank);
+}
+
+// Every fill of a ring this thread issued has landed (the leader sees its full
+// barriers complete; a pair's peer sees the MMA release each slot, which needs
+// the fill landed), so the CTA may exit with no copy in flight.
+__device__ __forceinline__ void drain_ring(uint64_t* full, uint64_t* empty, int stages, long long issued, bool leader,
+                                           unsigned* status, volatile int* abort) {
+    for (int s = 0; s < stages; ++s) {
+        const long long fills = issued / stages + (s < issued % stages ? 1 : 0);
+        if (fills == 0) continue;
+        const uint32_t par = static_cast<uint32_t>((fills - 1) & 1);
+        const bool done = leader ? mbar_wait(&full[s], par, nullptr) : mbar_wait(&empty[s], par, nullptr);
+        if (!done) record_status(status, kStatusTimeoutDrain, abort);
+    }
+}
+
+// Producers (one thread per role).  ROLE 0 issues the blocks' halos in order,
+// up to halo_stages ahead of the MMAs; ROLE 1 issues the weight stages.  A weight
+// stage holds `btaps` consecutive taps of one block (the last stage of a block
+// may hold fewer), so every barrier wait of the MMA issuer is followed by enough
+// MMAs to cover its latency.  Each role drains its own ring before returning.
+template <bool PAIR, bool DUAL, int ROLE>
+__device__ __forceinline__ void halo_producer(const TcGemmParams& p, const CUtensorMap* a_map,
+                                              const CUtensorMap* b_map, const TcSmem& sm, int unit0, int unit_step,
+                                              int num_units, uint32_t rank, bool leader, volatile int* abort) {
+    const int T = p.g.Kh * p.g.Kw;
+    const int my_units = unit0 < num_units ? (num_units - 1 - unit0) / unit_step + 1 : 0;
+    const int nblocks = my_units * p.gpc * p.kblk;
+    if (nblocks == 0) return;
+    HaloWalk w;
+    halo_walk_start<PAIR, DUAL>(p, w, unit0, rank);
+    long long issued = 0;
+    int st = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    if constexpr (ROLE == 0) {
+        const int HS = p.halo_stages;
+        const uint32_t h_tx = (PAIR ? 2u : 1u) * static_cast<uint32_t>(p.halo_w * p.halo_h) * 128u;
+        for (int blk = 0; blk < nblocks; ++blk) {
+            if (!mbar_wait(&sm.hempty[st], ph ^ 1u, abort)) {
+                record_status(p.status, kStatusTimeoutProducer, abort);
+                break;
+            }
+            if (leader) mbar_arrive_expect_tx(&sm.hfull[st], h_tx);
+            uint8_t* dst = sm.a + st * p.halo_bytes;
+            if constexpr (PAIR)
+                tma_load_4d_pair(dst, a_map, mapa_shared(smem_addr(&sm.hfull[st]), 0), w.c, w.w0, w.h0, w.n);
+            else
+                tma_load_4d(dst, a_map, &sm.hfull[st], w.c, w.w0, w.h0, w.n);
+            ++issued;
+            if (++st == HS) {
+                st = 0;
+                ph ^= 1u;
+            }
+            if (blk + 1 < nblocks) halo_walk_next<PAIR, DUAL>(p, w, unit_step, num_units, rank);
+        }
+        drain_ring(sm.hfull, sm.hempty, HS, issued, leader, p.status, abort);
+    } else {
+        const int BT = p.btaps, BS = p.stages;
+        const int b_rows = PAIR ? p.mma_n / 2 : p.mma_n;
+        const uint32_t b_tap = static_cast<uint32_t>(b_rows) * 128u;  // one tap's weight rows in this CTA
+        const uint32_t b_tx = (PAIR ? 2u : 1u) * b_tap;
+        for (int blk = 0; blk < nblocks && ok; ++blk) {
+            for (int tap0 = 0; tap0 < T; tap0 += BT) {
+                if (!mbar_wait(&sm.empty[st], ph ^ 1u, abort)) {
+                    record_status(p.status, kStatusTimeoutProducer, abort);
+                    ok = false;
+                    break;
+                }
+                const int nt = T - tap0 < BT ? T - tap0 : BT;
+                if (leader) mbar_arrive_expect_tx(&sm.full[st], b_tx * static_cast<uint32_t>(nt));
+                uint8_t* b_dst = sm.b + st * b_tap * static_cast<uint32_t>(BT);
+                const uint32_t full_leader = PAIR ? mapa_shared(smem_addr(&sm.full[st]), 0) : 0u;
+                for (int i = 0; i < nt; ++i) {
+                    const int kcol = (tap0 + i) * p.g.cin_g + w.kb * kTcBlockK;
+                    if constexpr (PAIR)
+                        tma_load_2d_pair(b_dst + i * b_tap, b_map, full_leader, kcol,
+                                         w.brow + static_cast<int>(rank) * b_rows);
+                    else
+                        tma_load_2d(b_dst + i * b_tap, b_map, &sm.full[st], kcol, w.brow);
+                }
+                ++issued;
+                if (++st == BS) {
+                    st = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (blk + 1 < nblocks) halo_walk_next<PAIR, DUAL>(p, w, unit_step, num_units, rank);
+        }
+        drain_ring(sm.full, sm.empty, BS, issued, leader, p.status, abort);
+    }
+}
+
+// MMA issuer (one thread of the leader).  Per block: wait for its halo; per
+// weight stage: wait once, then for each of its taps issue the K = 64 slice as
+// four K = 16 MMAs whose A descriptor starts at the tap's shifted halo row.
+template <bool PAIR, bool DUAL>
+__device__ __forceinline__ void halo_mma(const TcGemmParams& p, const TcSmem& sm, uint32_t tmem_base, int unit0,
+                                         int unit_step, int num_units, volatile int* abort) {
+    const uint32_t idesc = idesc_bf16_f32((PAIR ? 2 : 1) * kTcBlockM, p.mma_n);
+    const int T = p.g.Kh * p.g.Kw;
+    const int BT = p.btaps;
+    const int b_rows = PAIR ? p.mma_n / 2 : p.mma_n;
+    const uint32_t b_tap = static_cast<uint32_t>(b_rows) * 128u;
+    const uint32_t b_stage = b_tap * static_cast<uint32_t>(BT);
+    const uint32_t sbo = static_cast<uint32_t>(p.halo_w) * 128u;   // 8 output rows apart: one halo row
+    const uint32_t row_kh = static_cast<uint32_t>(p.g.D * p.halo_w) * 128u;
+    const uint32_t row_kw = static_cast<uint32_t>(p.g.D) * 128u;
+    int hs = 0, bs = 0;
+    uint32_t hph = 0, bph = 0;
+    int local = 0;
+    bool ok = true;
+    for (int u = unit0; u < num_units && ok; u += unit_step, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = static_cast<uint32_t>(local >> 1) & 1u;
+        const bool free_acc = PAIR ? mbar_wait_cluster(&sm.tempty[buf], use ^ 1u, abort)
+                                   : mbar_wait(&sm.tempty[buf], use ^ 1u, abort);
+        if (!free_acc) {
+            record_status(p.status, kStatusTimeoutMma, abort);
+            break;
+        }
+        tc_fence_after();
+        const uint32_t d_base = tmem_base + static_cast<uint32_t>(buf * (DUAL ? 2 : 1) * p.n_tile);
+        for (int j = 0; j < p.gpc && ok; ++j) {
+            const uint32_t d = d_base + static_cast<uint32_t>(j * p.mma_n);
+            for (int kb = 0; kb < p.kblk && ok; ++kb) {
+                if (!mbar_wait(&sm.hfull[hs], hph, abort)) {
+                    record_status(p.status, kStatusTimeoutMma, abort);
+                    ok = false;
+                    break;
+                }
+                const uint32_t hbase = smem_addr(sm.a + hs * p.halo_bytes);
+                int kh = 0, kw = 0;
+                for (int tap0 = 0; tap0 < T; tap0 += BT) {
+                    if (!mbar_wait(&sm.full[bs], bph, abort)) {
+                        record_status(p.status, kStatusTimeoutMma, abort);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int nt = T - tap0 < BT ? T - tap0 : BT;
+                    const uint32_t bbase = smem_addr(sm.b + bs * b_stage);
+                    for (int i = 0; i < nt; ++i) {
+                        const uint32_t a_addr =
+                            hbase + static_cast<uint32_t>(kh) * row_kh + static_cast<uint32_t>(kw) * row_kw;
+                        const uint64_t adesc = sdesc_sw128_rows(a_addr, sbo);
+                        const uint64_t bdesc = sdesc_sw128(bbase + static_cast<uint32_t>(i) * b_tap);
+                        const uint32_t first = (kb | tap0 | i) != 0 ? 1u : 0u;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            if constexpr (PAIR)
+                                mma_bf16_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (first | k) != 0 ? 1u : 0u);
+                            else
+                                mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (first | k) != 0 ? 1u : 0u);
+                        }
+                        if constexpr (DUAL) {
+                            const uint64_t adesc1 = sdesc_sw128_rows(a_addr + 8u * 128u, sbo);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                mma_bf16(d + static_cast<uint32_t>(p.n_tile), adesc1 + 2 * k, bdesc + 2 * k, idesc,
+                                         (first | k) != 0 ? 1u : 0u);
+                        }
+                        if (++kw == p.g.Kw) {
+                            kw = 0;
+                            ++kh;
+                        }
+                    }
+                    if constexpr (PAIR)
+                        mma_commit_pair(&sm.empty[bs], 0x3);
+                    else
+                        mma_commit(&sm.empty[bs]);
+                    if (++bs == p.stages) {
+                        bs = 0;
+                        bph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if constexpr (PAIR)
+                    mma_commit_pair(&sm.hempty[hs], 0x3);
+                else
+                    mma_commit(&sm.hempty[hs]);
+                if (++hs == p.halo_stages) {
+                    hs = 0;
+                    hph ^= 1u;
+                }
+            }
+        }
+        if (ok) {
+            if constexpr (PAIR)
+                mma_commit_pair(&sm.tfull[buf], 0x3);
+            else
+                mma_commit(&sm.tfull[buf]);
+        }
+    }
+    if constexpr (PAIR)
+        mma_commit_pair(sm.drain, 0x1);
+    else
+        mma_commit(sm.drain);
+    if (!mbar_wait(sm.drain, 0, nullptr)) record_status(p.status, kStatusTimeoutDrain, abort);
+}
+
 }  // namespace
 
 // PHASE: the transposed-convolution phase mode (kTcModePhase), compiled
@@ -193,8 +458,10 @@ __device__ __forceinline__ void load_a(const TcGemmParams& p, const CUtensorMap*
 // output channels: each K-step loads both tiles' A operands and one weight
 // block and issues the MMAs of both into two accumulators, so the producer's
 // per-K-step work feeds twice the tensor work.
-template <bool PAIR, bool PHASE, bool DUAL>
-__global__ void __launch_bounds__(kTcThreads, 1)
+// HALO: the halo mode (kTcModeHalo, stride 1): one input halo per 64-channel
+// block feeds every tap through shifted descriptors.
+template <bool PAIR, bool PHASE, bool DUAL, bool HALO = false>
+__global__ void __launch_bounds__(HALO ? kTcHaloThreads : kTcThreads, 1)
     tc_conv_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
                    const __grid_constant__ CUtensorMap y_map, const TcGemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -202,7 +469,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr uint32_t a_stage = DUAL ? 2 * kABytes : kABytes;
     const int b_rows = PAIR ? p.mma_n / 2 : p.mma_n;  // weight rows this CTA loads per K-step
     const uint32_t b_bytes = static_cast<uint32_t>(b_rows) * 128u;
-    const TcSmem sm = carve(smem_raw, p, a_stage, b_bytes);
+    const TcSmem sm = carve(smem_raw, p, HALO ? static_cast<uint32_t>(p.halo_bytes) : a_stage,
+                            HALO ? b_bytes * static_cast<uint32_t>(p.btaps) : b_bytes);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     volatile int* abort = sm.abort;
@@ -223,6 +491,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&sm.tempty[b], PAIR ? 2 * 8 : 8);  // one arrival per warp of its two epilogue groups (both CTAs)
         }
         mbar_init(sm.drain, 1);
+        if constexpr (HALO) {
+            for (int h = 0; h < p.halo_stages; ++h) {
+                mbar_init(&sm.hfull[h], 1);
+                mbar_init(&sm.hempty[h], 1);
+            }
+        }
         *sm.abort = 0;
         fence_barrier_init();
         tma_prefetch_desc(&a_map);
@@ -244,7 +518,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *sm.tmem_slot;
 
-    if (warp == 0) {
+    if (HALO && (warp == 0 || warp == kTcBWarp)) {
+        if (lane == 0) {
+            if (warp == 0)
+                halo_producer<PAIR, DUAL, 0>(p, &a_map, &b_map, sm, unit0, unit_step, num_units, rank, leader, abort);
+            else
+                halo_producer<PAIR, DUAL, 1>(p, &a_map, &b_map, sm, unit0, unit_step, num_units, rank, leader, abort);
+        }
+    } else if (HALO && warp == 1) {
+        if (lane == 0 && leader) halo_mma<PAIR, DUAL>(p, sm, tmem_base, unit0, unit_step, num_units, abort);
+    } else if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             int stage = 0;
@@ -451,7 +734,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 yc1 = t.wo0;
                 yc2 = h;
                 yc3 = t.n;
-            } else if (p.mode == kTcModeRect) {
+            } else if (p.mode == kTcModeRect || p.mode == kTcModeHalo) {
                 const int h = t.ho0 + quarter * 32 / p.rect_w;
                 rows_exist = t.exists && h < p.g.H_out && t.wo0 < p.g.W_out;
                 yc1 = t.wo0;
@@ -484,7 +767,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (lane == 0 && rows_exist) {
                     if (PHASE)
                         tma_store_5d(&y_map, stg, co0 + c, t.rw, yc1, t.rh, yc3 * p.hq + yc2);
-                    else if (p.mode == kTcModeRect)
+                    else if (p.mode == kTcModeRect || p.mode == kTcModeHalo)
                         tma_store_4d(&y_map, stg, co0 + c, yc1, yc2, yc3);
                     else
                         tma_store_2d(&y_map, stg, co0 + c, yc1);
@@ -519,8 +802,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // per-device dynamic shared-memory limit already set on the pair kernel
 static int g_pair_smem_limits[64] = {};
 
+namespace {
+
+// Launch one instantiation: clusters of two CTAs for SM pairs, else plain.
+template <bool PAIR, bool PHASE, bool DUAL, bool HALO>
+cudaError_t launch_one(const CUtensorMap& a_map, const CUtensorMap& b_map, const CUtensorMap& y_map,
+                       const TcGemmParams& p, int grid, cudaStream_t stream) {
+    static int limits[64] = {};
+    auto* fn = tc_conv_kernel<PAIR, PHASE, DUAL, HALO>;
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fn), p.smem_bytes, limits);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(HALO ? kTcHaloThreads : kTcThreads, 1, 1);
+    cfg.dynamicSmemBytes = p.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = PAIR ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, fn, a_map, b_map, y_map, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, const CUtensorMap& y_map,
                            const TcGemmParams& p, int grid, cudaStream_t stream) {
+    if (p.halo) {
+        if (p.pair) return launch_one<true, false, false, true>(a_map, b_map, y_map, p, grid, stream);
+        if (p.dual) return launch_one<false, false, true, true>(a_map, b_map, y_map, p, grid, stream);
+        return launch_one<false, false, false, true>(a_map, b_map, y_map, p, grid, stream);
+    }
     if (p.pair) {
         static int pair_phase_limits[64] = {};
         cudaError_t e = p.mode == kTcModePhase
@@ -576,14 +893,16 @@ cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, c
 }
 
 int tc_gemm_pair_max_clusters(const TcGemmParams& p) {
-    if (ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<true, false, false>), p.smem_bytes,
-                          g_pair_smem_limits) != cudaSuccess) {
+    static int halo_pair_limits[64] = {};
+    const void* fn = p.halo ? reinterpret_cast<const void*>(tc_conv_kernel<true, false, false, true>)
+                            : reinterpret_cast<const void*>(tc_conv_kernel<true, false, false>);
+    if (ensure_smem_limit(fn, p.smem_bytes, p.halo ? halo_pair_limits : g_pair_smem_limits) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.blockDim = dim3(p.halo ? kTcHaloThreads : kTcThreads, 1, 1);
     cfg.dynamicSmemBytes = p.smem_bytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -593,7 +912,9 @@ int tc_gemm_pair_max_clusters(const TcGemmParams& p) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_conv_kernel<true, false, false>, &cfg) != cudaSuccess) {
+    const cudaError_t e = p.halo ? cudaOccupancyMaxActiveClusters(&n, tc_conv_kernel<true, false, false, true>, &cfg)
+                                 : cudaOccupancyMaxActiveClusters(&n, tc_conv_kernel<true, false, false>, &cfg);
+    if (e != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }

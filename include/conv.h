@@ -63,6 +63,15 @@ enum {
                                   64-channel blocks), one SM otherwise */
     CONV_FLAG_TRANSPOSED = 16u, /* transposed convolution (see below)                 */
     CONV_FLAG_ONE_SM = 64u,    /* tensor-core GEMM paths: one SM per 128-pixel tile    */
+    CONV_FLAG_PER_TAP = 128u,  /* stride-1 implicit GEMM: gather each tap's 128 input
+                                  pixels as their own TMA box (every input pixel lands
+                                  in shared memory once per tap) instead of the default
+                                  halo tiles, where one box per 64-channel block holds
+                                  the input under an 8 x 16 output tile plus the
+                                  (K-1)*D border its taps reach and every tap reads it
+                                  ("GPU lesson 9", sections 6 and 12-13: input reuse
+                                  across a tile's taps).  Same results up to the order
+                                  of the FP32 sum.  Ignored by other plans. */
     CONV_FLAG_WINOGRAD = 32u   /* FP32 3x3, stride 1, dilation 1, G = 1: Winograd F(2x2, 3x3)
                                   ("Convolution vs inner product", lnrq.cn, section 2.2;
                                   variants page, section 3.3): 4 multiplies per output

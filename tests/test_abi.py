@@ -52,7 +52,7 @@ def _create(*args):
     (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 1, 4),        # OUT_BF16 with BF16 input
     (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 2, 0),        # bad dtype
     (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 256),      # unknown flag
-    (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 128),      # unknown flag
+    (1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 512),      # unknown flag
     (1, 3, 2, 2, 4, 3, 3, 1, 3, 1, 1, 0, 16),       # transposed with an empty output: (2-1) - 6 + 2 + 1 < 1
 ])
 def test_create_rejects_bad_shapes(args):
@@ -256,3 +256,25 @@ def test_mma_rate_without_device_fails_loudly():
     L = cg.lib()
     buf = (ctypes.c_ulonglong * 1)()
     assert L.conv_measure_mma_rate(16, ctypes.c_void_p(ctypes.addressof(buf)), 1, None) == 4  # CONV_ERR_CUDA
+
+
+# Stride-1 BF16 implicit-GEMM plans take the halo mode (one input halo per 64-channel
+# block, 8 x 16 output tiles, a second producer warp: 608 threads); CONV_FLAG_PER_TAP,
+# other strides, 1x1 layers and halos wider than a TMA box (256) keep one box per tap.
+@pytest.mark.parametrize("shape,halo", [
+    ((32, 128, 112, 112, 256, 3, 3, 1, 1, 1, 1), True),     # body layer (SM pairs)
+    ((16, 256, 64, 64, 256, 3, 3, 1, 2, 2, 4), True),       # dilated grouped (two tiles per CTA)
+    ((2, 64, 12, 12, 64, 5, 5, 1, 2, 1, 1), True),          # 5x5
+    ((2, 64, 10, 14, 64, 1, 3, 1, 1, 1, 1), True),          # 1x3
+    ((2, 512, 8, 8, 128, 3, 3, 1, 2, 2, 8), True),          # groups packed side by side
+    ((1, 128, 9, 11, 256, 3, 3, 2, 1, 1, 1), False),        # stride 2: TMA im2col mode
+    ((2, 256, 9, 13, 512, 1, 1, 1, 0, 1, 1), False),        # 1x1 GEMM
+    ((1, 64, 4, 300, 64, 1, 3, 1, 125, 125, 1), False),     # halo 8 + 2*125 = 258 columns > 256
+])
+def test_halo_mode_choice(shape, halo):
+    p = cg.ConvPlan(*shape, dtype="bf16", bias=True, relu=True)
+    assert p.path in ("implicit_gemm", "gemm_1x1")
+    assert p.launch["block"] == (608 if halo else 576)
+    assert p.launch["smem_bytes"] <= 232448 and p.launch["stages"] >= 2
+    q = cg.ConvPlan(*shape, dtype="bf16", bias=True, relu=True, per_tap=True)
+    assert q.path == p.path and q.launch["block"] == 576

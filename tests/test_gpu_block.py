@@ -76,12 +76,13 @@ def test_block_matches_oracle(case):
     assert torch.equal(y, y2), worst
 
 
-def test_block_full_size_points_and_matches_two_kernel_path():
-    """The full-size block (N64, 256 -> 512, 56x56): sampled outputs against the oracle,
-    and every output bit-identical to the two-launch path (depthwise kernel writing BF16,
-    then the 1x1 GEMM kernel), which computes the same sums in the same order."""
+def test_block_full_size_and_matches_two_kernel_path():
+    """The full-size block (N64, 256 -> 512, 56x56): every output against the oracle (with
+    the BF16 intermediate, and end to end in FP64), and bit-identical to the two-launch
+    path (depthwise kernel writing BF16, then the 1x1 GEMM kernel), which computes the
+    same sums in the same order."""
     from cnn_convolution_implicit_gb300 import BlockPlan, ConvPlan, device_status
-    from parity import check_points, sample_points
+    from parity import check_full
     from workloads import w_device
     sd, x, wd, _ = inputs("dw")
     sp, _, wp, bp = inputs("pw")
@@ -99,11 +100,11 @@ def test_block_full_size_points_and_matches_two_kernel_path():
     y2 = ConvPlan.for_shape(sp).forward(mid, w_device(wp, "bf16"), bd)
     torch.cuda.synchronize()
     assert torch.equal(y, y2)
-    # sampled points against the FP64 oracle: the BF16-rounded intermediate, and end to end
-    ref_mid = oracle.conv2d(x, wd, None, 1, 1, 1, sd.G, False)
-    pts = sample_points(sp, 4096, 8)
-    check_points(sp, y, oracle.round_bf16(ref_mid), wp, bp, pts)
-    check_points(sp, y, ref_mid, wp, bp, pts)
+    # every output against the FP64 oracle: the BF16-rounded intermediate, and end to end
+    ref = oracle.dwpw_block(x, wd, wp, 1, pw_bias=bp, pw_relu=True, round_mid=True)
+    check_full(sp, y, ref)
+    ref64 = oracle.dwpw_block(x, wd, wp, 1, pw_bias=bp, pw_relu=True, round_mid=False)
+    check_full(sp, y, ref64)
 
 
 def test_block_rejects_bad_tensors():

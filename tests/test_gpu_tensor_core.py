@@ -119,31 +119,88 @@ def test_body_full_size_one_sm_kernel():
 
 
 def test_body_full_size():
-    """N=32, 128->256, 112x112, 3x3 s1 p1, bias+ReLU: the first and last images in full,
-    plus 65,536 seeded points over the whole batch (every corner included)."""
+    """N=32, 128->256, 112x112, 3x3 s1 p1, bias+ReLU (halo mode on SM pairs): every output
+    of the batch against the FP64 oracle, in chunks of images to bound host memory."""
     s, x, w, b = inputs("body")
     plan, y = run(s, x, w, b)
-    assert plan.path == "implicit_gemm"
-    check_points(s, y, x, w, b, sample_points(s, 65536, 3))
-    for n in (0, s.N - 1):
-        ref = oracle.conv2d(x[n:n + 1], w, b, 1, 1, 1, 1, True)
-        check_full(s, y[n:n + 1], ref)
+    assert plan.path == "implicit_gemm" and plan.launch["block"] == 608 and plan.launch["cluster"] == 2
+    for n0 in range(0, s.N, 8):
+        ref = oracle.conv2d(x[n0:n0 + 8], w, b, 1, 1, 1, 1, True)
+        check_full(s, y[n0:n0 + 8], ref)
 
 
 def test_pointwise_full_size():
+    """N64, 256 -> 512, 56x56 1x1 + bias + ReLU: every output of the batch against the
+    FP64 oracle ("Convolution variants", section 6.4: compare every element)."""
     s, x, w, b = inputs("pw")
     plan, y = run(s, x, w, b)
     assert plan.path == "gemm_1x1"
-    check_points(s, y, x, w, b, sample_points(s, 8192, 4))
-    check_full(s, y[:1], oracle.conv2d(x[:1], w, b, 1, 0, 1, 1, True))
+    check_full(s, y, oracle_full(s, x, w, b))
 
 
 def test_dilated_grouped_full_size():
+    """N16, 256 -> 256, 64x64, 3x3 d2 p2 g4 + bias + ReLU (halo mode, two tiles per CTA):
+    every output of the batch against the FP64 oracle."""
     s, x, w, b = inputs("dilated")
     plan, y = run(s, x, w, b)
-    assert plan.path == "implicit_gemm"
-    check_points(s, y, x, w, b, sample_points(s, 8192, 5))
-    check_full(s, y[:1], oracle.conv2d(x[:1], w, b, 1, 2, 2, 4, True))
+    assert plan.path == "implicit_gemm" and plan.launch["block"] == 608
+    check_full(s, y, oracle_full(s, x, w, b))
+
+
+# stride-1 implicit-GEMM shapes of the small-shape list, run with one TMA box per tap
+# (CONV_FLAG_PER_TAP) instead of the default halo tiles
+PER_TAP_SHAPES = [
+    ConvShape(2, 64, 13, 11, 32, 3, 3, 1, 1, 1, 1, "bf16", True, True),
+    ConvShape(2, 64, 12, 12, 64, 5, 5, 1, 2, 1, 1, "bf16", False, True),
+    ConvShape(2, 64, 15, 13, 64, 3, 3, 1, 3, 3, 1, "bf16", True, True),
+    ConvShape(2, 64, 10, 14, 64, 1, 3, 1, 1, 1, 1, "bf16", True, False),
+    ConvShape(2, 128, 9, 9, 64, 3, 3, 1, 1, 1, 2, "bf16", True, True),
+    ConvShape(1, 256, 8, 8, 256, 3, 3, 1, 2, 2, 4, "bf16", True, True),
+    ConvShape(2, 128, 20, 27, 256, 3, 3, 1, 1, 1, 1, "bf16", True, True),
+]
+
+
+@pytest.mark.parametrize("shape", PER_TAP_SHAPES, ids=lambda s: "K%dx%dD%dG%d_%dx%d" % (s.Kh, s.Kw, s.D, s.G, s.H, s.W))
+@pytest.mark.parametrize("sm_pairs", [False, True], ids=["single_sm", "sm_pairs"])
+def test_per_tap_mode_full(shape, sm_pairs):
+    """Every output with one input box per tap (the per-tap mode): same results as the
+    halo mode up to the order of the FP32 sum, both against the oracle."""
+    from cnn_convolution_implicit_gb300 import ConvPlan
+    x, w, b = draw(shape, (61, 62, 63))
+    ref = oracle_full(shape, x, w, b)
+    plan, y = run(shape, x, w, b, plan=ConvPlan.for_shape(shape, sm_pairs=sm_pairs, per_tap=True))
+    assert plan.path == "implicit_gemm" and plan.launch["block"] == 576
+    check_full(shape, y, ref)
+    plan_h, y_h = run(shape, x, w, b, plan=ConvPlan.for_shape(shape, sm_pairs=sm_pairs))
+    assert plan_h.launch["block"] == 608
+    check_full(shape, y_h, ref)
+
+
+def test_halo_mode_random_sweep():
+    """Random stride-1 BF16 shapes in the halo mode (kernel sizes 1-5 per axis, dilation
+    1-3, padding, groups, ragged 8 x 16 tiles, widths that leave a lone right-hand tile of
+    a two-tile unit): every output against the oracle."""
+    from cnn_convolution_implicit_gb300 import ConvPlan
+    rng = np.random.default_rng(29)
+    done = 0
+    while done < 16:
+        G = int(rng.choice([1, 1, 2, 4]))
+        cin_g = 64 * int(rng.integers(1, 3))
+        cout_g = int(rng.choice([32, 64, 96, 128, 256]))
+        Kh, Kw = int(rng.integers(1, 6)), int(rng.integers(1, 6))
+        D = int(rng.integers(1, 4))
+        s = ConvShape(int(rng.integers(1, 3)), cin_g * G, int(rng.integers(3, 30)), int(rng.integers(3, 40)),
+                      cout_g * G, Kh, Kw, 1, int(rng.integers(0, 4)), D, G, "bf16",
+                      bool(rng.integers(0, 2)), bool(rng.integers(0, 2)))
+        if s.H_out < 1 or s.W_out < 1 or Kh * Kw == 1:
+            continue
+        plan = ConvPlan.for_shape(s)
+        if plan.path != "implicit_gemm" or plan.launch["block"] != 608:
+            continue
+        x, w, b = draw(s, (900 + done, 910 + done, 920 + done))
+        _, y = run(s, x, w, b, plan=plan)
+        check_full(s, y, oracle_full(s, x, w, b))
+        done += 1
 
 
 def test_depthwise_separable_block():
