@@ -269,7 +269,7 @@ def measure_layer(name, steps, warmup, flush, peaks, affine=False, winograd=Fals
         plan.forward(xd, wd, bd, y, scale=scale)
 
     ms = time_steps(step, steps, warmup, flush)
-    t = float(np.mean(ms)) * 1e-3
+    t = float(np.median(ms)) * 1e-3   # the median step: one slow step (a preempted box) does not move it
     tflops = s.flops / t / 1e12
     gbs = s.algorithmic_bytes / t / 1e9
     if s.dtype == "f32" and s.G == 1:
@@ -280,6 +280,7 @@ def measure_layer(name, steps, warmup, flush, peaks, affine=False, winograd=Fals
     res = {"workload": name + ("+affine" if affine else "") + ("+winograd" if winograd else ""),
            "kernel": plan.path, "ms": t * 1e3, "tflops": tflops, "gbs": gbs,
            "bound": bound, "flops": s.flops, "bytes": s.algorithmic_bytes, "launches": steps,
+           "ms_mean": float(np.mean(ms)),
            "source_hash": kernel_source_hash("winograd" if plan.path == "winograd" else name), "launch": plan.launch}
     if bound == "tensor":
         res["frac"] = tflops / peaks["bf16_tflops"]
@@ -305,7 +306,7 @@ def measure_block(steps, warmup, flush, peaks):
     bd = b_device(bp)
     y = plan.empty_output()
     ms = time_steps(lambda: plan.forward(xd, wdd, wpd, pw_bias=bd, y=y), steps, warmup, flush)
-    t = float(np.mean(ms)) * 1e-3
+    t = float(np.median(ms)) * 1e-3
     # algorithmic bytes: FP32 input and BF16 output once, weights and bias once
     nbytes = x.size * 4 + sp.pixels * sp.C_out * 2 + wd.size * 4 + wp.size * 2 + bp.size * 4
     flops = sd.flops + sp.flops
@@ -325,7 +326,7 @@ def measure_block(steps, warmup, flush, peaks):
         pw_plan.forward(mid, wpd4, bd, y2)
 
     ms2 = time_steps(two, steps, warmup, flush)
-    t2 = float(np.mean(ms2)) * 1e-3
+    t2 = float(np.median(ms2)) * 1e-3
     two_res = {"workload": "block (two launches: dw -> bf16 -> pw)", "kernel": "depthwise + gemm_1x1",
                "ms": t2 * 1e3, "gbs": nbytes / t2 / 1e9, "frac": nbytes / t2 / 1e9 / peaks["hbm_gbs"],
                "launches": 2 * steps}
@@ -386,7 +387,7 @@ def measure_e2e(s, xd, wd, bd, y, chunks, steps, flush, dist, world):
         main.wait_stream(s_out)
         torch.cuda.synchronize()
         ms.append(a.elapsed_time(e))
-    t = max_over_ranks(float(np.mean(ms)) * 1e-3, dist, "cuda")
+    t = max_over_ranks(float(np.median(ms)) * 1e-3, dist, "cuda")
     if not torch.equal(y_h, y.cpu()):  # the chunked result must be the full-batch result, bit for bit
         sys.stderr.write("e2e: downloaded output differs from the device-resident run\n")
     return {"value": whole_job_rate(s.flops, world, t) / 1e12, "unit": "TFLOP/s",
@@ -528,7 +529,7 @@ def main():
             tf, cores, sample = sampler.step(per_step_s)
             vals.append(tf)
             samples.append(sample)
-        v = float(np.mean(vals))
+        v = float(np.median(vals))
         line = {"impl": "reference", "metric": METRIC, "value": v,
                 "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "higher_is_better": True, "dtype": "f64", "data": "synthetic (seeded)",
@@ -558,9 +559,11 @@ def main():
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    t_step_local = float(np.mean(ms)) * 1e-3
-    t_total = max_over_ranks(float(np.sum(ms)) * 1e-3, dist, "cuda")
-    t_step = t_total / args.steps
+    # per-step statistic: the median of the K CUDA-event-timed steps (the mean is reported
+    # beside it); the job's step time is the slowest rank's
+    t_step_local = float(np.median(ms)) * 1e-3
+    t_step = max_over_ranks(t_step_local, dist, "cuda")
+    t_mean = max_over_ranks(float(np.mean(ms)) * 1e-3, dist, "cuda")
     value = whole_job_rate(s.flops, world, t_step) / 1e12
     kern_tflops = s.flops / t_step_local / 1e12
 
@@ -593,7 +596,7 @@ def main():
                 "frac": kern_tflops / peaks["bf16_tflops"],
                 "peak_source": "%s bf16_tflops (burst, kernel timed alone)" % peaks["source"],
                 "traffic": (tr[0] if tr and tr[1] == kernel_source_hash("body") else None),
-                "kernel": "tc_conv_kernel (implicit GEMM, TMA im2col, tcgen05)",
+                "kernel": "tc_conv_kernel (implicit GEMM, halo tiles on SM pairs, tcgen05)",
                 "algorithmic_flops_per_launch": s.flops}
     # clock-derived tensor peak: this GPU's own tcgen05 rate per SM per clock x SMs x the
     # SM clock sampled during the timed loop (a second denominator beside the cuBLAS one)
@@ -602,6 +605,7 @@ def main():
     clk_mhz = clk.get("sm_mhz") or clk.get("sm_max_mhz")
     if clk_mhz:
         theo = fpc * sms * clk_mhz * 1e6 / 1e12
+        roofline["frac_chip_peak"] = kern_tflops / theo
         roofline["theoretical"] = {"peak": theo, "unit": "TFLOP/s", "frac": kern_tflops / theo,
                                    "flop_per_clk_sm": fpc, "sms": sms, "sm_mhz": clk_mhz,
                                    "how": "tcgen05.mma M128 N256 K16 chain per SM (conv_measure_mma_rate) "
@@ -626,7 +630,8 @@ def main():
     if rank == 0:
         line = {"metric": METRIC,
                 "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
+                "ms_per_step": t_step * 1e3, "ms_per_step_mean": t_mean * 1e3, "step_statistic": "median",
+                "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs, Kaiming weights)",
                 "config": config, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": args.steps, "clocks": clk,

@@ -174,6 +174,12 @@ conv_status conv_block_forward(conv_block_plan* p, const void* x, const void* w_
     for (const void* ptr : {x, w_dw, dw_scale, dw_bias, w_pw, pw_scale, pw_bias, static_cast<const void*>(y)})
         if (ptr != nullptr && !aligned16(ptr)) return CONV_ERR_MISALIGNED;
     if (p->device < 0) return CONV_ERR_CUDA;  // host-only plan
+    int cur = -1;  // the plan belongs to the device current at its creation
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return CONV_ERR_CUDA;
+    }
+    if (cur != p->device) return CONV_ERR_INVALID_ARG;
     const conv_status s = encode_block_maps(p, x, w_pw, y);
     if (s != CONV_OK) return s;
     BlockParams b = p->bp;

@@ -754,6 +754,14 @@ conv_status forward_impl(conv_plan* p, const void* x, const void* w, const float
                          void* stream) {
     if (p == nullptr || x == nullptr || w == nullptr || y == nullptr) return CONV_ERR_INVALID_ARG;
     if (p->device < 0) return CONV_ERR_CUDA;  // host-only plan: no device to run on
+    // the plan's SM count, cluster occupancy, shared-memory limits and status word belong
+    // to the device current at creation: another current device is a caller error
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return CONV_ERR_CUDA;
+    }
+    if (cur != p->device) return CONV_ERR_INVALID_ARG;
     const bool has_bias = (p->flags & CONV_FLAG_BIAS) != 0;
     if (has_bias && bias == nullptr) return CONV_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (has_bias && !aligned16(bias)))

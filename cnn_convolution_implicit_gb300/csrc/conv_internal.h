@@ -2,6 +2,7 @@
 // code (conv_api.cu) and the kernel translation units.  Not part of the ABI.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -9,18 +10,28 @@
 
 namespace convgb {
 
+// Per-device dynamic shared-memory limit already set on one kernel (zero-initialised
+// when declared static; atomic, so plans driven from different host threads may
+// launch the same kernel concurrently).
+using SmemLimitCache = std::atomic<int>[64];
+
 // Raise a kernel's dynamic shared-memory limit only when a launch needs more
 // than what was set before on this device (`limits` is the caller's per-kernel
-// table).  The limit is a per-function attribute, so a plan's later launches
-// cost no extra runtime call.  Concurrent first calls may both set it: harmless.
-inline cudaError_t ensure_smem_limit(const void* func, int bytes, int (&limits)[64]) {
+// cache).  The limit is a per-function attribute, so a plan's later launches
+// cost no extra runtime call.  Concurrent first calls may both set it: harmless,
+// and the cache only ever grows.
+inline cudaError_t ensure_smem_limit(const void* func, int bytes, SmemLimitCache& limits) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
         return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     }
-    if (limits[dev] >= bytes) return cudaSuccess;
+    if (limits[dev].load(std::memory_order_relaxed) >= bytes) return cudaSuccess;
     const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess) limits[dev] = bytes;
+    if (e == cudaSuccess) {
+        int cur = limits[dev].load(std::memory_order_relaxed);
+        while (cur < bytes && !limits[dev].compare_exchange_weak(cur, bytes, std::memory_order_relaxed)) {
+        }
+    }
     return e;
 }
 

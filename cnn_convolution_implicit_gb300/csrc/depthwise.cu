@@ -341,7 +341,7 @@ int depthwise_config(const ConvGeom& g, int smem_per_sm, int num_sms, DepthwiseP
 
 template <int K, int TW>
 static cudaError_t launch_dw(const CUtensorMap& x_map, const DepthwiseParams& p, cudaStream_t stream) {
-    static int limits[64] = {};
+    static SmemLimitCache limits;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(depthwise_kernel<K, TW>), p.smem_bytes, limits);
     if (e != cudaSuccess) return e;
     depthwise_kernel<K, TW><<<p.grid, kDwThreads, p.smem_bytes, stream>>>(x_map, p);

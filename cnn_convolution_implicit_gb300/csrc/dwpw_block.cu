@@ -510,7 +510,7 @@ int dwpw_block_smem_bytes(int C, int C_out, int slice_n, int halo_stages, int b_
 
 cudaError_t launch_dwpw_block(const CUtensorMap& x_map, const CUtensorMap& w_map, const CUtensorMap& y_map,
                               const BlockParams& p, int grid, cudaStream_t stream) {
-    static int limits[64] = {};
+    static SmemLimitCache limits;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(dwpw_block_kernel), p.smem_bytes, limits);
     if (e != cudaSuccess) return e;
     dwpw_block_kernel<<<grid, kBkThreads, p.smem_bytes, stream>>>(x_map, w_map, y_map, p);

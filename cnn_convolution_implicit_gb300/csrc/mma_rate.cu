@@ -73,7 +73,7 @@ extern "C" conv_status conv_measure_mma_rate(int iters, unsigned long long* cycl
     if (iters <= 0 || iters > kRateMaxIters || cycles == nullptr || grid <= 0) return CONV_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(cycles) % 8u != 0) return CONV_ERR_MISALIGNED;
     unsigned* status = nullptr;
-    static int limits[64] = {};
+    static SmemLimitCache limits;
     if (device_status_word(&status) != cudaSuccess ||
         ensure_smem_limit(reinterpret_cast<const void*>(mma_rate_kernel), kRateSmem, limits) != cudaSuccess) {
         cudaGetLastError();

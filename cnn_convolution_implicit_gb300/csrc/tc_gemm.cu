@@ -800,7 +800,7 @@ __global__ void __launch_bounds__(HALO ? kTcHaloThreads : kTcThreads, 1)
 }
 
 // per-device dynamic shared-memory limit already set on the pair kernel
-static int g_pair_smem_limits[64] = {};
+static SmemLimitCache g_pair_smem_limits;
 
 namespace {
 
@@ -808,7 +808,7 @@ namespace {
 template <bool PAIR, bool PHASE, bool DUAL, bool HALO>
 cudaError_t launch_one(const CUtensorMap& a_map, const CUtensorMap& b_map, const CUtensorMap& y_map,
                        const TcGemmParams& p, int grid, cudaStream_t stream) {
-    static int limits[64] = {};
+    static SmemLimitCache limits;
     auto* fn = tc_conv_kernel<PAIR, PHASE, DUAL, HALO>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fn), p.smem_bytes, limits);
     if (e != cudaSuccess) return e;
@@ -839,7 +839,7 @@ cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, c
         return launch_one<false, false, false, true>(a_map, b_map, y_map, p, grid, stream);
     }
     if (p.pair) {
-        static int pair_phase_limits[64] = {};
+        static SmemLimitCache pair_phase_limits;
         cudaError_t e = p.mode == kTcModePhase
                             ? ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<true, true, false>), p.smem_bytes,
                                                 pair_phase_limits)
@@ -864,7 +864,7 @@ cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, c
         return cudaGetLastError();
     }
     if (p.dual) {  // two pixel tiles per CTA
-        static int dual_limits[64] = {}, dual_phase_limits[64] = {};
+        static SmemLimitCache dual_limits, dual_phase_limits;
         const bool ph = p.mode == kTcModePhase;
         const void* fn = ph ? reinterpret_cast<const void*>(tc_conv_kernel<false, true, true>)
                             : reinterpret_cast<const void*>(tc_conv_kernel<false, false, true>);
@@ -877,14 +877,14 @@ cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, c
         return cudaGetLastError();
     }
     if (p.mode == kTcModePhase) {
-        static int phase_limits[64] = {};
+        static SmemLimitCache phase_limits;
         cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<false, true, false>), p.smem_bytes,
                                           phase_limits);
         if (e != cudaSuccess) return e;
         tc_conv_kernel<false, true, false><<<grid, kTcThreads, p.smem_bytes, stream>>>(a_map, b_map, y_map, p);
         return cudaGetLastError();
     }
-    static int limits[64] = {};
+    static SmemLimitCache limits;
     cudaError_t e =
         ensure_smem_limit(reinterpret_cast<const void*>(tc_conv_kernel<false, false, false>), p.smem_bytes, limits);
     if (e != cudaSuccess) return e;
@@ -893,7 +893,7 @@ cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, c
 }
 
 int tc_gemm_pair_max_clusters(const TcGemmParams& p) {
-    static int halo_pair_limits[64] = {};
+    static SmemLimitCache halo_pair_limits;
     const void* fn = p.halo ? reinterpret_cast<const void*>(tc_conv_kernel<true, false, false, true>)
                             : reinterpret_cast<const void*>(tc_conv_kernel<true, false, false>);
     if (ensure_smem_limit(fn, p.smem_bytes, p.halo ? halo_pair_limits : g_pair_smem_limits) != cudaSuccess) {

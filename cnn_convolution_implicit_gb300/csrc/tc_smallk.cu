@@ -613,7 +613,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 
 template <int CIN, int KH, int KW>
 static cudaError_t launch_sk(const SmallKParams& p, int grid, cudaStream_t stream) {
-    static int limits[64] = {};
+    static SmemLimitCache limits;
     cudaError_t e =
         ensure_smem_limit(reinterpret_cast<const void*>(tc_smallk_kernel<CIN, KH, KW>), p.smem_bytes, limits);
     if (e != cudaSuccess) return e;

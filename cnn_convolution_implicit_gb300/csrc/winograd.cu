@@ -272,7 +272,7 @@ cudaError_t launch_winograd(const WinogradParams& p, cudaStream_t stream) {
     unsigned gx, gy;
     winograd_grid(p.g, gx, gy);
     const int smem = winograd_smem_bytes();
-    static int limits_f32[64] = {}, limits_bf16[64] = {};
+    static SmemLimitCache limits_f32, limits_bf16;
     cudaError_t e;
     if (p.out_bf16) {
         e = ensure_smem_limit(reinterpret_cast<const void*>(winograd_kernel<__nv_bfloat16>), smem, limits_bf16);

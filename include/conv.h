@@ -132,7 +132,8 @@ typedef enum {
  * CONV_ERR_INVALID_ARG for a bad shape or out == NULL, CONV_ERR_NO_MEMORY if
  * the host allocation fails, CONV_ERR_CUDA if the current device cannot be
  * queried.  On error *out is set to NULL.  The plan is tied to the CUDA device
- * current at creation.
+ * current at creation: conv_forward / conv_forward_affine with another device
+ * current return CONV_ERR_INVALID_ARG without launching.
  */
 conv_status conv_plan_create(conv_plan **out, int N, int C_in, int H, int W, int C_out,
                              int Kh, int Kw, int S, int P, int D, int G,
@@ -255,7 +256,9 @@ typedef struct conv_block_plan conv_block_plan; /* opaque, host-owned */
 
 /*
  * Check the block's shape and choose its launch configuration.  *plan gets a
- * new plan, or NULL on error.  Returns CONV_ERR_INVALID_ARG for non-positive
+ * new plan, or NULL on error.  Like a convolution plan, it is tied to the
+ * device current at creation (its forward returns CONV_ERR_INVALID_ARG with
+ * another device current).  Returns CONV_ERR_INVALID_ARG for non-positive
  * sizes, an empty output or unknown flags, CONV_ERR_UNSUPPORTED for a valid
  * block outside the supported family above, CONV_ERR_CUDA if the device
  * cannot be queried.  Without a device a host-only plan is made (shape checks
