@@ -5,7 +5,7 @@ direct fallback kernel, behind the C ABI of include/conv.h.
     from cnn_convolution_implicit_gb300 import ConvPlan, conv2d
 """
 from .binding import (CONV_BF16, CONV_F32, EXPORTS, PATHS, BlockPlan, ConvError, ConvPlan,
-                      conv2d, device_status, lib, measure_mma_rate)
+                      check_wait_timeout, conv2d, device_status, lib, measure_mma_rate)
 
-__all__ = ["ConvPlan", "BlockPlan", "conv2d", "ConvError", "device_status", "lib", "measure_mma_rate", "PATHS",
-           "EXPORTS", "CONV_BF16", "CONV_F32"]
+__all__ = ["ConvPlan", "BlockPlan", "conv2d", "ConvError", "device_status", "lib", "measure_mma_rate",
+           "check_wait_timeout", "PATHS", "EXPORTS", "CONV_BF16", "CONV_F32"]

@@ -26,7 +26,7 @@ EXPORTS = ("conv_plan_create", "conv_plan_output_shape", "conv_plan_info", "conv
            "conv_plan_destroy", "conv_status_string", "conv_device_status", "conv_plan_num_sms",
            "conv_plan_launch_info", "conv_forward_affine", "conv_block_plan_create",
            "conv_block_plan_output_shape", "conv_block_forward", "conv_block_plan_launch_info",
-           "conv_block_plan_destroy", "conv_measure_mma_rate")
+           "conv_block_plan_destroy", "conv_measure_mma_rate", "conv_check_wait_timeout")
 CONV_BLOCK_DW_RELU, CONV_BLOCK_PW_RELU = 1, 2
 
 _lock = threading.Lock()
@@ -89,6 +89,8 @@ def lib():
             L.conv_block_plan_destroy.restype = c_int
             L.conv_measure_mma_rate.argtypes = [c_int, vp, c_int, vp]
             L.conv_measure_mma_rate.restype = c_int
+            L.conv_check_wait_timeout.argtypes = [ctypes.c_ulonglong, vp, vp]
+            L.conv_check_wait_timeout.restype = c_int
             _lib = L
         return _lib
 
@@ -318,6 +320,24 @@ def measure_mma_rate(iters: int = 1 << 16, device=None):
     c = cycles.cpu().numpy().astype(np.float64)
     per_sm = 2.0 * 128 * 256 * 16 * iters / c
     return float(np.median(per_sm)), per_sm, sms
+
+
+def check_wait_timeout(limit_ns: int, device=None):
+    """Run conv_check_wait_timeout: one role's bounded wait on a barrier nothing completes
+    gives up after ``limit_ns``, a second role leaves through the abort flag.  Returns
+    (the status word conv_device_status read and cleared, the second role's wait in ns)."""
+    import torch
+    L = lib()
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    elapsed = torch.zeros(1, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    st = L.conv_check_wait_timeout(int(limit_ns), ctypes.c_void_p(elapsed.data_ptr()),
+                                   ctypes.c_void_p(stream.cuda_stream))
+    if st != 0:
+        raise ConvError(st, "conv_check_wait_timeout")
+    torch.cuda.synchronize(dev)
+    code = device_status()
+    return code, int(elapsed.item())
 
 
 def conv2d(x, w, bias=None, stride=1, padding=0, dilation=1, groups=1, relu=False, out_bf16=False,

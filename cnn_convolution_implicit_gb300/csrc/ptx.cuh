@@ -72,9 +72,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
-// Wait for the phase of parity `parity` to complete.  Returns false on timeout
-// or when *abort is raised; the caller then records the error and leaves.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// Wait for the phase of parity `parity` to complete.  Returns false after
+// `limit_ns` of %globaltimer time or when *abort is raised; the caller then
+// records the error and leaves.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          unsigned long long limit_ns = kWaitTimeoutNs) {
     const uint32_t a = smem_addr(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
@@ -82,7 +84,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
         if (mbar_try_wait(a, parity)) return true;
         if ((i & 255u) == 0) {
             if (abort != nullptr && *abort) return false;
-            if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
         }
     }
 }

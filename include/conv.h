@@ -212,6 +212,24 @@ int conv_plan_num_sms(const conv_plan *p);
 conv_status conv_measure_mma_rate(int iters, unsigned long long *cycles, int grid, void *stream);
 
 /*
+ * Test aid, not a convolution: makes the kernels' bounded-wait failure path run.
+ * Every mbarrier wait in this library's kernels gives up after a time limit
+ * (2 s), sets a bit in the device status word, raises its CTA's abort flag so
+ * the CTA's other roles leave their waits, frees tensor memory and returns (the
+ * pipeline-hang detection of the failure-handling design; no trap, no fault).
+ * This launches one CTA on `stream` in which one role waits on an mbarrier that
+ * nothing completes, with a limit of `limit_ns` (1 .. 2e9 ns), and a second role
+ * waits on another such barrier with the kernels' own 2 s limit.  The first gives
+ * up after limit_ns and sets bit 2; the second leaves through the abort flag and
+ * sets bit 4.  conv_device_status afterwards returns CONV_ERR_TIMEOUT with code
+ * 6 and clears the word; the context stays usable.  If `elapsed_ns` is non-NULL
+ * (device memory, 8-byte aligned) it receives how long the second role waited
+ * (%globaltimer ns): at least limit_ns, far below 2 s.  Returns CONV_ERR_INVALID_ARG / CONV_ERR_MISALIGNED without launching,
+ * CONV_ERR_CUDA if the launch fails.  Asynchronous.
+ */
+conv_status conv_check_wait_timeout(unsigned long long limit_ns, unsigned long long *elapsed_ns, void *stream);
+
+/*
  * Launch configuration conv_forward uses for this plan: grid and block size
  * (CTAs, threads), dynamic shared memory per CTA in bytes, pipeline stages,
  * and CTAs per cluster (2 for SM pairs, else 1).  Any output pointer may be

@@ -278,3 +278,15 @@ def test_halo_mode_choice(shape, halo):
     assert p.launch["smem_bytes"] <= 232448 and p.launch["stages"] >= 2
     q = cg.ConvPlan(*shape, dtype="bf16", bias=True, relu=True, per_tap=True)
     assert q.path == p.path and q.launch["block"] == 576
+
+
+def test_wait_timeout_check_rejects_bad_arguments_without_launching():
+    """conv_check_wait_timeout validates its limit and pointer before any CUDA call; with
+    no device a valid call fails loudly (CONV_ERR_CUDA), it never runs on the host."""
+    L = cg.lib()
+    assert L.conv_check_wait_timeout(0, None, None) == 1                 # limit 0
+    assert L.conv_check_wait_timeout(2_000_000_001, None, None) == 1     # above the kernels' own 2 s
+    assert L.conv_check_wait_timeout(1_000_000, ctypes.c_void_p(12), None) == 3  # misaligned
+    import torch
+    if not torch.cuda.is_available():
+        assert L.conv_check_wait_timeout(1_000_000, None, None) == 4
