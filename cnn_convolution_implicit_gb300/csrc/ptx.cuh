@@ -72,11 +72,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
-// Wait for the phase of parity `parity` to complete.  Returns false after
-// `limit_ns` of %globaltimer time or when *abort is raised; the caller then
-// records the error and leaves.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          unsigned long long limit_ns = kWaitTimeoutNs) {
+// Wait for the phase of parity `parity` to complete.  Returns false on timeout
+// or when *abort is raised; the caller then records the error and leaves.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    const uint32_t a = smem_addr(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(a, parity)) return true;
+        if ((i & 255u) == 0) {
+            if (abort != nullptr && *abort) return false;
+            if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+        }
+    }
+}
+
+// mbar_wait with the time limit as an argument (the failure-path test gives it a
+// short one; the kernels keep the fixed 2 s of mbar_wait).
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                unsigned long long limit_ns) {
     const uint32_t a = smem_addr(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer_ns();

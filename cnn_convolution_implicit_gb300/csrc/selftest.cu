@@ -1,7 +1,8 @@
 // selftest.cu -- makes the kernels' bounded-wait failure path run, on purpose,
 // without a fault: a test aid behind conv_check_wait_timeout (include/conv.h).
 //
-// Every mbarrier wait in the convolution kernels gives up after a time limit,
+// Every mbarrier wait in the convolution kernels gives up after a time limit
+// (mbar_wait: 2 s; mbar_wait_limit is the same loop with the limit as argument),
 // latches a bit in the device status word, raises the CTA's abort flag so the
 // other roles leave their loops, frees tensor memory and returns.  A working
 // pipeline never takes that path, so this kernel builds the situation with the
@@ -39,7 +40,7 @@ __global__ void __launch_bounds__(128, 1)
     tc_fence_after();
     if (warp == 1 && lane == 0) {
         // a consumer whose data never lands: the short limit runs out
-        if (!mbar_wait(&never[0], 0, abort, limit_ns)) record_status(status, kStatusTimeoutMma, abort);
+        if (!mbar_wait_limit(&never[0], 0, abort, limit_ns)) record_status(status, kStatusTimeoutMma, abort);
     } else if (warp == 2 && lane == 0) {
         // another role blocked on its own barrier with the kernels' 2 s limit: it sees
         // the abort flag and leaves long before that; it times its own wait
