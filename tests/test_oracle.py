@@ -563,11 +563,24 @@ def test_winograd_equals_direct_convolution_in_fp64(N, C, H, W, Co, P):
     assert np.max(np.abs(y - r)) <= 1e-12 * (1 + np.max(np.abs(r)))
 
 
-def test_winograd_multiply_count_and_precision_cost():
-    """4 multiplies per output instead of 9 (16 per 2x2 tile): the pages' 2.25x.  In FP32 its
-    error on Kaiming-scale data is of the same order as direct FP32 sums (whose own error moves
-    with the summation order) and within the FP32 tolerance of the library's FP32 paths: for
-    this smallest tile the pages' precision caveat is mild."""
+def _direct_fp32_in_order(x, w):
+    """3x3 stride-1 pad-1 convolution summed in FP32 in one fixed order (channel, kernel
+    row, kernel column), each product added to the running output: a plain loop's rounding."""
+    N, C, H, W = x.shape
+    xp = np.pad(x.astype(np.float32), ((0, 0), (0, 0), (1, 1), (1, 1)))
+    w32 = w.astype(np.float32)
+    y = np.zeros((N, w.shape[0], H, W), np.float32)
+    for c in range(C):
+        for i in range(3):
+            for j in range(3):
+                y += xp[:, c:c + 1, i:i + H, j:j + W] * w32[None, :, c, i, j, None, None]
+    return y.astype(np.float64)
+
+
+def test_winograd_multiply_count_and_fp32_tolerance():
+    """4 multiplies per output instead of 9 (16 per 2x2 tile): the pages' 2.25x.  On
+    Kaiming-scale multi-channel data its FP32 result stays within the FP32 tolerance the
+    library's FP32 paths are held to."""
     assert oracle.WINO_BT.shape[0] * oracle.WINO_BT.shape[0] / (oracle.WINO_AT.shape[0] ** 2) == 4.0
     assert 9 / (16 / 4) == 2.25
     rng = np.random.default_rng(33)
@@ -575,11 +588,25 @@ def test_winograd_multiply_count_and_precision_cost():
     w = rng.standard_normal((32, 64, 3, 3)) * np.sqrt(2.0 / 576)
     ref = oracle.conv2d(x, w, None, 1, 1)
     wino32 = oracle.winograd_conv2d(x.astype(np.float32), w.astype(np.float32), None, 1, dtype=np.float32)
-    # direct FP32 sums: explicit im2col columns times the weight matrix, in float32
-    xp = np.pad(x.astype(np.float32), ((0, 0), (0, 0), (1, 1), (1, 1)))
-    cols = np.lib.stride_tricks.sliding_window_view(xp, (3, 3), axis=(2, 3))      # N C H W 3 3
-    direct32 = np.einsum("nchwij,ocij->nohw", cols, w.astype(np.float32), optimize=True).astype(np.float64)
+    e_w = np.linalg.norm(wino32 - ref) / np.linalg.norm(ref)
+    assert np.max(np.abs(wino32 - ref) / (1 + np.abs(ref))) <= 1e-5 and e_w <= 1e-5
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_winograd_precision_caveat_single_channel(seed):
+    """The pages' precision caveat of Winograd ("Convolution vs inner product", lnrq.cn,
+    section 2.2; "Convolution variants and their matrix operations", section 3.3), where it
+    shows: with one input channel no channel sum's ordering hides it, and the transforms'
+    own rounding (the input transform adds up to four values, the output transform four
+    products' sums) leaves F(2x2, 3x3) in FP32 with a larger normwise error than the nine
+    products summed in order: measured 1.6-1.8x over seeds; pinned at > 1.3x."""
+    rng = np.random.default_rng(100 + seed)
+    x = rng.standard_normal((4, 1, 32, 32))
+    w = rng.standard_normal((16, 1, 3, 3))
+    ref = oracle.conv2d(x, w, None, 1, 1)
+    wino32 = oracle.winograd_conv2d(x.astype(np.float32), w.astype(np.float32), None, 1, dtype=np.float32)
+    direct32 = _direct_fp32_in_order(x, w)
     e_w = np.linalg.norm(wino32 - ref) / np.linalg.norm(ref)
     e_d = np.linalg.norm(direct32 - ref) / np.linalg.norm(ref)
-    assert e_d / 3 <= e_w <= 3 * e_d
-    assert np.max(np.abs(wino32 - ref) / (1 + np.abs(ref))) <= 1e-5 and e_w <= 1e-5
+    assert e_w > 1.3 * e_d, (e_w, e_d)
+    assert e_w <= 1e-5
