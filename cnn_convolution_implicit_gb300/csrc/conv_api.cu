@@ -676,7 +676,7 @@ conv_status conv_plan_launch_info(const conv_plan* p, int* grid, int* block, int
         case CONV_PATH_GEMM_1X1:
         case CONV_PATH_IMPLICIT_GEMM: {
             const TcGemmParams& t = p->tc;
-            bl = t.halo ? kTcHaloThreads : kTcThreads;
+            bl = tc_threads(t.halo != 0, t.dual != 0);
             sm = t.smem_bytes;
             st = t.stages;
             if (t.pair) {

@@ -110,6 +110,12 @@ constexpr int kTcBlockK = 64;     // BF16 elements per K-step (one 128-byte swiz
 constexpr int kTcThreads = 576;   // producer warp, MMA warp, 4 x 4 epilogue warps
 constexpr int kTcHaloThreads = 608;  // halo mode: + a weight producer warp (the halo producer is warp 0)
 constexpr int kTcBWarp = 18;      // halo mode: the weight (B operand) producer warp
+// Two pixel tiles per CTA: a second MMA-issuing warp (tile 1's MMAs; warp 1 issues tile 0's)
+// after the other warps: warp 18, or 19 in halo mode.
+__host__ __device__ constexpr int tc_mma2_warp(bool halo) { return halo ? 19 : 18; }
+__host__ __device__ constexpr int tc_threads(bool halo, bool dual) {
+    return (halo ? kTcHaloThreads : kTcThreads) + (dual ? 32 : 0);
+}
 constexpr int kTcMaxGroupsPerTile = 8;  // groups packed side by side in one accumulator (<= ring stages)
 
 enum TcMode { kTcMode1x1 = 0, kTcModeIm2col = 1, kTcModeRect = 2, kTcModePhase = 3, kTcModeHalo = 4 };

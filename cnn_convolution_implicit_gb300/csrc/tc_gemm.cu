@@ -345,9 +345,11 @@ __device__ __forceinline__ void halo_producer(const TcGemmParams& p, const CUten
 // MMA issuer (one thread of the leader).  Per block: wait for its halo; per
 // weight stage: wait once, then for each of its taps issue the K = 64 slice as
 // four K = 16 MMAs whose A descriptor starts at the tap's shifted halo row.
+// part: 0 or 1 = only that pixel tile's MMAs (two tiles per CTA, one issuing thread per
+// tile), 2 = every MMA.
 template <bool PAIR, bool DUAL>
 __device__ __forceinline__ void halo_mma(const TcGemmParams& p, const TcSmem& sm, uint32_t tmem_base, int unit0,
-                                         int unit_step, int num_units, volatile int* abort) {
+                                         int unit_step, int num_units, volatile int* abort, int part) {
     const uint32_t idesc = idesc_bf16_f32((PAIR ? 2 : 1) * kTcBlockM, p.mma_n);
     const int T = p.g.Kh * p.g.Kw;
     const int BT = p.btaps;
@@ -397,14 +399,16 @@ __device__ __forceinline__ void halo_mma(const TcGemmParams& p, const TcSmem& sm
                         const uint64_t adesc = sdesc_sw128_rows(a_addr, sbo);
                         const uint64_t bdesc = sdesc_sw128(bbase + static_cast<uint32_t>(i) * b_tap);
                         const uint32_t first = (kb | tap0 | i) != 0 ? 1u : 0u;
+                        if (!DUAL || part != 1) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            if constexpr (PAIR)
-                                mma_bf16_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (first | k) != 0 ? 1u : 0u);
-                            else
-                                mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (first | k) != 0 ? 1u : 0u);
+                            for (int k = 0; k < 4; ++k) {
+                                if constexpr (PAIR)
+                                    mma_bf16_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (first | k) != 0 ? 1u : 0u);
+                                else
+                                    mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (first | k) != 0 ? 1u : 0u);
+                            }
                         }
-                        if constexpr (DUAL) {
+                        if (DUAL && part != 0) {
                             const uint64_t adesc1 = sdesc_sw128_rows(a_addr + 8u * 128u, sbo);
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
@@ -461,7 +465,7 @@ __device__ __forceinline__ void halo_mma(const TcGemmParams& p, const TcSmem& sm
 // HALO: the halo mode (kTcModeHalo, stride 1): one input halo per 64-channel
 // block feeds every tap through shifted descriptors.
 template <bool PAIR, bool PHASE, bool DUAL, bool HALO = false>
-__global__ void __launch_bounds__(HALO ? kTcHaloThreads : kTcThreads, 1)
+__global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
     tc_conv_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
                    const __grid_constant__ CUtensorMap y_map, const TcGemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -482,19 +486,22 @@ __global__ void __launch_bounds__(HALO ? kTcHaloThreads : kTcThreads, 1)
     const int num_units = TWO ? ((p.num_m_tiles + 1) / 2) * p.num_n_tiles : p.num_tiles;
 
     if (threadIdx.x == 0) {
+        // two tiles per CTA: both MMA-issuing threads commit to the barriers that release
+        // a stage, a halo, an accumulator or the final drain
+        constexpr uint32_t mma_threads = DUAL ? 2 : 1;
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], 1);
+            mbar_init(&sm.empty[s], mma_threads);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&sm.tfull[b], 1);
+            mbar_init(&sm.tfull[b], mma_threads);
             mbar_init(&sm.tempty[b], PAIR ? 2 * 8 : 8);  // one arrival per warp of its two epilogue groups (both CTAs)
         }
-        mbar_init(sm.drain, 1);
+        mbar_init(sm.drain, mma_threads);
         if constexpr (HALO) {
             for (int h = 0; h < p.halo_stages; ++h) {
                 mbar_init(&sm.hfull[h], 1);
-                mbar_init(&sm.hempty[h], 1);
+                mbar_init(&sm.hempty[h], mma_threads);
             }
         }
         *sm.abort = 0;
@@ -525,8 +532,9 @@ __global__ void __launch_bounds__(HALO ? kTcHaloThreads : kTcThreads, 1)
             else
                 halo_producer<PAIR, DUAL, 1>(p, &a_map, &b_map, sm, unit0, unit_step, num_units, rank, leader, abort);
         }
-    } else if (HALO && warp == 1) {
-        if (lane == 0 && leader) halo_mma<PAIR, DUAL>(p, sm, tmem_base, unit0, unit_step, num_units, abort);
+    } else if (HALO && (warp == 1 || (DUAL && warp == tc_mma2_warp(true)))) {
+        if (lane == 0 && leader)
+            halo_mma<PAIR, DUAL>(p, sm, tmem_base, unit0, unit_step, num_units, abort, DUAL ? (warp == 1 ? 0 : 1) : 2);
     } else if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -622,8 +630,11 @@ __global__ void __launch_bounds__(HALO ? kTcHaloThreads : kTcThreads, 1)
                 if (!done) record_status(p.status, kStatusTimeoutDrain, abort);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || (DUAL && warp == tc_mma2_warp(false))) {
         // ------------------------------------------------------------ MMA issuer (leader only)
+        // Two tiles per CTA: warp 1 issues tile 0's MMAs and a second warp tile 1's, each
+        // waiting for the same stages (one thread issues at most one MMA per ~55 clocks)
+        const int part = DUAL ? (warp == 1 ? 0 : 1) : 2;
         if (lane == 0 && leader) {
             const uint32_t idesc = idesc_bf16_f32((PAIR ? 2 : 1) * kTcBlockM, p.mma_n);
             int stage = 0;
@@ -657,15 +668,17 @@ __global__ void __launch_bounds__(HALO ? kTcHaloThreads : kTcThreads, 1)
                         tc_fence_after();
                         const uint64_t adesc = sdesc_sw128(smem_addr(sm.a + stage * a_stage));
                         const uint64_t bdesc = sdesc_sw128(smem_addr(sm.b + stage * b_bytes));
+                        if (!DUAL || part != 1) {
 #pragma unroll
-                        for (int k = 0; k < kTcBlockK / 16; ++k) {
-                            // +32 bytes along K inside the swizzle row = +2 in the >>4 address field
-                            if constexpr (PAIR)
-                                mma_bf16_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
-                            else
-                                mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
+                            for (int k = 0; k < kTcBlockK / 16; ++k) {
+                                // +32 bytes along K inside the swizzle row = +2 in the >>4 address field
+                                if constexpr (PAIR)
+                                    mma_bf16_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
+                                else
+                                    mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (ks | k) != 0 ? 1u : 0u);
+                            }
                         }
-                        if constexpr (DUAL) {  // the unit's second tile: A at +16 KB, its own accumulator
+                        if (DUAL && part != 0) {  // the unit's second tile: A at +16 KB, its own accumulator
                             const uint64_t adesc1 = sdesc_sw128(smem_addr(sm.a + stage * a_stage + kABytes));
 #pragma unroll
                             for (int k = 0; k < kTcBlockK / 16; ++k)
@@ -814,7 +827,7 @@ cudaError_t launch_one(const CUtensorMap& a_map, const CUtensorMap& b_map, const
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(HALO ? kTcHaloThreads : kTcThreads, 1, 1);
+    cfg.blockDim = dim3(tc_threads(HALO, DUAL), 1, 1);
     cfg.dynamicSmemBytes = p.smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -871,9 +884,9 @@ cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, c
         cudaError_t e = ensure_smem_limit(fn, p.smem_bytes, ph ? dual_phase_limits : dual_limits);
         if (e != cudaSuccess) return e;
         if (ph)
-            tc_conv_kernel<false, true, true><<<grid, kTcThreads, p.smem_bytes, stream>>>(a_map, b_map, y_map, p);
+            tc_conv_kernel<false, true, true><<<grid, tc_threads(false, true), p.smem_bytes, stream>>>(a_map, b_map, y_map, p);
         else
-            tc_conv_kernel<false, false, true><<<grid, kTcThreads, p.smem_bytes, stream>>>(a_map, b_map, y_map, p);
+            tc_conv_kernel<false, false, true><<<grid, tc_threads(false, true), p.smem_bytes, stream>>>(a_map, b_map, y_map, p);
         return cudaGetLastError();
     }
     if (p.mode == kTcModePhase) {
