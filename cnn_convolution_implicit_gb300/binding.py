@@ -26,7 +26,8 @@ EXPORTS = ("conv_plan_create", "conv_plan_output_shape", "conv_plan_info", "conv
            "conv_plan_destroy", "conv_status_string", "conv_device_status", "conv_plan_num_sms",
            "conv_plan_launch_info", "conv_forward_affine", "conv_block_plan_create",
            "conv_block_plan_output_shape", "conv_block_forward", "conv_block_plan_launch_info",
-           "conv_block_plan_destroy", "conv_measure_mma_rate", "conv_check_wait_timeout")
+           "conv_block_plan_destroy", "conv_measure_mma_rate", "conv_check_wait_timeout",
+           "conv_plan_gemm_config")
 CONV_BLOCK_DW_RELU, CONV_BLOCK_PW_RELU = 1, 2
 
 _lock = threading.Lock()
@@ -77,6 +78,8 @@ def lib():
             L.conv_plan_num_sms.restype = c_int
             L.conv_plan_launch_info.argtypes = [vp] + [ctypes.POINTER(c_int)] * 5
             L.conv_plan_launch_info.restype = c_int
+            L.conv_plan_gemm_config.argtypes = [vp] + [ctypes.POINTER(c_int)] * 5
+            L.conv_plan_gemm_config.restype = c_int
             L.conv_block_plan_create.argtypes = [ctypes.POINTER(vp)] + [c_int] * 7 + [ctypes.c_uint]
             L.conv_block_plan_create.restype = c_int
             L.conv_block_plan_output_shape.argtypes = [vp, ctypes.POINTER(c_int), ctypes.POINTER(c_int)]
@@ -147,6 +150,11 @@ class ConvPlan:
         li = [ctypes.c_int() for _ in range(5)]
         L.conv_plan_launch_info(h, *[ctypes.byref(v) for v in li])
         self.launch = dict(zip(("grid", "block", "smem_bytes", "stages", "cluster"), [v.value for v in li]))
+        gc = [ctypes.c_int(0) for _ in range(5)]
+        if L.conv_plan_gemm_config(h, *[ctypes.byref(v) for v in gc]) == 0:
+            self.gemm = dict(zip(("mode", "n_tile", "pair", "dual", "resident_weights"), [v.value for v in gc]))
+        else:
+            self.gemm = None  # not a tensor-core GEMM plan
 
     @classmethod
     def for_shape(cls, s, sm_pairs=None, winograd=False, per_tap=False):

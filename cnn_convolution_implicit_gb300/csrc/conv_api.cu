@@ -265,6 +265,7 @@ bool configure_tc(conv_plan* pl, bool one_by_one, bool transposed = false) {
     t.halo = 0;
     t.halo_w = t.halo_h = t.halo_bytes = t.halo_stages = 0;
     t.btaps = 1;
+    t.bres = 0;
     if (t.mode == kTcModeHalo) {
         // one box {64 ch, halo_w, halo_h} per 64-channel block: the tile (two side by side
         // for two tiles per CTA) plus the (K-1)*D border its taps reach
@@ -281,8 +282,22 @@ bool configure_tc(conv_plan* pl, bool one_by_one, bool transposed = false) {
         int bt_max = (1536 + tap_clk - 1) / tap_clk;
         if (bt_max > taps) bt_max = taps;
         int hs = 0, bs = 0, hbytes = 0, bt = 0;
+        long long wbytes = 0;
         if (hw <= 256 && hh <= 256) {
             hbytes = static_cast<int>((hw * hh * 128 + 1023) / 1024 * 1024);
+            // Resident weights (one SM per unit): where every CTA keeps one n-tile and its
+            // rows for all taps and channel blocks fit beside two halos, they load once and
+            // the MMA issuer waits only for halos.
+            wbytes = static_cast<long long>(t.ksteps) * mma_n * 128;
+            if (!t.pair && gpc == 1 && t.num_n_tiles <= 8 &&
+                fixed + 2LL * hbytes + wbytes <= static_cast<long long>(pl->smem_optin)) {
+                t.bres = 1;
+                hs = fixed + 3LL * hbytes + wbytes <= static_cast<long long>(pl->smem_optin) ? 3 : 2;
+                bt = taps;
+                bs = 1;
+            }
+        }
+        if (hbytes > 0 && !t.bres) {
             for (int cbt = bt_max; cbt >= 1 && hs == 0; --cbt) {
                 const long long stage = static_cast<long long>(cbt) * b_rows * 128;
                 auto fit = [&](int h) {
@@ -310,7 +325,7 @@ bool configure_tc(conv_plan* pl, bool one_by_one, bool transposed = false) {
             }
             t.btaps = bt;
             t.stages = bs;
-            t.smem_bytes = fixed + hs * hbytes + bs * bt * b_rows * 128;
+            t.smem_bytes = fixed + hs * hbytes + (t.bres ? static_cast<int>(wbytes) : bs * bt * b_rows * 128);
         } else {  // the halo does not fit: per-tap rectangle tiles
             t.mode = kTcModeRect;
             int best = 0;
@@ -338,6 +353,24 @@ bool configure_tc(conv_plan* pl, bool one_by_one, bool transposed = false) {
         if (stages < 2 || stages < gpc) return false;
         t.stages = stages;
         t.smem_bytes = fixed + stages * stage_bytes;
+    }
+    // 1x1 layers: where one n-tile's weight rows for the whole reduction fit beside an A
+    // ring of at least four stages, they stay in shared memory (loaded once per CTA) and
+    // the ring carries the pixels only.  The weights were the larger part of each stage
+    // (a 256-row block against 128 pixel rows) and came from L2 again for every tile.
+    // Every CTA's units share one n-tile (the grid is a multiple of the n-tile count).
+    if (t.mode == kTcMode1x1 && gpc == 1 && !t.dual && t.num_n_tiles <= 8) {
+        const bool pairs = t.pair != 0;
+        const long long wbytes = static_cast<long long>(t.ksteps) * (pairs ? mma_n / 2 : mma_n) * 128;
+        const long long left = static_cast<long long>(pl->smem_optin) - fixed - wbytes;
+        long long st = left > 0 ? left / (kTcBlockM * kTcBlockK * 2) : 0;
+        if (st > 8) st = 8;
+        if (st >= 4) {
+            t.bres = 1;
+            t.pair = pairs ? 1 : 0;
+            t.stages = static_cast<int>(st);
+            t.smem_bytes = fixed + static_cast<int>(wbytes) + t.stages * kTcBlockM * kTcBlockK * 2;
+        }
     }
     t.tmem_cols = pow2_at_least((t.dual ? 4 : 2) * n_tile);
     t.relu = (pl->flags & CONV_FLAG_RELU) ? 1 : 0;
@@ -668,6 +701,19 @@ conv_status conv_plan_info(const conv_plan* p, int* path, long long* gemm_m, lon
 
 int conv_plan_num_sms(const conv_plan* p) { return p ? p->num_sms : 0; }
 
+conv_status conv_plan_gemm_config(const conv_plan* p, int* mode, int* n_tile, int* pair, int* dual,
+                                  int* resident_weights) {
+    if (p == nullptr || (p->path != CONV_PATH_GEMM_1X1 && p->path != CONV_PATH_IMPLICIT_GEMM))
+        return CONV_ERR_INVALID_ARG;
+    const TcGemmParams& t = p->tc;
+    if (mode) *mode = t.mode;
+    if (n_tile) *n_tile = t.n_tile;
+    if (pair) *pair = t.pair;
+    if (dual) *dual = t.dual;
+    if (resident_weights) *resident_weights = t.bres;
+    return CONV_OK;
+}
+
 conv_status conv_plan_launch_info(const conv_plan* p, int* grid, int* block, int* smem_bytes, int* stages,
                                   int* cluster) {
     if (p == nullptr) return CONV_ERR_INVALID_ARG;
@@ -683,13 +729,19 @@ conv_status conv_plan_launch_info(const conv_plan* p, int* grid, int* block, int
                 const int pair_tiles = ((t.num_m_tiles + 1) / 2) * t.num_n_tiles;
                 int clusters = p->pair_clusters > 0 ? p->pair_clusters : p->num_sms / 2;
                 if (clusters > pair_tiles) clusters = pair_tiles;
+                if (t.bres) {  // whole n-tile sets, so every cluster keeps one n-tile
+                    clusters -= clusters % t.num_n_tiles;
+                    if (clusters == 0) clusters = t.num_n_tiles;
+                }
                 gr = 2 * clusters;
                 cl = 2;
-            } else if (t.dual) {
-                const int units = ((t.num_m_tiles + 1) / 2) * t.num_n_tiles;
-                gr = units < p->num_sms ? units : p->num_sms;
             } else {
-                gr = t.num_tiles < p->num_sms ? t.num_tiles : p->num_sms;
+                const int units = t.dual ? ((t.num_m_tiles + 1) / 2) * t.num_n_tiles : t.num_tiles;
+                gr = units < p->num_sms ? units : p->num_sms;
+                if (t.bres) {  // whole n-tile sets, so every CTA keeps one n-tile
+                    gr -= gr % t.num_n_tiles;
+                    if (gr == 0) gr = t.num_n_tiles;
+                }
             }
             break;
         }

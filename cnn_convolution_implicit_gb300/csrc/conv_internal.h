@@ -164,6 +164,7 @@ struct TcGemmParams {
     int halo_bytes;      // kTcModeHalo: one halo stage (box bytes rounded up to 1024)
     int halo_stages;     // kTcModeHalo: halos in flight (stages is then the weight ring)
     int btaps;           // kTcModeHalo: taps per weight stage (one barrier wait feeds btaps x 4 MMAs)
+    int bres;            // 1x1 mode: the tile's weights stay in shared memory (loaded once per CTA; the ring carries A only)
     int ps;            // kTcModePhase: the transposed convolution's stride S (phases = S*S)
     int hq, wq;        // kTcModePhase: output rows / columns per phase (H_out / S, W_out / S)
     TcPhaseAxis ph, pw;

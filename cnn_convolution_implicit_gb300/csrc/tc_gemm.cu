@@ -63,18 +63,20 @@ struct TcSmem {
     uint64_t* drain;
     uint64_t* hfull;   // halo mode: halo landed
     uint64_t* hempty;  // halo mode: every tap of the halo consumed
+    uint64_t* bfull;   // resident weights landed
     uint32_t* tmem_slot;
     int* abort;
 };
 
-// a_bytes: one A stage (per-tap modes) or one halo stage (halo mode, p.halo_stages of them).
-__device__ __forceinline__ TcSmem carve(uint8_t* raw, const TcGemmParams& p, uint32_t a_bytes, uint32_t b_bytes) {
+// a_bytes: one A stage (per-tap modes) or one halo stage (halo mode, p.halo_stages of them);
+// b_total: the weight ring, or the resident weights.
+__device__ __forceinline__ TcSmem carve(uint8_t* raw, const TcGemmParams& p, uint32_t a_bytes, uint32_t b_total) {
     TcSmem s;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     const int a_stages = p.halo ? p.halo_stages : p.stages;
     s.a = base;
     s.b = s.a + a_stages * a_bytes;
-    s.out = s.b + p.stages * b_bytes;
+    s.out = s.b + b_total;
     uint64_t* bars = reinterpret_cast<uint64_t*>(s.out + 8 * 2 * kOutTileBytes);
     s.full = bars;
     s.empty = bars + p.stages;
@@ -83,7 +85,8 @@ __device__ __forceinline__ TcSmem carve(uint8_t* raw, const TcGemmParams& p, uin
     s.drain = s.tempty + 2;
     s.hfull = s.drain + 1;
     s.hempty = s.hfull + kTcMaxHaloStages;
-    s.tmem_slot = reinterpret_cast<uint32_t*>(s.hempty + kTcMaxHaloStages);
+    s.bfull = s.hempty + kTcMaxHaloStages;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(s.bfull + 1);
     s.abort = reinterpret_cast<int*>(s.tmem_slot + 1);
     return s;
 }
@@ -270,7 +273,9 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, uint64_t* empty, int 
 // stage holds `btaps` consecutive taps of one block (the last stage of a block
 // may hold fewer), so every barrier wait of the MMA issuer is followed by enough
 // MMAs to cover its latency.  Each role drains its own ring before returning.
-template <bool PAIR, bool DUAL, int ROLE>
+// RESB (resident weights, one SM per unit): ROLE 1 loads the n-tile's rows for every
+// channel block and tap once, and the MMAs read them in place.
+template <bool PAIR, bool DUAL, int ROLE, bool RESB = false>
 __device__ __forceinline__ void halo_producer(const TcGemmParams& p, const CUtensorMap* a_map,
                                               const CUtensorMap* b_map, const TcSmem& sm, int unit0, int unit_step,
                                               int num_units, uint32_t rank, bool leader, volatile int* abort) {
@@ -306,6 +311,14 @@ __device__ __forceinline__ void halo_producer(const TcGemmParams& p, const CUten
             if (blk + 1 < nblocks) halo_walk_next<PAIR, DUAL>(p, w, unit_step, num_units, rank);
         }
         drain_ring(sm.hfull, sm.hempty, HS, issued, leader, p.status, abort);
+    } else if constexpr (RESB) {
+        static_assert(!PAIR, "resident weights run one SM per unit");
+        const uint32_t b_tap = static_cast<uint32_t>(p.mma_n) * 128u;
+        mbar_arrive_expect_tx(sm.bfull, b_tap * static_cast<uint32_t>(T * p.kblk));
+        for (int kb = 0; kb < p.kblk; ++kb)
+            for (int tap = 0; tap < T; ++tap)
+                tma_load_2d(sm.b + (kb * T + tap) * b_tap, b_map, sm.bfull, tap * p.g.cin_g + kb * kTcBlockK, w.brow);
+        if (!mbar_wait(sm.bfull, 0, nullptr)) record_status(p.status, kStatusTimeoutDrain, abort);
     } else {
         const int BT = p.btaps, BS = p.stages;
         const int b_rows = PAIR ? p.mma_n / 2 : p.mma_n;
@@ -347,12 +360,12 @@ __device__ __forceinline__ void halo_producer(const TcGemmParams& p, const CUten
 // four K = 16 MMAs whose A descriptor starts at the tap's shifted halo row.
 // part: 0 or 1 = only that pixel tile's MMAs (two tiles per CTA, one issuing thread per
 // tile), 2 = every MMA.
-template <bool PAIR, bool DUAL>
+template <bool PAIR, bool DUAL, bool RESB = false>
 __device__ __forceinline__ void halo_mma(const TcGemmParams& p, const TcSmem& sm, uint32_t tmem_base, int unit0,
                                          int unit_step, int num_units, volatile int* abort, int part) {
     const uint32_t idesc = idesc_bf16_f32((PAIR ? 2 : 1) * kTcBlockM, p.mma_n);
     const int T = p.g.Kh * p.g.Kw;
-    const int BT = p.btaps;
+    const int BT = RESB ? T : p.btaps;  // resident weights: every tap of a block after one halo wait
     const int b_rows = PAIR ? p.mma_n / 2 : p.mma_n;
     const uint32_t b_tap = static_cast<uint32_t>(b_rows) * 128u;
     const uint32_t b_stage = b_tap * static_cast<uint32_t>(BT);
@@ -363,6 +376,10 @@ __device__ __forceinline__ void halo_mma(const TcGemmParams& p, const TcSmem& sm
     uint32_t hph = 0, bph = 0;
     int local = 0;
     bool ok = true;
+    if (RESB && unit0 < num_units && !mbar_wait(sm.bfull, 0, abort)) {
+        record_status(p.status, kStatusTimeoutMma, abort);
+        ok = false;
+    }
     for (int u = unit0; u < num_units && ok; u += unit_step, ++local) {
         const int buf = local & 1;
         const uint32_t use = static_cast<uint32_t>(local >> 1) & 1u;
@@ -385,14 +402,15 @@ __device__ __forceinline__ void halo_mma(const TcGemmParams& p, const TcSmem& sm
                 const uint32_t hbase = smem_addr(sm.a + hs * p.halo_bytes);
                 int kh = 0, kw = 0;
                 for (int tap0 = 0; tap0 < T; tap0 += BT) {
-                    if (!mbar_wait(&sm.full[bs], bph, abort)) {
+                    if (!RESB && !mbar_wait(&sm.full[bs], bph, abort)) {
                         record_status(p.status, kStatusTimeoutMma, abort);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const int nt = T - tap0 < BT ? T - tap0 : BT;
-                    const uint32_t bbase = smem_addr(sm.b + bs * b_stage);
+                    const uint32_t bbase = RESB ? smem_addr(sm.b) + static_cast<uint32_t>(kb * T) * b_tap
+                                                : smem_addr(sm.b + bs * b_stage);
                     for (int i = 0; i < nt; ++i) {
                         const uint32_t a_addr =
                             hbase + static_cast<uint32_t>(kh) * row_kh + static_cast<uint32_t>(kw) * row_kw;
@@ -420,13 +438,15 @@ __device__ __forceinline__ void halo_mma(const TcGemmParams& p, const TcSmem& sm
                             ++kh;
                         }
                     }
-                    if constexpr (PAIR)
-                        mma_commit_pair(&sm.empty[bs], 0x3);
-                    else
-                        mma_commit(&sm.empty[bs]);
-                    if (++bs == p.stages) {
-                        bs = 0;
-                        bph ^= 1u;
+                    if constexpr (!RESB) {
+                        if constexpr (PAIR)
+                            mma_commit_pair(&sm.empty[bs], 0x3);
+                        else
+                            mma_commit(&sm.empty[bs]);
+                        if (++bs == p.stages) {
+                            bs = 0;
+                            bph ^= 1u;
+                        }
                     }
                 }
                 if (!ok) break;
@@ -464,7 +484,11 @@ __device__ __forceinline__ void halo_mma(const TcGemmParams& p, const TcSmem& sm
 // per-K-step work feeds twice the tensor work.
 // HALO: the halo mode (kTcModeHalo, stride 1): one input halo per 64-channel
 // block feeds every tap through shifted descriptors.
-template <bool PAIR, bool PHASE, bool DUAL, bool HALO = false>
+// RESB: resident weights (1x1 and halo modes): every CTA keeps one n-tile (the grid
+// is a multiple of the n-tile count), whose weight rows for the whole reduction load
+// once into shared memory; the ring carries pixels only and the MMA issuer waits on
+// A (halo) stages alone.
+template <bool PAIR, bool PHASE, bool DUAL, bool HALO = false, bool RESB = false>
 __global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
     tc_conv_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
                    const __grid_constant__ CUtensorMap y_map, const TcGemmParams p) {
@@ -474,7 +498,9 @@ __global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
     const int b_rows = PAIR ? p.mma_n / 2 : p.mma_n;  // weight rows this CTA loads per K-step
     const uint32_t b_bytes = static_cast<uint32_t>(b_rows) * 128u;
     const TcSmem sm = carve(smem_raw, p, HALO ? static_cast<uint32_t>(p.halo_bytes) : a_stage,
-                            HALO ? b_bytes * static_cast<uint32_t>(p.btaps) : b_bytes);
+                            RESB ? b_bytes * static_cast<uint32_t>(p.ksteps)
+                                 : (HALO ? b_bytes * static_cast<uint32_t>(p.btaps) : b_bytes) *
+                                       static_cast<uint32_t>(p.stages));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     volatile int* abort = sm.abort;
@@ -498,6 +524,7 @@ __global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
             mbar_init(&sm.tempty[b], PAIR ? 2 * 8 : 8);  // one arrival per warp of its two epilogue groups (both CTAs)
         }
         mbar_init(sm.drain, mma_threads);
+        mbar_init(sm.bfull, 1);
         if constexpr (HALO) {
             for (int h = 0; h < p.halo_stages; ++h) {
                 mbar_init(&sm.hfull[h], 1);
@@ -530,11 +557,13 @@ __global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
             if (warp == 0)
                 halo_producer<PAIR, DUAL, 0>(p, &a_map, &b_map, sm, unit0, unit_step, num_units, rank, leader, abort);
             else
-                halo_producer<PAIR, DUAL, 1>(p, &a_map, &b_map, sm, unit0, unit_step, num_units, rank, leader, abort);
+                halo_producer<PAIR, DUAL, 1, RESB && HALO>(p, &a_map, &b_map, sm, unit0, unit_step, num_units, rank, leader,
+                                                   abort);
         }
     } else if (HALO && (warp == 1 || (DUAL && warp == tc_mma2_warp(true)))) {
         if (lane == 0 && leader)
-            halo_mma<PAIR, DUAL>(p, sm, tmem_base, unit0, unit_step, num_units, abort, DUAL ? (warp == 1 ? 0 : 1) : 2);
+            halo_mma<PAIR, DUAL, RESB && HALO>(p, sm, tmem_base, unit0, unit_step, num_units, abort,
+                                       DUAL ? (warp == 1 ? 0 : 1) : 2);
     } else if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -542,7 +571,23 @@ __global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
-            const uint32_t a_b_bytes = PAIR ? 2u * (kABytes + b_bytes) : a_stage + b_bytes;
+            const uint32_t a_b_bytes = RESB ? (PAIR ? 2u * kABytes : a_stage)
+                                            : (PAIR ? 2u * (kABytes + b_bytes) : a_stage + b_bytes);
+            if (RESB && unit0 < num_units) {
+                // resident weights: every CTA's units share one n-tile (the grid is a multiple of the
+                // n-tile count), so its weight rows for every K-step load once
+                int grp, brow;
+                sub_gemm(p, unit0 % p.num_n_tiles, 0, grp, brow);
+                const uint32_t bfull_leader = PAIR ? mapa_shared(smem_addr(sm.bfull), 0) : 0u;
+                if (leader) mbar_arrive_expect_tx(sm.bfull, (PAIR ? 2u : 1u) * b_bytes * static_cast<uint32_t>(p.ksteps));
+                for (int ks = 0; ks < p.ksteps; ++ks) {
+                    if constexpr (PAIR)
+                        tma_load_2d_pair(sm.b + ks * b_bytes, &b_map, bfull_leader, ks * kTcBlockK,
+                                         brow + static_cast<int>(rank) * b_rows);
+                    else
+                        tma_load_2d(sm.b + ks * b_bytes, &b_map, sm.bfull, ks * kTcBlockK, brow);
+                }
+            }
             for (int u = unit0; u < num_units && ok; u += unit_step) {
                 const int mu = u / p.num_n_tiles;
                 const int nt = u - mu * p.num_n_tiles;
@@ -607,10 +652,12 @@ __global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
                         load_a<PAIR, PHASE>(p, &a_map, a_dst, &sm.full[stage], full_leader, t, c, tp);
                         if constexpr (DUAL) load_a<PAIR, PHASE>(p, &a_map, a_dst + kABytes, &sm.full[stage], 0u, t1, c, tp);
                         const int kcol = tp.wtap * p.g.cin_g + kb * kTcBlockK;
-                        if constexpr (PAIR)
-                            tma_load_2d_pair(b_dst, &b_map, full_leader, kcol, brow + static_cast<int>(rank) * b_rows);
-                        else
-                            tma_load_2d(b_dst, &b_map, &sm.full[stage], kcol, brow);
+                        if constexpr (!RESB) {
+                            if constexpr (PAIR)
+                                tma_load_2d_pair(b_dst, &b_map, full_leader, kcol, brow + static_cast<int>(rank) * b_rows);
+                            else
+                                tma_load_2d(b_dst, &b_map, &sm.full[stage], kcol, brow);
+                        }
                         ++issued;
                         if (++stage == p.stages) {
                             stage = 0;
@@ -629,6 +676,10 @@ __global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
                 const bool done = leader ? mbar_wait(&sm.full[s], par, nullptr) : mbar_wait(&sm.empty[s], par, nullptr);
                 if (!done) record_status(p.status, kStatusTimeoutDrain, abort);
             }
+            // the resident weights (a peer's land on the leader's barrier, which its MMA
+            // waited for before releasing the stages waited on above)
+            if (RESB && leader && unit0 < num_units && !mbar_wait(sm.bfull, 0, nullptr))
+                record_status(p.status, kStatusTimeoutDrain, abort);
         }
     } else if (warp == 1 || (DUAL && warp == tc_mma2_warp(false))) {
         // ------------------------------------------------------------ MMA issuer (leader only)
@@ -641,6 +692,10 @@ __global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
             uint32_t phase = 0;
             int local = 0;
             bool ok = true;
+            if (RESB && unit0 < num_units) {
+                ok = mbar_wait(sm.bfull, 0, abort);
+                if (!ok) record_status(p.status, kStatusTimeoutMma, abort);
+            }
             for (int u = unit0; u < num_units && ok; u += unit_step, ++local) {
                 const int buf = local & 1;
                 const uint32_t use = static_cast<uint32_t>(local >> 1) & 1u;
@@ -667,7 +722,7 @@ __global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
                         }
                         tc_fence_after();
                         const uint64_t adesc = sdesc_sw128(smem_addr(sm.a + stage * a_stage));
-                        const uint64_t bdesc = sdesc_sw128(smem_addr(sm.b + stage * b_bytes));
+                        const uint64_t bdesc = sdesc_sw128(smem_addr(sm.b + (RESB ? ks : stage) * b_bytes));
                         if (!DUAL || part != 1) {
 #pragma unroll
                             for (int k = 0; k < kTcBlockK / 16; ++k) {
@@ -818,11 +873,11 @@ static SmemLimitCache g_pair_smem_limits;
 namespace {
 
 // Launch one instantiation: clusters of two CTAs for SM pairs, else plain.
-template <bool PAIR, bool PHASE, bool DUAL, bool HALO>
+template <bool PAIR, bool PHASE, bool DUAL, bool HALO, bool RESB = false>
 cudaError_t launch_one(const CUtensorMap& a_map, const CUtensorMap& b_map, const CUtensorMap& y_map,
                        const TcGemmParams& p, int grid, cudaStream_t stream) {
     static SmemLimitCache limits;
-    auto* fn = tc_conv_kernel<PAIR, PHASE, DUAL, HALO>;
+    auto* fn = tc_conv_kernel<PAIR, PHASE, DUAL, HALO, RESB>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fn), p.smem_bytes, limits);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -847,9 +902,17 @@ cudaError_t launch_one(const CUtensorMap& a_map, const CUtensorMap& b_map, const
 cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, const CUtensorMap& y_map,
                            const TcGemmParams& p, int grid, cudaStream_t stream) {
     if (p.halo) {
+        if (p.bres) {
+            if (p.dual) return launch_one<false, false, true, true, true>(a_map, b_map, y_map, p, grid, stream);
+            return launch_one<false, false, false, true, true>(a_map, b_map, y_map, p, grid, stream);
+        }
         if (p.pair) return launch_one<true, false, false, true>(a_map, b_map, y_map, p, grid, stream);
         if (p.dual) return launch_one<false, false, true, true>(a_map, b_map, y_map, p, grid, stream);
         return launch_one<false, false, false, true>(a_map, b_map, y_map, p, grid, stream);
+    }
+    if (p.bres) {
+        if (p.pair) return launch_one<true, false, false, false, true>(a_map, b_map, y_map, p, grid, stream);
+        return launch_one<false, false, false, false, true>(a_map, b_map, y_map, p, grid, stream);
     }
     if (p.pair) {
         static SmemLimitCache pair_phase_limits;

@@ -238,6 +238,25 @@ conv_status conv_check_wait_timeout(unsigned long long limit_ns, unsigned long l
 conv_status conv_plan_launch_info(const conv_plan *p, int *grid, int *block, int *smem_bytes,
                                   int *stages, int *cluster);
 
+/*
+ * How a tensor-core GEMM plan (CONV_PATH_GEMM_1X1, CONV_PATH_IMPLICIT_GEMM) runs the
+ * contraction (lesson 9, sections 21-24: the convolution as a GEMM over pixels x output
+ * channels x C_in/G*Kh*Kw), for tests and tuning:
+ *   mode              0 = 1x1 (A is the [pixels][C_in] matrix), 1 = TMA im2col (stride > 1),
+ *                     2 = one input box per tap (stride 1 with CONV_FLAG_PER_TAP, or a halo
+ *                     wider than a TMA box), 3 = phase (transposed), 4 = halo tiles;
+ *   n_tile            output channels per tile (the accumulator's columns);
+ *   pair              1: SM pairs (cta_group::2, 256 pixels per MMA);
+ *   dual              1: two pixel tiles per CTA;
+ *   resident_weights  1: every CTA keeps one n-tile, and that n-tile's weight rows for the
+ *                     whole reduction sit in shared memory from its first tile on (loaded
+ *                     once instead of once per tile).
+ * Any output pointer may be NULL.  Returns CONV_ERR_INVALID_ARG for a NULL plan or one on
+ * another path.
+ */
+conv_status conv_plan_gemm_config(const conv_plan *p, int *mode, int *n_tile, int *pair, int *dual,
+                                  int *resident_weights);
+
 /* ------------------------------------------------------------------------
  * Depthwise-separable block in one kernel: depthwise 3x3 (FP32) followed by
  * pointwise 1x1 (BF16 tensor cores), the two stages of "GPU lesson 9"

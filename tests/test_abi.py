@@ -221,7 +221,7 @@ def test_winograd_kernel_choice(shape, winograd, path):
 @pytest.mark.parametrize("shape,sm_pairs,cluster", [
     ((32, 128, 112, 112, 256, 3, 3, 1, 1, 1, 1), None, 2),    # body: long full-width reduction -> pairs
     ((32, 128, 112, 112, 256, 3, 3, 1, 1, 1, 1), False, 1),   # forced one SM
-    ((64, 256, 56, 56, 512, 1, 1, 1, 0, 1, 1), None, 1),      # pointwise: 4 K-steps -> one SM
+    ((64, 256, 56, 56, 512, 1, 1, 1, 0, 1, 1), None, 1),      # pointwise: 4 K-steps -> one SM (resident weights)
     ((64, 256, 56, 56, 512, 1, 1, 1, 0, 1, 1), True, 2),      # forced pairs
     ((16, 256, 64, 64, 256, 3, 3, 1, 2, 2, 4), None, 1),      # grouped: N = 64 per group -> one SM
     ((4, 128, 31, 29, 256, 3, 3, 2, 1, 1, 1), None, 2),       # strided (im2col mode), 18 K-steps, 8 tiles
@@ -276,10 +276,44 @@ def test_halo_mode_choice(shape, halo):
     warps); two pixel tiles per CTA add a second MMA-issuing warp in either mode."""
     p = cg.ConvPlan(*shape, dtype="bf16", bias=True, relu=True)
     assert p.path in ("implicit_gemm", "gemm_1x1")
-    assert p.launch["smem_bytes"] <= 232448 and p.launch["stages"] >= 2
+    assert p.launch["smem_bytes"] <= 232448
+    assert p.launch["stages"] >= (1 if p.gemm["resident_weights"] else 2)
+    assert (p.gemm["mode"] == 4) == halo
     q = cg.ConvPlan(*shape, dtype="bf16", bias=True, relu=True, per_tap=True)
-    assert q.path == p.path and q.launch["block"] in (576, 608)
+    assert q.path == p.path and q.launch["block"] in (576, 608) and q.gemm["mode"] != 4
     assert p.launch["block"] == q.launch["block"] + (32 if halo else 0)
+
+
+# Resident weights: where one n-tile's weight rows for the whole reduction fit in shared
+# memory beside the operand ring (two halos in the halo mode, four A stages in the 1x1
+# mode), on one SM per unit; every CTA keeps one n-tile, so the grid is a multiple of the
+# n-tile count.  (shape, resident, n-tiles)
+@pytest.mark.parametrize("shape,resident,sm_pairs", [
+    ((16, 256, 64, 64, 256, 3, 3, 1, 2, 2, 4), 1, None),   # dilated grouped: 9 taps x 64 rows (72 KB)
+    ((64, 256, 56, 56, 512, 1, 1, 1, 0, 1, 1), 1, None),   # pointwise: 4 blocks x 256 rows (128 KB)
+    ((3, 256, 9, 13, 768, 1, 1, 1, 0, 1, 1), 1, None),     # three n-tiles
+    ((2, 256, 21, 19, 64, 3, 3, 1, 1, 1, 2), 1, None),     # two channel blocks per tap, two groups
+    ((2, 64, 10, 14, 256, 1, 3, 1, 1, 1, 1), 1, None),     # halo mode, one tile per CTA
+    ((64, 256, 56, 56, 512, 1, 1, 1, 0, 1, 1), 1, True),   # 1x1 on SM pairs: half the rows per SM
+    ((32, 128, 112, 112, 256, 3, 3, 1, 1, 1, 1), 0, None),  # body: 18 K-steps x 128 rows do not fit
+    ((2, 64, 12, 12, 64, 5, 5, 1, 2, 1, 1), 0, None),      # 25 taps x 64 rows beside two halos do not fit
+    ((4, 128, 31, 29, 256, 3, 3, 2, 1, 1, 1), 0, None),    # strided (im2col mode): weights stream
+])
+def test_resident_weights_choice(shape, resident, sm_pairs):
+    p = cg.ConvPlan(*shape, dtype="bf16", bias=True, relu=True, sm_pairs=sm_pairs)
+    assert p.gemm["resident_weights"] == resident
+    assert p.launch["smem_bytes"] <= 232448
+    if resident:
+        n_tiles = shape[4] // p.gemm["n_tile"]
+        per_cta = p.launch["grid"] // p.launch["cluster"]
+        assert per_cta % n_tiles == 0
+
+
+def test_gemm_config_other_paths():
+    """conv_plan_gemm_config answers for the tensor-core GEMM paths only."""
+    p = cg.ConvPlan(2, 64, 9, 9, 64, 3, 3, 1, 1, 1, 64, dtype="f32", bias=True, relu=True)
+    assert p.path == "depthwise" and p.gemm is None
+    assert cg.lib().conv_plan_gemm_config(None, None, None, None, None, None) == 1
 
 
 def test_wait_timeout_check_rejects_bad_arguments_without_launching():

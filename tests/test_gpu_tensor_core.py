@@ -176,6 +176,31 @@ def test_per_tap_mode_full(shape, sm_pairs):
     check_full(shape, y_h, ref)
 
 
+# Resident weights: each CTA keeps one n-tile's weight rows for the whole reduction in
+# shared memory (halo mode with one and two tiles per CTA, 1x1 mode on one SM and on SM
+# pairs), including two channel blocks per tap, several n-tiles and ragged tiles.
+RESIDENT_SHAPES = [
+    (ConvShape(2, 256, 21, 19, 64, 3, 3, 1, 1, 1, 2, "bf16", True, True), None),
+    (ConvShape(2, 64, 10, 14, 256, 1, 3, 1, 1, 1, 1, "bf16", True, False), None),
+    (ConvShape(1, 128, 11, 35, 64, 3, 3, 1, 2, 2, 2, "bf16", False, True), None),
+    (ConvShape(3, 256, 9, 13, 768, 1, 1, 1, 0, 1, 1, "bf16", True, True), None),
+    (ConvShape(3, 256, 9, 13, 768, 1, 1, 1, 0, 1, 1, "bf16", True, True), True),
+    (ConvShape(2, 128, 7, 9, 96, 1, 1, 1, 0, 1, 1, "bf16", False, False), None),
+]
+
+
+@pytest.mark.parametrize("shape,sm_pairs", RESIDENT_SHAPES,
+                         ids=lambda v: ("K%dx%dG%d_%dto%d" % (v.Kh, v.Kw, v.G, v.C_in, v.C_out))
+                         if isinstance(v, ConvShape) else str(v))
+def test_resident_weights_full(shape, sm_pairs):
+    """Every output of plans whose weights stay in shared memory across tiles."""
+    from cnn_convolution_implicit_gb300 import ConvPlan
+    x, w, b = draw(shape, (71, 72, 73))
+    plan, y = run(shape, x, w, b, plan=ConvPlan.for_shape(shape, sm_pairs=sm_pairs))
+    assert plan.gemm["resident_weights"] == 1
+    check_full(shape, y, oracle_full(shape, x, w, b))
+
+
 def test_halo_mode_random_sweep():
     """Random stride-1 BF16 shapes in the halo mode (kernel sizes 1-5 per axis, dilation
     1-3, padding, groups, ragged 8 x 16 tiles, widths that leave a lone right-hand tile of
