@@ -494,6 +494,11 @@ __global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
                    const __grid_constant__ CUtensorMap y_map, const TcGemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     constexpr bool TWO = PAIR || DUAL;                   // work units of two pixel tiles
+    // 1x1 with resident weights: every epilogue warp drains every tile (a quarter of its
+    // columns each), so a tile drains in half the time; the MMAs of the next tile meanwhile
+    // fill the other accumulator.  (Pointwise layer 64.4 -> 61.5 us; the per-tap and halo
+    // kernels measured slower this way and keep two groups per accumulator.)
+    constexpr bool ALLW = RESB && !HALO && !PAIR && !DUAL;
     constexpr uint32_t a_stage = DUAL ? 2 * kABytes : kABytes;
     const int b_rows = PAIR ? p.mma_n / 2 : p.mma_n;  // weight rows this CTA loads per K-step
     const uint32_t b_bytes = static_cast<uint32_t>(b_rows) * 128u;
@@ -521,7 +526,7 @@ __global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.tfull[b], mma_threads);
-            mbar_init(&sm.tempty[b], PAIR ? 2 * 8 : 8);  // one arrival per warp of its two epilogue groups (both CTAs)
+            mbar_init(&sm.tempty[b], ALLW ? 16 : (PAIR ? 2 * 8 : 8));  // one arrival per warp that drains it (both CTAs)
         }
         mbar_init(sm.drain, mma_threads);
         mbar_init(sm.bfull, 1);
@@ -779,7 +784,7 @@ __global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
         int local = 0;
         for (int u = unit0; u < num_units; u += unit_step, ++local) {
             const int buf = local & 1;
-            if (buf != group) continue;
+            if (!ALLW && buf != group) continue;
             const uint32_t use = static_cast<uint32_t>(local >> 1) & 1u;
             // warp-uniform outcome, so the .sync.aligned TMEM loads below stay converged
             const bool ready = __all_sync(0xffffffffu, mbar_wait(&sm.tfull[buf], use, abort));
@@ -819,14 +824,17 @@ __global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
                                    static_cast<uint32_t>(buf * (DUAL ? 2 : 1) * p.n_tile + (DUAL ? chalf * p.n_tile : 0));
             // this group's half of the columns, 32 per step, one staging tile per warp
             const int chunks = p.n_tile / 32;
-            const int c_lo = DUAL ? 0 : (chalf == 0 ? 0 : ((chunks + 1) / 2) * 32);
-            const int c_hi = DUAL ? p.n_tile : (chalf == 0 ? ((chunks + 1) / 2) * 32 : p.n_tile);
+            const int c_lo = ALLW ? 32 * ((chunks * egroup) / 4)
+                                  : DUAL ? 0 : (chalf == 0 ? 0 : ((chunks + 1) / 2) * 32);
+            const int c_hi = ALLW ? 32 * ((chunks * (egroup + 1)) / 4)
+                                  : DUAL ? p.n_tile : (chalf == 0 ? ((chunks + 1) / 2) * 32 : p.n_tile);
             for (int c = c_lo; c < c_hi; c += 32) {
                 uint32_t v[32];
                 __syncwarp();
                 tmem_ld32(t_row + static_cast<uint32_t>(c), v);
+                if (ALLW && lane == 0) bulk_wait_read_all();
                 tmem_ld_wait(v);
-                if (lane == 0) bulk_wait_read_all();
+                if (!ALLW && lane == 0) bulk_wait_read_all();
                 __syncwarp();
                 stage_row32(v, p.bias ? p.bias + co0 + c : nullptr, p.relu, stg, lane,
                             p.scale ? p.scale + co0 + c : nullptr);
