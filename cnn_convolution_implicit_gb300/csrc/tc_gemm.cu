@@ -830,14 +830,39 @@ __global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
                                   : DUAL ? p.n_tile : (chalf == 0 ? ((chunks + 1) / 2) * 32 : p.n_tile);
             for (int c = c_lo; c < c_hi; c += 32) {
                 uint32_t v[32];
-                __syncwarp();
-                tmem_ld32(t_row + static_cast<uint32_t>(c), v);
-                if (ALLW && lane == 0) bulk_wait_read_all();
-                tmem_ld_wait(v);
-                if (!ALLW && lane == 0) bulk_wait_read_all();
-                __syncwarp();
-                stage_row32(v, p.bias ? p.bias + co0 + c : nullptr, p.relu, stg, lane,
-                            p.scale ? p.scale + co0 + c : nullptr);
+                if constexpr (ALLW) {
+                    __syncwarp();
+                    tmem_ld32(t_row + static_cast<uint32_t>(c), v);
+                    if (lane == 0) bulk_wait_read_all();
+                    tmem_ld_wait(v);
+                    __syncwarp();
+                    stage_row32(v, p.bias ? p.bias + co0 + c : nullptr, p.relu, stg, lane,
+                                p.scale ? p.scale + co0 + c : nullptr);
+                } else {
+                    // lane l loads the scale and shift of channel co0 + c + l before the TMEM
+                    // load, and shuffles hand them round: no global load waits behind the
+                    // accumulator (body with a folded batch norm 145.4 -> 136.8 us, body 136.3 ->
+                    // 134.2, dilated 27.5 -> 26.7; the 1x1 kernel above measured slower this way)
+                    const float sl = p.scale ? __ldg(p.scale + co0 + c + lane) : 1.f;
+                    const float bl = p.bias ? __ldg(p.bias + co0 + c + lane) : 0.f;
+                    __syncwarp();
+                    tmem_ld32(t_row + static_cast<uint32_t>(c), v);
+                    tmem_ld_wait(v);
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+                    if (p.scale) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float si = __shfl_sync(0xffffffffu, sl, i), bi = __shfl_sync(0xffffffffu, bl, i);
+                            v[i] = __float_as_uint(fmaf(__uint_as_float(v[i]), si, bi));
+                        }
+                    } else if (p.bias) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = __float_as_uint(__uint_as_float(v[i]) + __shfl_sync(0xffffffffu, bl, i));
+                    }
+                    stage_row32(v, nullptr, p.relu, stg, lane, nullptr);
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0 && rows_exist) {
