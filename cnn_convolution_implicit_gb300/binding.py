@@ -78,7 +78,7 @@ def lib():
             L.conv_plan_num_sms.restype = c_int
             L.conv_plan_launch_info.argtypes = [vp] + [ctypes.POINTER(c_int)] * 5
             L.conv_plan_launch_info.restype = c_int
-            L.conv_plan_gemm_config.argtypes = [vp] + [ctypes.POINTER(c_int)] * 5
+            L.conv_plan_gemm_config.argtypes = [vp] + [ctypes.POINTER(c_int)] * 6
             L.conv_plan_gemm_config.restype = c_int
             L.conv_block_plan_create.argtypes = [ctypes.POINTER(vp)] + [c_int] * 7 + [ctypes.c_uint]
             L.conv_block_plan_create.restype = c_int
@@ -150,9 +150,9 @@ class ConvPlan:
         li = [ctypes.c_int() for _ in range(5)]
         L.conv_plan_launch_info(h, *[ctypes.byref(v) for v in li])
         self.launch = dict(zip(("grid", "block", "smem_bytes", "stages", "cluster"), [v.value for v in li]))
-        gc = [ctypes.c_int(0) for _ in range(5)]
+        gc = [ctypes.c_int(0) for _ in range(6)]
         if L.conv_plan_gemm_config(h, *[ctypes.byref(v) for v in gc]) == 0:
-            self.gemm = dict(zip(("mode", "n_tile", "pair", "dual", "resident_weights"), [v.value for v in gc]))
+            self.gemm = dict(zip(("mode", "n_tile", "pair", "dual", "resident_weights", "swapped"), [v.value for v in gc]))
         else:
             self.gemm = None  # not a tensor-core GEMM plan
 

@@ -255,6 +255,10 @@ bool configure_tc(conv_plan* pl, bool one_by_one, bool transposed = false) {
     // reduction: each K-step then feeds twice the tensor work for one weight block and
     // one more A copy (a 2-K-step 1x1 layer measured slower: its epilogue dominates).
     t.dual = (!t.pair && gpc == 1 && n_tile <= kDualMaxN && t.num_m_tiles >= 2 && min_ksteps >= 4) ? 1 : 0;
+    // Two tiles of 128 channels: one M128 N256 MMA (weights x both tiles' pixels) per K = 16 reads
+    // 12 KB of shared-memory operands instead of two M128 N128 MMAs' 16 KB (the per-tap modes;
+    // the halo mode's operands are the shifted halo windows).
+    t.swap = (t.dual && n_tile == kDualMaxN && mma_n == kDualMaxN) ? 1 : 0;
     if ((t.pair || t.dual) && transposed) {  // both tiles of a unit in one phase: round each phase's count up
         const long long spatial = static_cast<long long>(g.N) * t.rect_tiles_w * t.rect_tiles_h;
         t.num_m_tiles = static_cast<int>(((spatial + 1) / 2) * 2 * t.ps * t.ps);
@@ -314,6 +318,7 @@ bool configure_tc(conv_plan* pl, bool one_by_one, bool transposed = false) {
         }
         if (hs > 0) {
             t.halo = 1;
+            t.swap = 0;  // the halo mode's A operands are shifted halo windows
             t.halo_w = static_cast<int>(hw);
             t.halo_h = static_cast<int>(hh);
             t.halo_bytes = hbytes;
@@ -702,7 +707,7 @@ conv_status conv_plan_info(const conv_plan* p, int* path, long long* gemm_m, lon
 int conv_plan_num_sms(const conv_plan* p) { return p ? p->num_sms : 0; }
 
 conv_status conv_plan_gemm_config(const conv_plan* p, int* mode, int* n_tile, int* pair, int* dual,
-                                  int* resident_weights) {
+                                  int* resident_weights, int* swapped) {
     if (p == nullptr || (p->path != CONV_PATH_GEMM_1X1 && p->path != CONV_PATH_IMPLICIT_GEMM))
         return CONV_ERR_INVALID_ARG;
     const TcGemmParams& t = p->tc;
@@ -711,6 +716,7 @@ conv_status conv_plan_gemm_config(const conv_plan* p, int* mode, int* n_tile, in
     if (pair) *pair = t.pair;
     if (dual) *dual = t.dual;
     if (resident_weights) *resident_weights = t.bres;
+    if (swapped) *swapped = t.swap;
     return CONV_OK;
 }
 

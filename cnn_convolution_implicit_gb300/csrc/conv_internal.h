@@ -165,6 +165,7 @@ struct TcGemmParams {
     int halo_stages;     // kTcModeHalo: halos in flight (stages is then the weight ring)
     int btaps;           // kTcModeHalo: taps per weight stage (one barrier wait feeds btaps x 4 MMAs)
     int bres;            // 1x1 mode: the tile's weights stay in shared memory (loaded once per CTA; the ring carries A only)
+    int swap;            // two tiles per CTA of 128 channels (per-tap modes): weights are the MMA's M operand
     int ps;            // kTcModePhase: the transposed convolution's stride S (phases = S*S)
     int hq, wq;        // kTcModePhase: output rows / columns per phase (H_out / S, W_out / S)
     TcPhaseAxis ph, pw;

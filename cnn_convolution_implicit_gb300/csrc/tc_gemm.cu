@@ -488,7 +488,12 @@ __device__ __forceinline__ void halo_mma(const TcGemmParams& p, const TcSmem& sm
 // is a multiple of the n-tile count), whose weight rows for the whole reduction load
 // once into shared memory; the ring carries pixels only and the MMA issuer waits on
 // A (halo) stages alone.
-template <bool PAIR, bool PHASE, bool DUAL, bool HALO = false, bool RESB = false>
+// SWAP: two tiles per CTA of 128 output channels (per-tap modes): the weights are the
+// MMA's M = 128 operand and both tiles' 256 pixels its N, so one M128 N256 MMA per K = 16
+// reads 12 KB of operands where two M128 N128 MMAs read 16 KB (the tensor core reads
+// its shared-memory operands at 128 bytes per clock, which N = 128 MMAs already fill).
+// TMEM then holds D with output channels on the lanes; the epilogue transposes it.
+template <bool PAIR, bool PHASE, bool DUAL, bool HALO = false, bool RESB = false, bool SWAP = false>
 __global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
     tc_conv_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map,
                    const __grid_constant__ CUtensorMap y_map, const TcGemmParams p) {
@@ -519,7 +524,7 @@ __global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
     if (threadIdx.x == 0) {
         // two tiles per CTA: both MMA-issuing threads commit to the barriers that release
         // a stage, a halo, an accumulator or the final drain
-        constexpr uint32_t mma_threads = DUAL ? 2 : 1;
+        constexpr uint32_t mma_threads = (DUAL && !SWAP) ? 2 : 1;
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], mma_threads);
@@ -686,7 +691,7 @@ __global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
             if (RESB && leader && unit0 < num_units && !mbar_wait(sm.bfull, 0, nullptr))
                 record_status(p.status, kStatusTimeoutDrain, abort);
         }
-    } else if (warp == 1 || (DUAL && warp == tc_mma2_warp(false))) {
+    } else if (warp == 1 || (DUAL && !SWAP && warp == tc_mma2_warp(false))) {
         // ------------------------------------------------------------ MMA issuer (leader only)
         // Two tiles per CTA: warp 1 issues tile 0's MMAs and a second warp tile 1's, each
         // waiting for the same stages (one thread issues at most one MMA per ~55 clocks)
@@ -728,7 +733,13 @@ __global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
                         tc_fence_after();
                         const uint64_t adesc = sdesc_sw128(smem_addr(sm.a + stage * a_stage));
                         const uint64_t bdesc = sdesc_sw128(smem_addr(sm.b + (RESB ? ks : stage) * b_bytes));
-                        if (!DUAL || part != 1) {
+                        if constexpr (SWAP) {
+                            // weights (128 rows) x both tiles' pixels (256 rows of the stage's A block)
+                            constexpr uint32_t idesc_sw = idesc_bf16_f32(kTcBlockM, 2 * kTcBlockM);
+#pragma unroll
+                            for (int k = 0; k < kTcBlockK / 16; ++k)
+                                mma_bf16(d, bdesc + 2 * k, adesc + 2 * k, idesc_sw, (ks | k) != 0 ? 1u : 0u);
+                        } else if (!DUAL || part != 1) {
 #pragma unroll
                             for (int k = 0; k < kTcBlockK / 16; ++k) {
                                 // +32 bytes along K inside the swizzle row = +2 in the >>4 address field
@@ -798,81 +809,150 @@ __global__ void __launch_bounds__(tc_threads(HALO, DUAL), 1)
             // DUAL: group half h drains tile h of the unit (all its columns)
             const int m = PAIR ? 2 * mu + static_cast<int>(rank) : (DUAL ? 2 * mu + chalf : mu);
             const PixTile t = pix_tile<PHASE, TWO>(p, m);
-            // this warp's 32 pixels: rect mode = 32/TW rows of the rectangle, else 32 linear pixels
-            bool rows_exist;
-            int yc1, yc2, yc3;
-            if (PHASE) {
-                const int h = t.ho0 + quarter * 32 / p.rect_w;  // phase-grid row
-                rows_exist = t.exists && h < p.hq && t.wo0 < p.wq;
-                yc1 = t.wo0;
-                yc2 = h;
-                yc3 = t.n;
-            } else if (p.mode == kTcModeRect || p.mode == kTcModeHalo) {
-                const int h = t.ho0 + quarter * 32 / p.rect_w;
-                rows_exist = t.exists && h < p.g.H_out && t.wo0 < p.g.W_out;
-                yc1 = t.wo0;
-                yc2 = h;
-                yc3 = t.n;
-            } else {
-                const long long row0 = t.pix0 + quarter * 32;
-                rows_exist = t.exists && row0 < p.g.pixels;
-                yc1 = static_cast<int>(row0);
-                yc2 = yc3 = 0;
-            }
-            const int co0 = nt * p.n_tile;
-            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                   static_cast<uint32_t>(buf * (DUAL ? 2 : 1) * p.n_tile + (DUAL ? chalf * p.n_tile : 0));
-            // this group's half of the columns, 32 per step, one staging tile per warp
-            const int chunks = p.n_tile / 32;
-            const int c_lo = ALLW ? 32 * ((chunks * egroup) / 4)
-                                  : DUAL ? 0 : (chalf == 0 ? 0 : ((chunks + 1) / 2) * 32);
-            const int c_hi = ALLW ? 32 * ((chunks * (egroup + 1)) / 4)
-                                  : DUAL ? p.n_tile : (chalf == 0 ? ((chunks + 1) / 2) * 32 : p.n_tile);
-            for (int c = c_lo; c < c_hi; c += 32) {
-                uint32_t v[32];
-                if constexpr (ALLW) {
-                    __syncwarp();
-                    tmem_ld32(t_row + static_cast<uint32_t>(c), v);
-                    if (lane == 0) bulk_wait_read_all();
-                    tmem_ld_wait(v);
-                    __syncwarp();
-                    stage_row32(v, p.bias ? p.bias + co0 + c : nullptr, p.relu, stg, lane,
-                                p.scale ? p.scale + co0 + c : nullptr);
-                } else {
-                    // lane l loads the scale and shift of channel co0 + c + l before the TMEM
-                    // load, and shuffles hand them round: no global load waits behind the
-                    // accumulator (body with a folded batch norm 145.4 -> 136.8 us, body 136.3 ->
-                    // 134.2, dilated 27.5 -> 26.7; the 1x1 kernel above measured slower this way)
-                    const float sl = p.scale ? __ldg(p.scale + co0 + c + lane) : 1.f;
-                    const float bl = p.bias ? __ldg(p.bias + co0 + c + lane) : 0.f;
-                    __syncwarp();
-                    tmem_ld32(t_row + static_cast<uint32_t>(c), v);
-                    tmem_ld_wait(v);
-                    if (lane == 0) bulk_wait_read_all();
-                    __syncwarp();
-                    if (p.scale) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const float si = __shfl_sync(0xffffffffu, sl, i), bi = __shfl_sync(0xffffffffu, bl, i);
-                            v[i] = __float_as_uint(fmaf(__uint_as_float(v[i]), si, bi));
-                        }
-                    } else if (p.bias) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            v[i] = __float_as_uint(__uint_as_float(v[i]) + __shfl_sync(0xffffffffu, bl, i));
+            if constexpr (SWAP) {
+                // D holds output channels on TMEM lanes and the unit's 256 pixels on columns
+                // (tile h: columns 128h ..): this warp drains channels 32*quarter .. of its tile,
+                // 32 pixels per step; lane pairs swap halves so that each lane writes whole
+                // 32-bit words (two channels of one pixel) into the pixel-major staging tile
+                const int co = nt * p.n_tile + 32 * quarter;  // this warp's first output channel
+                const float bl = p.bias ? __ldg(p.bias + co + lane) : 0.f;
+                const float sl = p.scale ? __ldg(p.scale + co + lane) : 1.f;
+                const uint32_t t_col = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                       static_cast<uint32_t>(buf * 2 * p.n_tile + chalf * p.n_tile);
+                const int odd = lane & 1;
+                for (int cc = 0; cc < kTcBlockM / 32; ++cc) {
+                    bool rows_exist;
+                    int yc1, yc2, yc3;
+                    if (PHASE) {
+                        const int h = t.ho0 + cc * 32 / p.rect_w;
+                        rows_exist = t.exists && h < p.hq && t.wo0 < p.wq;
+                        yc1 = t.wo0;
+                        yc2 = h;
+                        yc3 = t.n;
+                    } else if (p.mode == kTcModeRect || p.mode == kTcModeHalo) {
+                        const int h = t.ho0 + cc * 32 / p.rect_w;
+                        rows_exist = t.exists && h < p.g.H_out && t.wo0 < p.g.W_out;
+                        yc1 = t.wo0;
+                        yc2 = h;
+                        yc3 = t.n;
+                    } else {
+                        const long long row0 = t.pix0 + cc * 32;
+                        rows_exist = t.exists && row0 < p.g.pixels;
+                        yc1 = static_cast<int>(row0);
+                        yc2 = yc3 = 0;
                     }
-                    stage_row32(v, nullptr, p.relu, stg, lane, nullptr);
+                    uint32_t v[32];
+                    __syncwarp();
+                    tmem_ld32(t_col + static_cast<uint32_t>(cc * 32), v);
+                    tmem_ld_wait(v);
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+                    float f[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        f[i] = p.scale ? fmaf(__uint_as_float(v[i]), sl, bl) : __uint_as_float(v[i]) + bl;
+                    // even lane 2k writes pixels 0..15 of channels 2k, 2k+1; odd lane 2k+1 pixels 16..31
+                    const int c2 = (lane & ~1) * 2;  // byte offset of the channel pair in a 64-byte row
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float mine = odd ? f[i + 16] : f[i];
+                        const float send = odd ? f[i] : f[i + 16];
+                        const float other = __shfl_xor_sync(0xffffffffu, send, 1);
+                        const float lo = odd ? other : mine, hi = odd ? mine : other;
+                        const uint32_t w = p.relu ? pack_bf16x2_relu(lo, hi) : pack_bf16x2(lo, hi);
+                        const int r = i + 16 * odd;  // pixel row of the staging tile
+                        const int byte = r * 64 + ((((c2 >> 4) ^ ((r >> 1) & 3)) << 4) | (c2 & 15));
+                        *reinterpret_cast<uint32_t*>(stg + byte) = w;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && rows_exist) {
+                        if (PHASE)
+                            tma_store_5d(&y_map, stg, co, t.rw, yc1, t.rh, yc3 * p.hq + yc2);
+                        else if (p.mode == kTcModeRect || p.mode == kTcModeHalo)
+                            tma_store_4d(&y_map, stg, co, yc1, yc2, yc3);
+                        else
+                            tma_store_2d(&y_map, stg, co, yc1);
+                        bulk_commit();
+                    }
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0 && rows_exist) {
-                    if (PHASE)
-                        tma_store_5d(&y_map, stg, co0 + c, t.rw, yc1, t.rh, yc3 * p.hq + yc2);
-                    else if (p.mode == kTcModeRect || p.mode == kTcModeHalo)
-                        tma_store_4d(&y_map, stg, co0 + c, yc1, yc2, yc3);
-                    else
-                        tma_store_2d(&y_map, stg, co0 + c, yc1);
-                    bulk_commit();
+            } else {
+                // this warp's 32 pixels: rect mode = 32/TW rows of the rectangle, else 32 linear pixels
+                bool rows_exist;
+                int yc1, yc2, yc3;
+                if (PHASE) {
+                    const int h = t.ho0 + quarter * 32 / p.rect_w;  // phase-grid row
+                    rows_exist = t.exists && h < p.hq && t.wo0 < p.wq;
+                    yc1 = t.wo0;
+                    yc2 = h;
+                    yc3 = t.n;
+                } else if (p.mode == kTcModeRect || p.mode == kTcModeHalo) {
+                    const int h = t.ho0 + quarter * 32 / p.rect_w;
+                    rows_exist = t.exists && h < p.g.H_out && t.wo0 < p.g.W_out;
+                    yc1 = t.wo0;
+                    yc2 = h;
+                    yc3 = t.n;
+                } else {
+                    const long long row0 = t.pix0 + quarter * 32;
+                    rows_exist = t.exists && row0 < p.g.pixels;
+                    yc1 = static_cast<int>(row0);
+                    yc2 = yc3 = 0;
+                }
+                const int co0 = nt * p.n_tile;
+                const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                       static_cast<uint32_t>(buf * (DUAL ? 2 : 1) * p.n_tile + (DUAL ? chalf * p.n_tile : 0));
+                // this group's half of the columns, 32 per step, one staging tile per warp
+                const int chunks = p.n_tile / 32;
+                const int c_lo = ALLW ? 32 * ((chunks * egroup) / 4)
+                                      : DUAL ? 0 : (chalf == 0 ? 0 : ((chunks + 1) / 2) * 32);
+                const int c_hi = ALLW ? 32 * ((chunks * (egroup + 1)) / 4)
+                                      : DUAL ? p.n_tile : (chalf == 0 ? ((chunks + 1) / 2) * 32 : p.n_tile);
+                for (int c = c_lo; c < c_hi; c += 32) {
+                    uint32_t v[32];
+                    if constexpr (ALLW) {
+                        __syncwarp();
+                        tmem_ld32(t_row + static_cast<uint32_t>(c), v);
+                        if (lane == 0) bulk_wait_read_all();
+                        tmem_ld_wait(v);
+                        __syncwarp();
+                        stage_row32(v, p.bias ? p.bias + co0 + c : nullptr, p.relu, stg, lane,
+                                    p.scale ? p.scale + co0 + c : nullptr);
+                    } else {
+                        // lane l loads the scale and shift of channel co0 + c + l before the TMEM
+                        // load, and shuffles hand them round: no global load waits behind the
+                        // accumulator (body with a folded batch norm 145.4 -> 136.8 us, body 136.3 ->
+                        // 134.2, dilated 27.5 -> 26.7; the 1x1 kernel above measured slower this way)
+                        const float sl = p.scale ? __ldg(p.scale + co0 + c + lane) : 1.f;
+                        const float bl = p.bias ? __ldg(p.bias + co0 + c + lane) : 0.f;
+                        __syncwarp();
+                        tmem_ld32(t_row + static_cast<uint32_t>(c), v);
+                        tmem_ld_wait(v);
+                        if (lane == 0) bulk_wait_read_all();
+                        __syncwarp();
+                        if (p.scale) {
+    #pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const float si = __shfl_sync(0xffffffffu, sl, i), bi = __shfl_sync(0xffffffffu, bl, i);
+                                v[i] = __float_as_uint(fmaf(__uint_as_float(v[i]), si, bi));
+                            }
+                        } else if (p.bias) {
+    #pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                v[i] = __float_as_uint(__uint_as_float(v[i]) + __shfl_sync(0xffffffffu, bl, i));
+                        }
+                        stage_row32(v, nullptr, p.relu, stg, lane, nullptr);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && rows_exist) {
+                        if (PHASE)
+                            tma_store_5d(&y_map, stg, co0 + c, t.rw, yc1, t.rh, yc3 * p.hq + yc2);
+                        else if (p.mode == kTcModeRect || p.mode == kTcModeHalo)
+                            tma_store_4d(&y_map, stg, co0 + c, yc1, yc2, yc3);
+                        else
+                            tma_store_2d(&y_map, stg, co0 + c, yc1);
+                        bulk_commit();
+                    }
                 }
             }
             tmem_ld_wait();
@@ -906,11 +986,11 @@ static SmemLimitCache g_pair_smem_limits;
 namespace {
 
 // Launch one instantiation: clusters of two CTAs for SM pairs, else plain.
-template <bool PAIR, bool PHASE, bool DUAL, bool HALO, bool RESB = false>
+template <bool PAIR, bool PHASE, bool DUAL, bool HALO, bool RESB = false, bool SWAP = false>
 cudaError_t launch_one(const CUtensorMap& a_map, const CUtensorMap& b_map, const CUtensorMap& y_map,
                        const TcGemmParams& p, int grid, cudaStream_t stream) {
     static SmemLimitCache limits;
-    auto* fn = tc_conv_kernel<PAIR, PHASE, DUAL, HALO, RESB>;
+    auto* fn = tc_conv_kernel<PAIR, PHASE, DUAL, HALO, RESB, SWAP>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fn), p.smem_bytes, limits);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -971,6 +1051,10 @@ cudaError_t launch_tc_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, c
                                    : cudaLaunchKernelEx(&cfg, tc_conv_kernel<true, false, false>, a_map, b_map, y_map, p);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
+    }
+    if (p.dual && p.swap) {  // two pixel tiles per CTA, weights as the M operand
+        if (p.mode == kTcModePhase) return launch_one<false, true, true, false, false, true>(a_map, b_map, y_map, p, grid, stream);
+        return launch_one<false, false, true, false, false, true>(a_map, b_map, y_map, p, grid, stream);
     }
     if (p.dual) {  // two pixel tiles per CTA
         static SmemLimitCache dual_limits, dual_phase_limits;

@@ -250,12 +250,15 @@ conv_status conv_plan_launch_info(const conv_plan *p, int *grid, int *block, int
  *   dual              1: two pixel tiles per CTA;
  *   resident_weights  1: every CTA keeps one n-tile, and that n-tile's weight rows for the
  *                     whole reduction sit in shared memory from its first tile on (loaded
- *                     once instead of once per tile).
+ *                     once instead of once per tile);
+ *   swapped           1: two tiles per CTA of 128 output channels with the operands swapped:
+ *                     the weights are the MMA's M side and both tiles' 256 pixels its N
+ *                     side (one M128 N256 MMA per K = 16 instead of two M128 N128).
  * Any output pointer may be NULL.  Returns CONV_ERR_INVALID_ARG for a NULL plan or one on
  * another path.
  */
 conv_status conv_plan_gemm_config(const conv_plan *p, int *mode, int *n_tile, int *pair, int *dual,
-                                  int *resident_weights);
+                                  int *resident_weights, int *swapped);
 
 /* ------------------------------------------------------------------------
  * Depthwise-separable block in one kernel: depthwise 3x3 (FP32) followed by

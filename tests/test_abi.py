@@ -313,7 +313,25 @@ def test_gemm_config_other_paths():
     """conv_plan_gemm_config answers for the tensor-core GEMM paths only."""
     p = cg.ConvPlan(2, 64, 9, 9, 64, 3, 3, 1, 1, 1, 64, dtype="f32", bias=True, relu=True)
     assert p.path == "depthwise" and p.gemm is None
-    assert cg.lib().conv_plan_gemm_config(None, None, None, None, None, None) == 1
+    assert cg.lib().conv_plan_gemm_config(None, None, None, None, None, None, None) == 1
+
+
+# Swapped operands (weights on the MMA's M side, both tiles' pixels on N) for two-tile units of
+# exactly 128 output channels in the per-tap modes; never in the halo mode or at other widths.
+@pytest.mark.parametrize("shape,flags,swapped", [
+    ((16, 256, 56, 56, 128, 4, 4, 2, 1, 1, 1), {"transposed": True}, 1),  # transposed upsampling (phase mode)
+    ((4, 128, 29, 23, 128, 3, 3, 2, 1, 1, 1), {}, 1),                      # strided (im2col mode)
+    ((2, 256, 9, 13, 128, 1, 1, 1, 0, 1, 1), {}, 1),                       # 1x1, two tiles per CTA
+    ((2, 64, 13, 11, 128, 3, 3, 1, 1, 1, 1), {"per_tap": True}, 1),        # one box per tap
+    ((2, 64, 13, 11, 128, 3, 3, 1, 1, 1, 1), {}, 0),                       # halo mode
+    ((16, 256, 64, 64, 256, 3, 3, 1, 2, 2, 4), {}, 0),                     # 64-channel groups
+    ((2, 128, 13, 11, 64, 3, 3, 2, 1, 1, 1), {}, 0),                       # 64 channels
+])
+def test_swapped_operand_choice(shape, flags, swapped):
+    p = cg.ConvPlan(*shape, dtype="bf16", bias=True, relu=True, **flags)
+    assert p.gemm["swapped"] == swapped
+    if swapped:
+        assert p.gemm["dual"] == 1 and p.gemm["n_tile"] == 128
 
 
 def test_wait_timeout_check_rejects_bad_arguments_without_launching():

@@ -201,6 +201,26 @@ def test_resident_weights_full(shape, sm_pairs):
     check_full(shape, y, oracle_full(shape, x, w, b))
 
 
+# Swapped operands: two tiles per CTA of 128 output channels, the weights on the MMA's M side and
+# both tiles' 256 pixels on N; the epilogue transposes D (channels on TMEM lanes) back to NHWC.
+SWAPPED_SHAPES = [
+    (ConvShape(4, 128, 29, 23, 128, 3, 3, 2, 1, 1, 1, "bf16", True, True), {}),             # im2col mode
+    (ConvShape(3, 256, 9, 13, 128, 1, 1, 1, 0, 1, 1, "bf16", True, False), {}),             # 1x1 mode
+    (ConvShape(2, 64, 13, 11, 128, 3, 3, 1, 1, 1, 1, "bf16", False, True), {"per_tap": True}),  # one box per tap
+    (ConvShape(2, 256, 19, 17, 256, 3, 3, 2, 1, 1, 2, "bf16", True, True), {}),             # two groups of 128
+]
+
+
+@pytest.mark.parametrize("shape,kw", SWAPPED_SHAPES, ids=["im2col", "1x1", "per_tap", "groups"])
+def test_swapped_operands_full(shape, kw):
+    """Every output of plans whose weights are the MMA's M operand."""
+    from cnn_convolution_implicit_gb300 import ConvPlan
+    x, w, b = draw(shape, (81, 82, 83))
+    plan, y = run(shape, x, w, b, plan=ConvPlan.for_shape(shape, **kw))
+    assert plan.gemm["swapped"] == 1
+    check_full(shape, y, oracle_full(shape, x, w, b))
+
+
 def test_halo_mode_random_sweep():
     """Random stride-1 BF16 shapes in the halo mode (kernel sizes 1-5 per axis, dilation
     1-3, padding, groups, ragged 8 x 16 tiles, widths that leave a lone right-hand tile of

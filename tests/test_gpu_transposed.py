@@ -90,3 +90,18 @@ def test_upsample_full_size():
     assert device_status() == 0
     ref = oracle.conv_transpose2d(x, w, b, s.S, s.P, s.D, s.G, s.relu)
     check_full(s, y, ref)
+
+
+@pytest.mark.parametrize("case,scale", [
+    ((2, 128, 7, 9, 128, 4, 2, 1, 1, 1, "bf16", True, True, "implicit_gemm"), False),
+    ((3, 64, 11, 13, 128, 4, 2, 1, 1, 1, "bf16", True, False, "implicit_gemm"), True),
+    ((2, 256, 6, 6, 128, 3, 3, 0, 1, 1, "bf16", False, True, "implicit_gemm"), False),
+], ids=["K4S2", "K4S2_affine_ragged", "K3S3"])
+def test_transposed_swapped_operands(case, scale):
+    """Two phase tiles of 128 output channels per CTA with the weights as the MMA's M operand
+    and both tiles' pixels as N (D transposed in TMEM, transposed again by the epilogue)."""
+    from cnn_convolution_implicit_gb300 import ConvPlan
+    N, C_in, H, W, C_out, K, S, P, D, G, dtype, bias, relu, path = case
+    s = ConvShape(N, C_in, H, W, C_out, K, K, S, P, D, G, dtype, bias, relu, transposed=True)
+    assert ConvPlan.for_shape(s).gemm["swapped"] == 1
+    _run_case(case, 8400 + H, scale=scale)
