@@ -27,7 +27,7 @@ EXPORTS = ("conv_plan_create", "conv_plan_output_shape", "conv_plan_info", "conv
            "conv_plan_launch_info", "conv_forward_affine", "conv_block_plan_create",
            "conv_block_plan_output_shape", "conv_block_forward", "conv_block_plan_launch_info",
            "conv_block_plan_destroy", "conv_measure_mma_rate", "conv_check_wait_timeout",
-           "conv_plan_gemm_config")
+           "conv_plan_gemm_config", "conv_plan_device_status", "conv_block_plan_device_status")
 CONV_BLOCK_DW_RELU, CONV_BLOCK_PW_RELU = 1, 2
 
 _lock = threading.Lock()
@@ -80,6 +80,10 @@ def lib():
             L.conv_plan_launch_info.restype = c_int
             L.conv_plan_gemm_config.argtypes = [vp] + [ctypes.POINTER(c_int)] * 6
             L.conv_plan_gemm_config.restype = c_int
+            L.conv_plan_device_status.argtypes = [vp, vp, ctypes.POINTER(c_int)]
+            L.conv_plan_device_status.restype = c_int
+            L.conv_block_plan_device_status.argtypes = [vp, vp, ctypes.POINTER(c_int)]
+            L.conv_block_plan_device_status.restype = c_int
             L.conv_block_plan_create.argtypes = [ctypes.POINTER(vp)] + [c_int] * 7 + [ctypes.c_uint]
             L.conv_block_plan_create.restype = c_int
             L.conv_block_plan_output_shape.argtypes = [vp, ctypes.POINTER(c_int), ctypes.POINTER(c_int)]
@@ -104,6 +108,17 @@ def device_status() -> int:
     st = lib().conv_device_status(ctypes.byref(code))
     if st not in (0, 6):
         raise ConvError(st, "conv_device_status")
+    return code.value
+
+
+def _plan_status(fn, plan, stream, name) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    code = ctypes.c_int(0)
+    st = fn(plan, ctypes.c_void_p(stream.cuda_stream), ctypes.byref(code))
+    if st not in (0, 6):
+        raise ConvError(st, name)
     return code.value
 
 
@@ -227,6 +242,11 @@ class ConvPlan:
 
     __call__ = forward
 
+    def device_status(self, stream=None) -> int:
+        """Read and clear the plan's own status word after the work queued on ``stream``
+        (default: torch's current stream); waits for that stream only.  0 = clean."""
+        return _plan_status(lib().conv_plan_device_status, self._plan, stream, "conv_plan_device_status")
+
 
 class BlockPlan:
     """Fused depthwise-separable block: depthwise 3x3 (FP32) -> BF16 -> pointwise 1x1
@@ -303,6 +323,11 @@ class BlockPlan:
         return y
 
     __call__ = forward
+
+    def device_status(self, stream=None) -> int:
+        """The block plan's own status word, as ConvPlan.device_status."""
+        return _plan_status(lib().conv_block_plan_device_status, self._plan, stream,
+                            "conv_block_plan_device_status")
 
 
 _plan_cache = {}

@@ -9,12 +9,14 @@
 
 #include "../../include/conv.h"
 #include "conv_internal.h"
+#include "status_slots.h"
 
 using namespace convgb;
 
 struct conv_block_plan {
     BlockParams bp;
     int device;
+    int status_slot;  // index of the plan's own status word, -1: the library-wide word
     int num_sms;
     int grid;
     const void* cache_x;
@@ -120,11 +122,12 @@ conv_status conv_block_plan_create(conv_block_plan** out, int N, int C, int H, i
         pl->device = -1;
         pl->num_sms = 152;
         b.status = nullptr;
-    } else if (cudaGetDevice(&pl->device) != cudaSuccess ||
+        pl->status_slot = -1;
+    } else if ((pl->status_slot = -1, cudaGetDevice(&pl->device)) != cudaSuccess ||
                cudaDeviceGetAttribute(&pl->num_sms, cudaDevAttrMultiProcessorCount, pl->device) != cudaSuccess ||
                cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, pl->device) !=
                    cudaSuccess ||
-               device_status_word(&b.status) != cudaSuccess) {
+               acquire_status_word(pl->device, &b.status, &pl->status_slot) != cudaSuccess) {
         cudaGetLastError();
         delete pl;
         return CONV_ERR_CUDA;
@@ -139,6 +142,7 @@ conv_status conv_block_plan_create(conv_block_plan** out, int N, int C, int H, i
                 break;
             }
     if (b.halo_stages == 0) {
+        release_status_word(pl->device, pl->status_slot);
         delete pl;
         return CONV_ERR_UNSUPPORTED;
     }
@@ -196,7 +200,15 @@ conv_status conv_block_forward(conv_block_plan* p, const void* x, const void* w_
     return CONV_OK;
 }
 
+conv_status conv_block_plan_device_status(const conv_block_plan* p, void* stream, int* code) {
+    if (p == nullptr || code == nullptr) return CONV_ERR_INVALID_ARG;
+    *code = 0;
+    if (p->device < 0) return CONV_ERR_CUDA;  // host-only plan
+    return read_status_word(p->device, p->bp.status, stream, code);
+}
+
 conv_status conv_block_plan_destroy(conv_block_plan* p) {
+    if (p != nullptr) release_status_word(p->device, p->status_slot);
     delete p;
     return CONV_OK;
 }

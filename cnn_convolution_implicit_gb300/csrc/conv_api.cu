@@ -24,11 +24,57 @@
 
 #include "../../include/conv.h"
 #include "conv_internal.h"
+#include "status_slots.h"
 
 using namespace convgb;
 
 // Device status word: bits latched by kernels whose bounded waits gave up.
 __device__ unsigned int g_conv_status_word;
+
+// Per-plan status words (status_slots.h): a fixed array per device, taken and given
+// back on the host under a lock.
+constexpr int kStatusSlots = 1024;
+constexpr int kMaxStatusDevices = 64;
+__device__ unsigned int g_conv_status_slots[kStatusSlots];
+
+namespace convgb {
+namespace {
+std::mutex g_slot_mutex;
+bool g_slot_used[kMaxStatusDevices][kStatusSlots];
+}  // namespace
+
+cudaError_t acquire_status_word(int device, unsigned** word, int* slot) {
+    *slot = -1;
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(word), g_conv_status_word);
+    if (e != cudaSuccess || device < 0 || device >= kMaxStatusDevices) return e;
+    int idx = -1;
+    {
+        std::lock_guard<std::mutex> lock(g_slot_mutex);
+        for (int i = 0; i < kStatusSlots && idx < 0; ++i)
+            if (!g_slot_used[device][i]) {
+                g_slot_used[device][i] = true;
+                idx = i;
+            }
+    }
+    if (idx < 0) return cudaSuccess;  // every word is taken: share the library-wide one
+    unsigned* base = nullptr;
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&base), g_conv_status_slots);
+    if (e == cudaSuccess) e = cudaMemset(base + idx, 0, sizeof(unsigned));  // a previous owner's bits
+    if (e != cudaSuccess) {
+        release_status_word(device, idx);
+        return e;
+    }
+    *word = base + idx;
+    *slot = idx;
+    return cudaSuccess;
+}
+
+void release_status_word(int device, int slot) {
+    if (slot < 0 || device < 0 || device >= kMaxStatusDevices) return;
+    std::lock_guard<std::mutex> lock(g_slot_mutex);
+    g_slot_used[device][slot] = false;
+}
+}  // namespace convgb
 
 struct conv_plan {
     ConvGeom g;
@@ -41,6 +87,7 @@ struct conv_plan {
     int smem_per_sm;
     int pair_clusters;  // co-resident 2-CTA clusters of the pair kernel (0: unknown)
     unsigned* status;
+    int status_slot;    // index of the plan's own status word, -1: the library-wide word
     // per-path configuration
     TcGemmParams tc;
     SmallKParams sk;
@@ -599,6 +646,30 @@ cudaError_t device_status_word(unsigned** word) {
     return cudaGetSymbolAddress(reinterpret_cast<void**>(word), g_conv_status_word);
 }
 
+conv_status read_status_word(int device, unsigned* word, void* stream, int* code) {
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return CONV_ERR_CUDA;
+    }
+    if (cur != device) return CONV_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned v = 0;
+    // after everything queued on the stream before this call
+    if (cudaMemcpyAsync(&v, word, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaGetLastError();
+        return CONV_ERR_CUDA;
+    }
+    if (v != 0 && (cudaMemsetAsync(word, 0, sizeof(unsigned), st) != cudaSuccess ||
+                   cudaStreamSynchronize(st) != cudaSuccess)) {
+        cudaGetLastError();
+        return CONV_ERR_CUDA;
+    }
+    *code = static_cast<int>(v);
+    return v ? CONV_ERR_TIMEOUT : CONV_OK;
+}
+
 }  // namespace convgb
 
 extern "C" {
@@ -645,13 +716,14 @@ conv_status conv_plan_create(conv_plan** out, int N, int C_in, int H, int W, int
         pl->smem_optin = 232448;
         pl->smem_per_sm = 233472;
         pl->status = nullptr;
-    } else if (cudaGetDevice(&pl->device) != cudaSuccess ||
+        pl->status_slot = -1;
+    } else if ((pl->status_slot = -1, cudaGetDevice(&pl->device)) != cudaSuccess ||
                cudaDeviceGetAttribute(&pl->num_sms, cudaDevAttrMultiProcessorCount, pl->device) != cudaSuccess ||
                cudaDeviceGetAttribute(&pl->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, pl->device) !=
                    cudaSuccess ||
                cudaDeviceGetAttribute(&pl->smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, pl->device) !=
                    cudaSuccess ||
-               cudaGetSymbolAddress(reinterpret_cast<void**>(&pl->status), g_conv_status_word) != cudaSuccess) {
+               acquire_status_word(pl->device, &pl->status, &pl->status_slot) != cudaSuccess) {
         cudaGetLastError();
         delete pl;
         return CONV_ERR_CUDA;
@@ -905,8 +977,16 @@ conv_status forward_impl(conv_plan* p, const void* x, const void* w, const float
 extern "C" {
 
 conv_status conv_plan_destroy(conv_plan* p) {
+    if (p != nullptr) release_status_word(p->device, p->status_slot);
     delete p;
     return CONV_OK;
+}
+
+conv_status conv_plan_device_status(const conv_plan* p, void* stream, int* code) {
+    if (p == nullptr || code == nullptr) return CONV_ERR_INVALID_ARG;
+    *code = 0;
+    if (p->device < 0) return CONV_ERR_CUDA;  // host-only plan
+    return read_status_word(p->device, p->status, stream, code);
 }
 
 const char* conv_status_string(conv_status s) {
@@ -926,14 +1006,25 @@ conv_status conv_device_status(int* code) {
     if (code == nullptr) return CONV_ERR_INVALID_ARG;
     *code = 0;
     if (cudaDeviceSynchronize() != cudaSuccess) return CONV_ERR_CUDA;
+    // the library-wide word and every plan's own word
+    static unsigned words[kStatusSlots];  // guarded: conv_device_status may run on several threads
+    static std::mutex words_mutex;
+    std::lock_guard<std::mutex> lock(words_mutex);
     unsigned v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_conv_status_word, sizeof(v)) != cudaSuccess) return CONV_ERR_CUDA;
-    if (v != 0) {
+    if (cudaMemcpyFromSymbol(&v, g_conv_status_word, sizeof(v)) != cudaSuccess ||
+        cudaMemcpyFromSymbol(words, g_conv_status_slots, sizeof(words)) != cudaSuccess)
+        return CONV_ERR_CUDA;
+    unsigned any = v;
+    for (int i = 0; i < kStatusSlots; ++i) any |= words[i];
+    if (any != 0) {
         const unsigned zero = 0;
-        if (cudaMemcpyToSymbol(g_conv_status_word, &zero, sizeof(zero)) != cudaSuccess) return CONV_ERR_CUDA;
+        for (int i = 0; i < kStatusSlots; ++i) words[i] = 0;
+        if (cudaMemcpyToSymbol(g_conv_status_word, &zero, sizeof(zero)) != cudaSuccess ||
+            cudaMemcpyToSymbol(g_conv_status_slots, words, sizeof(words)) != cudaSuccess)
+            return CONV_ERR_CUDA;
     }
-    *code = static_cast<int>(v);
-    return v ? CONV_ERR_TIMEOUT : CONV_OK;
+    *code = static_cast<int>(any);
+    return any ? CONV_ERR_TIMEOUT : CONV_OK;
 }
 
 }  // extern "C"

@@ -37,7 +37,8 @@
  * Errors: every call returns a conv_status; no call prints, traps or aborts.
  * conv_forward is asynchronous on the given stream and never synchronises;
  * device-side wait timeouts (a safety net that fires only on a hang) are
- * latched in a device word read by conv_device_status.
+ * latched in the plan's own device word, read by conv_plan_device_status (one
+ * plan, in stream order) and by conv_device_status (every word, whole device).
  */
 #ifndef CONV_GB300_CONV_H
 #define CONV_GB300_CONV_H
@@ -179,21 +180,37 @@ conv_status conv_forward(conv_plan *p, const void *x, const void *w, const void 
 conv_status conv_forward_affine(conv_plan *p, const void *x, const void *w, const void *scale,
                                 const void *bias, void *y, void *stream);
 
-/* Free the plan (host memory only).  NULL is accepted. */
+/* Free the plan (host memory; its status word goes back to the pool).  Launches
+ * still in flight keep running; a wait of theirs that gives up after this call may
+ * latch its bit into the word's next owner.  NULL is accepted. */
 conv_status conv_plan_destroy(conv_plan *p);
 
 /* Static English text for a status code; never NULL. */
 const char *conv_status_string(conv_status s);
 
 /*
- * Synchronise the current device, then read and clear the library's device
- * status word for it.  *code receives 0 when no kernel hit a wait timeout
- * since the last call, else a non-zero bit set naming the waits that gave up.
- * Returns CONV_ERR_TIMEOUT when *code != 0, CONV_ERR_CUDA if the
- * synchronisation or read fails (a sticky fault from an earlier launch shows
- * up here), else CONV_OK.
+ * Synchronise the current device, then read and clear every status word the
+ * library keeps on it: the library-wide word and every plan's own word (below).
+ * *code receives 0 when no kernel hit a wait timeout since the last call, else
+ * the OR of the bit sets naming the waits that gave up.  Returns
+ * CONV_ERR_TIMEOUT when *code != 0, CONV_ERR_CUDA if the synchronisation or
+ * read fails (a sticky fault from an earlier launch shows up here), else CONV_OK.
  */
 conv_status conv_device_status(int *code);
+
+/*
+ * Each plan (conv_plan and conv_block_plan) takes its own device status word at
+ * creation, from a fixed array of 1,024 per device (no allocation: creation clears
+ * the word with a memset on the default stream); when all are taken it shares the
+ * library-wide word.  This reads and clears the plan's word in the order of
+ * `stream` (after the work queued on it, then waits for the stream only, not the
+ * device): *code receives the bits of the plan's kernels whose waits gave up.
+ * Returns CONV_ERR_TIMEOUT when *code != 0, CONV_ERR_INVALID_ARG for NULL
+ * arguments or with another device current than the plan's, CONV_ERR_CUDA for a
+ * host-only plan or a failed copy.  A plan used on several streams at once should
+ * be read after all of them (the word is shared by its launches).
+ */
+conv_status conv_plan_device_status(const conv_plan *p, void *stream, int *code);
 
 /* Number of SMs the plan's grid sizing uses (device property of the plan's device). */
 int conv_plan_num_sms(const conv_plan *p);
@@ -329,7 +346,11 @@ conv_status conv_block_forward(conv_block_plan *p, const void *x, const void *w_
 conv_status conv_block_plan_launch_info(const conv_block_plan *p, int *grid, int *block,
                                         int *smem_bytes, int *halo_stages, int *weight_stages);
 
-/* Free the block plan (host memory only).  NULL is accepted. */
+/* The block plan's own status word, read and cleared in the order of `stream`:
+ * the same contract as conv_plan_device_status. */
+conv_status conv_block_plan_device_status(const conv_block_plan *p, void *stream, int *code);
+
+/* Free the block plan: the same contract as conv_plan_destroy.  NULL is accepted. */
 conv_status conv_block_plan_destroy(conv_block_plan *p);
 
 #ifdef __cplusplus

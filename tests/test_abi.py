@@ -344,3 +344,22 @@ def test_wait_timeout_check_rejects_bad_arguments_without_launching():
     import torch
     if not torch.cuda.is_available():
         assert L.conv_check_wait_timeout(1_000_000, None, None) == 4
+
+
+def test_plan_status_words_validate_arguments():
+    """conv_plan_device_status / conv_block_plan_device_status reject NULL arguments; a
+    host-only plan (no device at creation) has no word of its own and fails loudly."""
+    L = cg.lib()
+    code = ctypes.c_int(7)
+    assert L.conv_plan_device_status(None, None, ctypes.byref(code)) == 1
+    assert L.conv_block_plan_device_status(None, None, ctypes.byref(code)) == 1
+    p = cg.ConvPlan(1, 8, 8, 8, 8, 3, 3, 1, 1, 1, 1, "f32")
+    b = cg.BlockPlan(1, 64, 8, 8, 32, 3, 1)
+    assert L.conv_plan_device_status(p._plan, None, None) == 1
+    assert L.conv_block_plan_device_status(b._plan, None, None) == 1
+    if not torch.cuda.is_available():
+        assert L.conv_plan_device_status(p._plan, None, ctypes.byref(code)) == 4
+        assert code.value == 0
+        code.value = 7
+        assert L.conv_block_plan_device_status(b._plan, None, ctypes.byref(code)) == 4
+        assert code.value == 0

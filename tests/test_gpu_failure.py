@@ -5,7 +5,7 @@ import pytest
 import torch
 
 from parity import check_full, oracle_full, run
-from workloads import ConvShape, draw
+from workloads import ConvShape, b_device, draw, w_device, x_device
 
 pytestmark = pytest.mark.gpu
 
@@ -26,3 +26,35 @@ def test_wait_gives_up_reports_and_context_survives(limit_ns):
     x, w, b = draw(s, (71, 72, 73))
     _, y = run(s, x, w, b, plan=ConvPlan.for_shape(s))
     check_full(s, y, oracle_full(s, x, w, b))
+
+
+def test_plan_status_words_attribute_timeouts():
+    """Each plan reads only its own status word, in the order of one stream.  A plan made
+    after all 1,024 words are taken shares the library-wide word, which is where the
+    wait-timeout check latches its bits: that plan reports them (and clears them), a plan
+    with its own word stays clean, and conv_device_status then finds nothing left."""
+    import ctypes
+    from cnn_convolution_implicit_gb300 import ConvPlan, device_status, lib
+    assert device_status() == 0
+    s = ConvShape(2, 128, 13, 11, 256, 3, 3, 1, 1, 1, 1, "bf16", True, True)
+    x, w, b = draw(s, (81, 82, 83))
+    own = ConvPlan.for_shape(s)
+    xd, wd, bd = x_device(x, s.dtype), w_device(w, s.dtype), b_device(b)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        y = own.forward(xd, wd, bd)
+    assert own.device_status(side) == 0           # after the forward, in the side stream's order
+    check_full(s, y, oracle_full(s, x, w, b))
+    plans = [ConvPlan(1, 8, 8, 8, 8, 3, 3, 1, 1, 1, 1, "bf16") for _ in range(1025)]
+    shared = plans[-1]                            # at least 1,025 plans alive: no word left
+    L = lib()
+    elapsed = torch.zeros(1, dtype=torch.int64, device="cuda")
+    stream = torch.cuda.current_stream()
+    assert L.conv_check_wait_timeout(1_000_000, ctypes.c_void_p(elapsed.data_ptr()),
+                                     ctypes.c_void_p(stream.cuda_stream)) == 0
+    assert own.device_status() == 0
+    assert shared.device_status() == 2 | 4        # read after the check in stream order
+    assert shared.device_status() == 0            # and cleared
+    assert device_status() == 0
+    del plans, shared
