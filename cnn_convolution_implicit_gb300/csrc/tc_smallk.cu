@@ -300,13 +300,33 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         // input copies are in flight.  Weights: row co = w[co][0..ktot), zero beyond
         // ktot, swizzled.
         const int t0 = threadIdx.x - 32, nt = kSkThreads - 32;
+        // every global load of a round is issued before its stores (one memory latency per round)
+        const bool has_c = t0 < p.g.C_out;  // C_out <= 256 < nt: one channel per thread
+        float bias_v = 0.f, scale_v = 1.f;
+        if (has_c) {
+            if (p.bias) bias_v = p.bias[t0];
+            if (p.scale) scale_v = p.scale[t0];
+        }
         const uint16_t* w16 = reinterpret_cast<const uint16_t*>(p.w);
         const int kw = p.a_row_bytes / 2;
-        for (int idx = t0; idx < p.g.C_out * kw; idx += nt) {
-            const int co = idx / kw;
-            const int k = idx - co * kw;
-            const uint16_t v = k < p.ktot ? w16[static_cast<long long>(co) * p.ktot + k] : uint16_t(0);
-            *reinterpret_cast<uint16_t*>(sm.b + sw_offset(co, k, p.a_row_bytes)) = v;
+        const int wtotal = p.g.C_out * kw;
+        for (int base = t0; base < wtotal; base += 4 * nt) {
+            uint16_t v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int idx = base + u * nt;
+                const int co = idx / kw;
+                const int k = idx - co * kw;
+                v[u] = (idx < wtotal && k < p.ktot) ? w16[static_cast<long long>(co) * p.ktot + k] : uint16_t(0);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int idx = base + u * nt;
+                if (idx < wtotal) {
+                    const int co = idx / kw;
+                    *reinterpret_cast<uint16_t*>(sm.b + sw_offset(co, idx - co * kw, p.a_row_bytes)) = v[u];
+                }
+            }
         }
         fence_proxy_async_smem();
         // K index -> (kh, kw, ci) decomposition, once per CTA (no divisions in the gather loop)
@@ -323,9 +343,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 sm.tab_kh[k] = -1;
             }
         }
-        for (int c = t0; c < p.g.C_out; c += nt) {
-            sm.bias[c] = p.bias ? p.bias[c] : 0.f;
-            sm.scale[c] = p.scale ? p.scale[c] : 1.f;
+        if (has_c) {
+            sm.bias[t0] = bias_v;
+            sm.scale[t0] = scale_v;
         }
         mbar_arrive(sm.ready);
         if (!mbar_wait(sm.ready, 0, abort)) record_status(p.status, kStatusTimeoutTransform, abort);
@@ -339,6 +359,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             long long issued = 0;
             const char* xb = reinterpret_cast<const char*>(p.x);
             SkStageWalk walk(p);
+            // One segment per output row and whole images per stage: a stage is R consecutive
+            // rows of one image, and its input rows are one run in closed form.
+            const bool whole_rows = p.segs == 1 && p.row_runs && p.g.H_out % R == 0;
             for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
                 if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
                     record_status(p.status, kStatusTimeoutProducer, abort);
@@ -347,12 +370,26 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 // segment info for the transform warps, then one copy per run of rows; the
                 // stage's arrival comes last, after every copy's bytes are expected
                 uint8_t* dst = sm.raw + stage * p.raw_bytes;
-                stage_rows(p, tile, walk.t, sm.seg_info + stage * kSkMaxRows, [&](int n, int row, int rows, int raw_row) {
+                auto emit = [&](int n, int row, int rows, int raw_row) {
                     const uint32_t bytes = static_cast<uint32_t>(rows * p.row_bytes);
                     mbar_expect_tx(&sm.raw_full[stage], bytes);
                     bulk_load(dst + raw_row * p.row_bytes, xb + (static_cast<long long>(n) * p.g.H + row) * p.row_bytes,
                               bytes, &sm.raw_full[stage]);
-                });
+                };
+                if (whole_rows) {
+                    const int top0 = walk.t.ho * p.g.S - p.g.P;  // input row of kernel row 0, first row
+                    const int lo = max(top0, 0);
+                    const int hi = min(top0 + (R - 1) * p.g.S + p.g.Kh - 1, p.g.H - 1);
+                    int4* info = sm.seg_info + stage * kSkMaxRows;
+                    for (int j = 0; j < R; ++j) {
+                        const int top = top0 + j * p.g.S;
+                        const int kh_lo = max(0, -top), kh_hi = min(p.g.Kh - 1, p.g.H - 1 - top);
+                        info[j] = make_int4(kh_lo <= kh_hi ? top - lo : 0, kh_lo | (kh_hi << 8), -p.g.P, p.g.W_out);
+                    }
+                    if (hi >= lo) emit(walk.t.n, lo, hi - lo + 1, 0);
+                } else {
+                    stage_rows(p, tile, walk.t, sm.seg_info + stage * kSkMaxRows, emit);
+                }
                 mbar_arrive(&sm.raw_full[stage]);
                 walk.next(p);
                 ++issued;
@@ -372,6 +409,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(128, n_tile);
             const uint64_t bdesc = a_desc(p, smem_addr(sm.b));
+            // descriptor of A tile 0; tile i starts a_tile_bytes * i further (address field in 16-byte units)
+            const uint64_t adesc0 = a_desc(p, smem_addr(sm.a));
+            const uint32_t tile16 = a_tile_bytes(p) >> 4;
             int stage = 0;
             uint32_t phase = 0;
             int local = 0;
@@ -385,12 +425,12 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 tc_fence_after();
                 const int rows = min(R, p.num_segments - tile * R);
                 // K slices outer, segments inner: consecutive MMAs go to independent accumulators
+                const uint64_t adesc_s = adesc0 + static_cast<uint64_t>(stage * R) * tile16;
+                const uint32_t d_s = tmem_base + static_cast<uint32_t>(buf * R * n_tile);
                 for (int k = 0; k < p.kmma; ++k)
-                    for (int j = 0; j < rows; ++j) {
-                        const uint64_t adesc = a_desc(p, smem_addr(sm.a + (stage * R + j) * a_tile_bytes(p)));
-                        const uint32_t d = tmem_base + static_cast<uint32_t>((buf * R + j) * n_tile);
-                        mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, k != 0 ? 1u : 0u);
-                    }
+                    for (int j = 0; j < rows; ++j)
+                        mma_bf16(d_s + static_cast<uint32_t>(j * n_tile), adesc_s + static_cast<uint64_t>(j) * tile16 + 2 * k,
+                                 bdesc + 2 * k, idesc, k != 0 ? 1u : 0u);
                 mma_commit(&sm.empty[stage]);
                 mma_commit(&sm.tfull[buf]);
                 if (++stage == p.stages) {

@@ -42,6 +42,10 @@ pytestmark = pytest.mark.gpu
     (ConvShape(1, 3, 2, 16, 32, 3, 3, 1, 3, 1, 1, "bf16", True, False), "small_k_gemm"),      # rows that are all padding
     (ConvShape(2, 3, 16, 24, 32, 3, 3, 1, 2, 1, 1, "bf16", True, True), "small_k_gemm"),      # P = 2: two taps off each side
     (ConvShape(2, 3, 21, 16, 32, 1, 1, 2, 0, 1, 1, "bf16", True, True), "small_k_gemm"),      # S > K: row per copy
+    # whole-row stages (one segment per row, H_out a multiple of the rows per stage: copies in closed form)
+    (ConvShape(1, 3, 4, 16, 32, 3, 3, 1, 3, 1, 1, "bf16", True, False), "small_k_gemm"),      # all-padding rows
+    (ConvShape(2, 3, 14, 24, 32, 3, 3, 1, 2, 1, 1, "bf16", True, True), "small_k_gemm"),      # P = 2
+    (ConvShape(2, 3, 16, 24, 64, 3, 3, 2, 1, 1, 1, "bf16", True, True), "small_k_gemm"),      # C_out = 64
 ])
 @pytest.mark.parametrize("sm_pairs", [False, True], ids=["single_sm", "sm_pairs"])
 def test_tensor_core_small_shapes_full(shape, path, sm_pairs):
