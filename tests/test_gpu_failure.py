@@ -34,7 +34,10 @@ def test_plan_status_words_attribute_timeouts():
     wait-timeout check latches its bits: that plan reports them (and clears them), a plan
     with its own word stays clean, and conv_device_status then finds nothing left."""
     import ctypes
-    from cnn_convolution_implicit_gb300 import ConvPlan, device_status, lib
+    import gc
+    from cnn_convolution_implicit_gb300 import ConvPlan, binding, device_status, lib
+    binding._plan_cache.clear()  # plans other tests left alive hold words of the pool
+    gc.collect()
     assert device_status() == 0
     s = ConvShape(2, 128, 13, 11, 256, 3, 3, 1, 1, 1, 1, "bf16", True, True)
     x, w, b = draw(s, (81, 82, 83))
