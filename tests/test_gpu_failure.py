@@ -61,3 +61,26 @@ def test_plan_status_words_attribute_timeouts():
     assert shared.device_status() == 0            # and cleared
     assert device_status() == 0
     del plans, shared
+
+
+def test_block_plan_status_word_in_stream_order():
+    """A fused-block forward on a side stream leaves the block plan's own status word clean,
+    read after that stream's work; the forward's output matches the same plan on the
+    default stream bit for bit."""
+    from cnn_convolution_implicit_gb300 import BlockPlan, device_status
+    assert device_status() == 0
+    g = torch.Generator().manual_seed(91)
+    N, C, H, W, Co = 2, 128, 17, 20, 96
+    plan = BlockPlan(N, C, H, W, Co, 3, 1)
+    x = torch.randn(N, H, W, C, generator=g).cuda()
+    wdw = (torch.randn(C, 3, 3, generator=g) * 0.3).cuda()
+    wpw = (torch.randn(Co, C, generator=g) * 0.1).to(torch.bfloat16).cuda()
+    bias = torch.randn(Co, generator=g).cuda()
+    ref = plan.forward(x, wdw, wpw, pw_bias=bias)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        y = plan.forward(x, wdw, wpw, pw_bias=bias)
+    assert plan.device_status(side) == 0
+    assert torch.equal(y.view(torch.int16).cpu(), ref.view(torch.int16).cpu())
+    assert device_status() == 0
